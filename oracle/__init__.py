@@ -1,0 +1,115 @@
+"""CPU ORACLE -- test infrastructure for the GDN prefill, not part of the product.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package. It shares no code with the CUDA library: the
+token-by-token fp64 recurrence lives in ``gdn_token_loop.c`` (compiled here
+with gcc + OpenMP), and an independent chunked-WY evaluation in numpy lives in
+``chunked_wy.py``.
+
+Parity pins: every function here is checked by ``tests/test_oracle.py``
+against closed forms (pure decay, exact overwrite with orthonormal keys,
+strong decay), exact rational brute force, dense transition-matrix products
+and the chunked evaluation; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from gdn_synth import Problem
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_token_loop.c")
+_LIBDIR = os.path.join(_HERE, "_lib")
+_LIB = os.path.join(_LIBDIR, "libgdn_oracle.so")
+_lock = threading.Lock()
+_handle = None
+
+DT_BF16, DT_F32, DT_F64 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle (gcc -O2 -fopenmp); returns the library path."""
+    os.makedirs(_LIBDIR, exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _lib():
+    global _handle
+    with _lock:
+        if _handle is None:
+            lib = ctypes.CDLL(build())
+            lib.gdn_oracle_run.restype = ctypes.c_int
+            lib.gdn_oracle_max_threads.restype = ctypes.c_int
+            _handle = lib
+    return _handle
+
+
+def max_threads() -> int:
+    return int(_lib().gdn_oracle_max_threads())
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.uint16:
+        return DT_BF16
+    if a.dtype == np.float32:
+        return DT_F32
+    if a.dtype == np.float64:
+        return DT_F64
+    raise TypeError(f"unsupported oracle input dtype {a.dtype}")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def token_loop_raw(q, k, v, g, beta, h0, *, B, T, nk, nv, dk, dv,
+                   cu_seqlens=None, heads=None, threads=0):
+    """Token-by-token fp64 recurrence on raw 2-D row arrays.
+
+    q, k: [rows, >= nk*dk]; v: [rows, >= nv*dv] (bf16 bits, fp32 or fp64);
+    g, beta: [rows, >= nv] (fp32 or fp64); h0: [B, nv, dk, dv] or None.
+    Returns (out [rows, nv, dv] fp64, hT [B, nv, dk, dv] fp64).
+    """
+    q = np.ascontiguousarray(q)
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    g = np.ascontiguousarray(g)
+    beta = np.ascontiguousarray(beta)
+    assert q.dtype == k.dtype == v.dtype and g.dtype == beta.dtype
+    rows = q.shape[0]
+    out = np.zeros((rows, nv, dv))
+    hT = np.zeros((B, nv, dk, dv))
+    h0c = None if h0 is None else np.ascontiguousarray(h0)
+    cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    hs = None if heads is None else np.ascontiguousarray(heads, dtype=np.int32)
+    rc = _lib().gdn_oracle_run(
+        _ptr(q), _ptr(k), _ptr(v), ctypes.c_int(_dtype_code(q)),
+        _ptr(g), _ptr(beta), ctypes.c_int(_dtype_code(g)),
+        _ptr(h0c), ctypes.c_int(_dtype_code(h0c) if h0c is not None else DT_F32),
+        _ptr(out), _ptr(hT),
+        ctypes.c_int(B), ctypes.c_int(T), ctypes.c_int(nk), ctypes.c_int(nv),
+        ctypes.c_int(dk), ctypes.c_int(dv),
+        ctypes.c_int64(q.shape[1]), ctypes.c_int64(k.shape[1]), ctypes.c_int64(v.shape[1]),
+        ctypes.c_int64(g.shape[1]), ctypes.c_int64(beta.shape[1]),
+        _ptr(cu), _ptr(hs), ctypes.c_int(0 if hs is None else len(hs)), ctypes.c_int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle rejected its arguments")
+    return out, hT
+
+
+def token_loop(p: Problem, heads=None, threads=0):
+    """Oracle evaluation of a ``gdn_synth.Problem`` (see ``token_loop_raw``)."""
+    return token_loop_raw(p.q, p.k, p.v, p.g, p.beta, p.h0, B=p.B, T=p.T, nk=p.nk, nv=p.nv,
+                          dk=p.dk, dv=p.dv, cu_seqlens=p.cu_seqlens, heads=heads,
+                          threads=threads)
