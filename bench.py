@@ -1,0 +1,361 @@
+"""Benchmark of the chunked gated-delta-rule prefill on GB300.
+
+Default: N=1, the B=4, T=8192, nk=16, nv=32, dk=dv=128 workload with a carried
+fp32 state (seeded synthetic inputs, resident in HBM before timing). One step
+is one prefill call over the whole batch: every stage of the method (gates,
+WY solve, state spine, output) for all 32,768 tokens x 32 heads.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
+on the host cores instead (a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gdn_synth  # noqa: E402
+
+METRIC = "GDN prefill tokens/s (nv=32,dk=dv=128,T=8192) and % of roofline, 1×GB300"
+FLOP_PER_TOKEN_HEAD = 139_136  # W.S, Kd^T u, Q.S_c, KK^T, solve, QK^T, A.u (dk=dv=128, C=64)
+KERNEL_SOURCES = ["gated_delta_rule_17_gb300/csrc/gdn_chunk_kernel.cuh", "gated_delta_rule_17_gb300/csrc/tc.cuh",
+                  "gated_delta_rule_17_gb300/csrc/gdn_api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_chunk_kernel_traffic.json")
+
+
+def algorithmic_bytes(p) -> int:
+    """Each input read once, each output written once, state read and written."""
+    tokens = p.tokens
+    per_token = 2 * p.nk * p.dk * 2 + p.nv * p.dv * 2 * 2 + p.nv * 8
+    return tokens * per_token + 2 * p.B * p.nv * p.dk * p.dv * 4
+
+
+def algorithmic_flops(p) -> int:
+    return p.tokens * p.nv * FLOP_PER_TOKEN_HEAD
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from an ncu capture, if taken on the current kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_sha") != kernel_sha() or d.get("workload") != workload:
+        return None
+    return d.get("traffic_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class OracleSample:
+    """A bounded sample of the workload for the fp64 CPU oracle, calibrated once
+    so that one timed call takes about ``seconds`` on this host."""
+
+    def __init__(self, p, seconds: float):
+        import oracle
+
+        self.oracle = oracle
+        self.nv = p.nv
+        self.cores = oracle.max_threads()
+        probe = gdn_synth.make_problem(seed=1002, B=1, T=256, nk=p.nk, nv=p.nv, h0_std=0.02)
+        t0 = time.perf_counter()
+        oracle.token_loop(probe, heads=list(range(min(p.nv, max(2, self.cores)))))
+        per_token_head = max(time.perf_counter() - t0, 1e-4) / (256 * min(p.nv, max(2, self.cores)))
+        self.heads = list(range(p.nv))
+        self.tokens = int(max(64, min(8192, seconds / (per_token_head * p.nv))))
+        self.sub = gdn_synth.make_problem(seed=1002, B=1, T=self.tokens, nk=p.nk, nv=p.nv, h0_std=0.02)
+        self.sample = (f"1 sequence x {self.tokens} tokens x all {p.nv} v-heads with the B=4 T=8192 "
+                       f"workload's shapes and distributions; fp64 token loop on {self.cores} threads")
+
+    def run(self):
+        """Returns (tokens/s of the full nv-head workload, seconds)."""
+        t0 = time.perf_counter()
+        self.oracle.token_loop(self.sub, heads=self.heads)
+        dt = time.perf_counter() - t0
+        return self.tokens * len(self.heads) / dt / self.nv, dt
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    p_shape = gdn_synth.config_problem(2, T=64)  # shapes and distributions only
+    per_step = max(1.0, min(args.ref_seconds, 150.0 / (args.warmup + args.steps)))
+    sample = OracleSample(p_shape, per_step)
+    times, rates = [], []
+    for i in range(args.warmup + args.steps):
+        rate, dt = sample.run()
+        if i >= args.warmup:
+            times.append(dt)
+            rates.append(rate)
+    value = statistics.median(rates)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": gdn_synth.CONFIG_NAMES[2] + " (bounded oracle sample per step)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": sample.cores, "kind": "oracle",
+                             "sample": sample.sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    import gated_delta_rule_17_gb300 as gdn
+    from gated_delta_rule_17_gb300 import build as gbuild
+
+    gbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    p = gdn_synth.config_problem(args.config)
+    workload = gdn_synth.CONFIG_NAMES[args.config]
+    from tests.gpu_helpers import DeviceProblem
+
+    dp = DeviceProblem(p, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ws = None
+    if p.varlen:
+        ws = torch.empty(max(gdn.workspace_bytes(p.B, p.T, p.nv, True), 256), dtype=torch.uint8, device=dev)
+
+    def step():
+        dp.run(workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    launches_per_step = gdn.last_launch_count()
+    torch.cuda.synchronize()
+    gdn.check()
+
+    # ---- device-resident timing: K steps between events on the launching stream ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(t_all0.elapsed_time(t_all1), world)
+    per_launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    gdn.check()
+    clocks = clk.summary()
+
+    tokens = p.tokens
+    ms_per_step = total_ms / args.steps
+    value = world * tokens / (ms_per_step / 1e3)
+    hbm_peak, tf_peak, peak_src = measured_peaks()
+    kern_ms = statistics.mean(per_launch_ms)
+    abytes = algorithmic_bytes(p)
+    aflops = algorithmic_flops(p)
+    achieved_gbs = abytes / (kern_ms / 1e3) / 1e9
+    roofline_ms = max(aflops / (tf_peak * 1e12), abytes / (hbm_peak * 1e9)) * 1e3
+
+    # ---- end to end through the public API with host buffers ----------------------
+    host = {}
+    for name in ("q", "k", "v", "g", "beta"):
+        t = getattr(dp, name)
+        host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+    h_state = torch.empty(dp.state.shape, dtype=dp.state.dtype, pin_memory=True).copy_(dp.state)
+    h_out = torch.empty(dp.out.shape, dtype=dp.out.dtype, pin_memory=True)
+    h_state_out = torch.empty_like(h_state)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in host) + h_state.numel() * 4
+    d2h = h_out.numel() * h_out.element_size() + h_state_out.numel() * 4
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        for n in host:
+            getattr(dp, n).copy_(host[n], non_blocking=True)
+        dp.state.copy_(h_state, non_blocking=True)
+        gdn.prefill(dp.q, dp.k, dp.v, dp.g, dp.beta, dp.state, dp.out, nk=p.nk, nv=p.nv, B=p.B, T=p.T,
+                    cu_seqlens=dp.cu, state_is_table=dp.table, workspace=ws)
+        h_out.copy_(dp.out, non_blocking=True)
+        h_state_out.copy_(dp.state, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    barrier(world)
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(p, args.ref_seconds)
+        rate, _ = sample.run()
+        cpu = {"value": rate, "unit": "tokens/s", "cores": sample.cores, "kind": "oracle", "sample": sample.sample}
+    traffic = recorded_traffic(workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 I/O, fp16/bf16 tensor-core operands, fp32 accumulate and state",
+        "data": "synthetic",
+        "config": {"workload": workload, "tokens_per_step": tokens, "l2": "no flush: inputs+outputs "
+                   f"{abytes / 1e6:.0f} MB per step > 129 MB L2", "parallelism": "replicas" if world > 1 else "1 GPU",
+                   "state": "carried from step to step (in place)"},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_peak, "traffic": traffic,
+                     "kernel": "gdn_chunk_kernel", "kernel_ms": kern_ms, "algorithmic_bytes": abytes,
+                     "algorithmic_flops": aflops, "tflops": aflops / (kern_ms / 1e3) / 1e12,
+                     "roofline_ms": roofline_ms, "frac_of_roofline_time": roofline_ms / kern_ms,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
+    ap.add_argument("--config", type=int, default=2, help="workload index (2 = B=4 T=8192 nv=32)")
+    ap.add_argument("--ref-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,163 @@
+"""GB300-native chunked gated-delta-rule (GDN) prefill forward.
+
+A thin ctypes binding over the C ABI in ``include/gdn_prefill.h``; every step
+of the computation runs in the library's CUDA kernels. PyTorch only supplies
+device memory and the current stream. There is no fallback: if the compiled
+library is missing, importing works but every call raises ``GdnError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = ["prefill", "workspace_bytes", "check", "last_launch_count", "lib_path", "load", "GdnError",
+           "Strides", "GDN_OK", "GDN_ERR_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
+           "GDN_ERR_DEVICE_STATUS", "GDN_ERR_TIMEOUT"]
+
+GDN_OK, GDN_ERR_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_STATUS, GDN_ERR_TIMEOUT = range(6)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libgdn_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"gdn error {code}: {message}")
+        self.code = code
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_int64), ("k", ctypes.c_int64), ("v", ctypes.c_int64),
+                ("g", ctypes.c_int64), ("beta", ctypes.c_int64), ("out", ctypes.c_int64),
+                ("state_is_table", ctypes.c_int32)]
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load the compiled library (raises GdnError if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise GdnError(GDN_ERR_UNSUPPORTED, f"CUDA library not built: {_LIB_PATH} is missing "
+                                                    "(run __graft_entry__.build())")
+            lib = ctypes.CDLL(_LIB_PATH)
+            vp, i, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+            common = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, ctypes.POINTER(Strides), vp]
+            lib.gdn_prefill.argtypes = common + [vp]
+            lib.gdn_prefill.restype = i
+            lib.gdn_prefill_ex.argtypes = common + [vp, sz, vp]
+            lib.gdn_prefill_ex.restype = i
+            lib.gdn_prefill_workspace_bytes.argtypes = [i, i, i, i, i, i]
+            lib.gdn_prefill_workspace_bytes.restype = sz
+            lib.gdn_prefill_check.argtypes = [vp]
+            lib.gdn_prefill_check.restype = i
+            lib.gdn_last_error.argtypes = []
+            lib.gdn_last_error.restype = ctypes.c_char_p
+            lib.gdn_last_launch_count.argtypes = []
+            lib.gdn_last_launch_count.restype = i
+            del i64
+            _lib = lib
+    return _lib
+
+
+def _raise(code):
+    msg = load().gdn_last_error().decode(errors="replace")
+    raise GdnError(code, msg)
+
+
+def _row_stride(t, name, inner):
+    """Row stride (elements) of a [rows, ...] tensor whose per-row part is contiguous."""
+    if t.dim() < 2:
+        raise GdnError(GDN_ERR_ARG, f"{name} must be at least 2-D ([rows, ...])")
+    per_row = 1
+    for d in t.shape[1:]:
+        per_row *= d
+    expect = 1
+    for d in range(t.dim() - 1, 0, -1):
+        if t.shape[d] != 1 and t.stride(d) != expect:
+            raise GdnError(GDN_ERR_ARG, f"{name}: the part of each row must be contiguous")
+        expect *= t.shape[d]
+    if per_row < inner:
+        raise GdnError(GDN_ERR_ARG, f"{name}: rows hold {per_row} elements, need {inner}")
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), per_row)
+
+
+def workspace_bytes(B, T, nv, varlen, dk=128, dv=128) -> int:
+    return int(load().gdn_prefill_workspace_bytes(B, T, nv, dk, dv, 1 if varlen else 0))
+
+
+def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = None, T: int | None = None,
+            cu_seqlens=None, state_is_table: bool = False, workspace=None, stream=None, dk: int = 128,
+            dv: int = 128) -> None:
+    """Enqueue one GDN prefill on ``stream`` (default: torch's current stream).
+
+    q, k: bf16 CUDA tensors [rows, nk*dk] (or [rows, nk, dk]); v: bf16 [rows, nv*dv];
+    g, beta: fp32 [rows, nv]; out: bf16 [rows, nv*dv]. ``state``: fp32 CUDA tensor
+    [B, nv, dk, dv] updated in place, or (``state_is_table``) an int64 CUDA tensor of
+    B device addresses of [nv, dk, dv] fp32 states. Dense batches give ``B`` and ``T``
+    (rows = B*T); varlen batches give ``cu_seqlens`` (int32 CUDA [B+1]).
+    ``workspace`` (uint8 CUDA tensor) selects the allocation-free entry point.
+    """
+    import torch
+
+    lib = load()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("g", g, torch.float32), ("beta", beta, torch.float32), ("out", out, torch.bfloat16)):
+        if t.dtype != dt:
+            raise GdnError(GDN_ERR_ARG, f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_cuda:
+            raise GdnError(GDN_ERR_ARG, f"{name} must be a CUDA tensor")
+    rows = q.shape[0]
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise GdnError(GDN_ERR_ARG, "cu_seqlens must be an int32 CUDA tensor")
+        B = cu_seqlens.numel() - 1
+        T = rows
+    elif B is None or T is None:
+        raise GdnError(GDN_ERR_ARG, "dense batches need B and T")
+    st = Strides(_row_stride(q, "q", nk * dk), _row_stride(k, "k", nk * dk), _row_stride(v, "v", nv * dv),
+                 _row_stride(g, "g", nv), _row_stride(beta, "beta", nv), _row_stride(out, "out", nv * dv),
+                 1 if state_is_table else 0)
+    if state_is_table:
+        if state.dtype != torch.int64:
+            raise GdnError(GDN_ERR_ARG, "a state table must be an int64 tensor of device addresses")
+    elif state.dtype != torch.float32 or not state.is_contiguous():
+        raise GdnError(GDN_ERR_ARG, "state must be a contiguous fp32 tensor [B, nv, dk, dv]")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(), state.data_ptr(),
+            out.data_ptr(), B, T, nk, nv, dk, dv, ctypes.byref(st),
+            None if cu_seqlens is None else cu_seqlens.data_ptr()]
+    if workspace is None:
+        rc = lib.gdn_prefill(*args, stream)
+    else:
+        rc = lib.gdn_prefill_ex(*args, workspace.data_ptr() if workspace.numel() else None,
+                                workspace.numel() * workspace.element_size(), stream)
+    if rc != GDN_OK:
+        _raise(rc)
+
+
+def check(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel reported a device-side error."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = load().gdn_prefill_check(stream)
+    if rc != GDN_OK:
+        _raise(rc)
+
+
+def last_launch_count() -> int:
+    return int(load().gdn_last_launch_count())

@@ -1,0 +1,131 @@
+/*
+ * gdn_prefill.h -- C ABI of the GB300 (sm_103a) chunked gated-delta-rule
+ * prefill forward.
+ *
+ * The operation (GDN prefill op, ssm_gdn_a3.rs, doc comment and problem
+ * arguments of `gdn_prefill_fla`): for every sequence s and value head h,
+ * with key/query head kh = h / (nv / nk), run the recurrence
+ *
+ *     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = S_t^T q_t / sqrt(dk)
+ *
+ * over the tokens of s, starting from the carried-in state S_0 = h_state[s][h]
+ * and leaving S_T there. It is evaluated in chunks of 64 tokens in WY form:
+ * a per-chunk triangular solve (the op's recompute_wu stage), a serial state
+ * spine over chunks (its chunk_delta_h stage) and the chunk-parallel output
+ * (its chunk_fwd_o stage). Here the three stages run inside one kernel per
+ * (sequence, v-head, v-column slice), so the stage hand-offs stay on chip.
+ *
+ * All entry points are plain C; pointers marked "device" are CUDA device
+ * (or managed) addresses on the current device, `stream` is a cudaStream_t
+ * passed as void* (NULL = legacy default stream).
+ */
+#ifndef GDN_PREFILL_H
+#define GDN_PREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. Host-detectable errors launch nothing. */
+enum {
+  GDN_OK = 0,
+  GDN_ERR_ARG = 1,           /* a NULL pointer, a negative size, a bad stride or alignment */
+  GDN_ERR_UNSUPPORTED = 2,   /* dk/dv other than 128, nv not a multiple of nk, no sm_103 device */
+  GDN_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (message names it) */
+  GDN_ERR_DEVICE_STATUS = 4, /* a kernel found malformed cu_seqlens (reported by gdn_prefill_check) */
+  GDN_ERR_TIMEOUT = 5        /* a bounded on-device wait expired (reported by gdn_prefill_check) */
+};
+
+/*
+ * Row strides, in elements, between consecutive token rows of each tensor
+ * (the op's qk_stride / v_stride / gb_stride arguments; the packed conv layout
+ * uses qk_stride = v_stride = conv width and a g/beta stride of 2*nv).
+ *   q, k : bf16 elements; multiple of 8 (16-byte rows for TMA); >= nk*dk
+ *   v    : bf16 elements; multiple of 8; >= nv*dv
+ *   g, beta : fp32 elements; >= nv
+ *   out  : bf16 elements; multiple of 8; >= nv*dv
+ *   state_is_table : 0 -> h_state_inout is float[B][nv][dk][dv];
+ *                    1 -> h_state_inout is a device array of B device
+ *                         pointers, each to one float[nv][dk][dv]
+ * Passing NULL for the struct means packed rows (q = k = nk*dk, v = out =
+ * nv*dv, g = beta = nv) and a contiguous state.
+ */
+typedef struct {
+  int64_t q, k, v;
+  int64_t g, beta;
+  int64_t out;
+  int32_t state_is_table;
+} gdn_strides_t;
+
+/*
+ * Enqueue the prefill on `stream` and return; no host synchronisation.
+ *
+ *   q, k    : device bf16, row r holds nk heads of dk values (head kh at
+ *             column kh*dk); rows are already L2-normalised by the caller.
+ *   v       : device bf16, row r holds nv heads of dv values.
+ *   g       : device fp32 log-decay per (row, v-head), finite and <= 0
+ *             (exp(g) is the decay; -inf is not supported).
+ *   beta    : device fp32 write strength per (row, v-head), in [0, 1].
+ *   h_state_inout : device fp32 state, see state_is_table; read as S_0 and
+ *             overwritten with S_T of each sequence, k-major ([dk][dv]).
+ *   out     : device bf16 [rows][nv][dv] at row stride strides->out;
+ *             every row of every sequence is written, nothing else.
+ *   B, T    : dense (cu_seqlens == NULL): B sequences of T tokens, row
+ *             r = b*T + t. Varlen: B sequences packed into T rows in total,
+ *             sequence s owns rows [cu_seqlens[s], cu_seqlens[s+1]).
+ *   nk, nv  : key/query and value head counts, nv % nk == 0; v-head h reads
+ *             q/k head h / (nv / nk).
+ *   dk, dv  : must both be 128.
+ *   cu_seqlens : device int32 [B+1] (non-decreasing, cu[0] = 0, cu[B] = T)
+ *             or NULL. Malformed offsets are detected on the device: the
+ *             affected sequences write nothing and gdn_prefill_check reports
+ *             GDN_ERR_DEVICE_STATUS.
+ *   stream  : cudaStream_t as void*.
+ * Numerics: products run on the tensor cores with fp16 operands and fp32
+ * accumulation; the state is carried in fp32. Inputs must keep |v|, |S| and
+ * intermediate values inside the fp16 range (about 6.5e4).
+ * Allocation: needs gdn_prefill_workspace_bytes() of device scratch, which
+ * this call allocates and frees stream-ordered (cudaMallocAsync /
+ * cudaFreeAsync); use gdn_prefill_ex to supply it instead.
+ * Buffers are owned by the caller and must stay valid until the stream
+ * reaches the end of this work. q/k/v/out must be 16-byte aligned.
+ */
+int gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
+                const gdn_strides_t* strides, const int32_t* cu_seqlens, void* stream);
+
+/* Bytes of device scratch gdn_prefill_ex needs for these sizes (0 for dense
+ * batches; a per-sequence schedule for varlen ones). */
+size_t gdn_prefill_workspace_bytes(int B, int T, int nv, int dk, int dv, int varlen);
+
+/* gdn_prefill with caller-provided scratch: `workspace` is a device buffer
+ * of at least gdn_prefill_workspace_bytes(...) bytes (may be NULL when that
+ * is 0), 256-byte aligned, not used by other work until the stream passes
+ * this call. Allocates nothing. */
+int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                   void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
+                   const gdn_strides_t* strides, const int32_t* cu_seqlens, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the current device's status word
+ * that kernels set on malformed cu_seqlens (GDN_ERR_DEVICE_STATUS) or on an
+ * expired bounded wait (GDN_ERR_TIMEOUT). The word is shared by all calls on
+ * the device since the last check. */
+int gdn_prefill_check(void* stream);
+
+/* Message for the last error returned on the calling thread, naming the
+ * argument or guard that rejected the call ("" after success). */
+const char* gdn_last_error(void);
+
+/* Number of kernel launches the last successful call on this thread enqueued. */
+int gdn_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_PREFILL_H */

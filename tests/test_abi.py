@@ -1,0 +1,132 @@
+"""C ABI checks that need no GPU: the library builds for sm_103a, loads, and
+exports every function the header declares; host-side validation rejects bad
+arguments with named reasons before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn_prefill.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_17_gb300 import build
+
+    build.build()
+    import gated_delta_rule_17_gb300 as gdn
+
+    return gdn.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(gdn_[a-z_0-9]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("gdn_prefill", "gdn_prefill_ex", "gdn_prefill_workspace_bytes", "gdn_prefill_check",
+              "gdn_last_error", "gdn_last_launch_count"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_no_cpu_fallback_symbols(lib):
+    # the library is CUDA-only: its product path links nothing from oracle/
+    data = open(lib._name, "rb").read()
+    assert b"gdn_oracle_run" not in data
+
+
+def _call(lib, B=1, T=64, nk=1, nv=1, dk=128, dv=128, strides=None, ptr=16, cu=None):
+    import gated_delta_rule_17_gb300 as gdn
+
+    p = ctypes.c_void_p(ptr) if ptr else None
+    st = ctypes.byref(strides) if strides is not None else None
+    rc = lib.gdn_prefill(p, p, p, p, p, p, p, B, T, nk, nv, dk, dv, st, cu, None)
+    return rc, lib.gdn_last_error().decode()
+
+
+def test_rejects_head_dims(lib):
+    import gated_delta_rule_17_gb300 as gdn
+
+    rc, msg = _call(lib, dk=64)
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "128" in msg
+
+
+def test_rejects_gqa_mismatch(lib):
+    import gated_delta_rule_17_gb300 as gdn
+
+    rc, msg = _call(lib, nk=3, nv=4)
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "multiple of nk" in msg
+
+
+def test_rejects_negative_sizes(lib):
+    import gated_delta_rule_17_gb300 as gdn
+
+    assert _call(lib, B=-1)[0] == gdn.GDN_ERR_ARG
+    assert _call(lib, T=-5)[0] == gdn.GDN_ERR_ARG
+    assert _call(lib, nk=0)[0] == gdn.GDN_ERR_ARG
+
+
+def test_rejects_null_and_misaligned_pointers(lib):
+    import gated_delta_rule_17_gb300 as gdn
+
+    rc, msg = _call(lib, ptr=0)
+    assert rc == gdn.GDN_ERR_ARG and "NULL" in msg
+    rc, msg = _call(lib, ptr=18)
+    assert rc == gdn.GDN_ERR_ARG and "aligned" in msg
+
+
+def test_rejects_bad_strides(lib):
+    import gated_delta_rule_17_gb300 as gdn
+
+    st = gdn.Strides(132, 128, 128, 1, 1, 128, 0)  # q stride not a multiple of 8
+    rc, msg = _call(lib, strides=st)
+    assert rc == gdn.GDN_ERR_ARG and "q row stride" in msg
+    st = gdn.Strides(128, 128, 64, 1, 1, 128, 0)  # v stride below nv*dv
+    rc, msg = _call(lib, strides=st)
+    assert rc == gdn.GDN_ERR_ARG and "v row stride" in msg
+    st = gdn.Strides(128, 128, 128, 0, 1, 128, 0)  # g stride below nv
+    assert _call(lib, strides=st)[0] == gdn.GDN_ERR_ARG
+    st = gdn.Strides(128, 128, 128, 1, 1, 128, 2)  # bad table flag
+    assert _call(lib, strides=st)[0] == gdn.GDN_ERR_ARG
+
+
+def test_empty_problem_is_a_no_op(lib):
+    import gated_delta_rule_17_gb300 as gdn
+
+    assert _call(lib, B=0, ptr=0)[0] == gdn.GDN_OK
+    assert lib.gdn_last_launch_count() == 0
+    assert _call(lib, T=0, ptr=0)[0] == gdn.GDN_OK
+
+
+def test_workspace_sizes(lib):
+    assert lib.gdn_prefill_workspace_bytes(4, 8192, 32, 128, 128, 0) == 0
+    assert lib.gdn_prefill_workspace_bytes(8, 64000, 48, 128, 128, 1) == 256
+    assert lib.gdn_prefill_workspace_bytes(100, 64000, 48, 128, 128, 1) == 512
+
+
+def test_ex_rejects_small_workspace(lib):
+    import gated_delta_rule_17_gb300 as gdn
+
+    p = ctypes.c_void_p(256)
+    cu = ctypes.c_void_p(512)
+    rc = lib.gdn_prefill_ex(p, p, p, p, p, p, p, 4, 100, 1, 1, 128, 128, None, cu, p, 8, None)
+    assert rc == gdn.GDN_ERR_ARG and "workspace" in lib.gdn_last_error().decode()
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import gated_delta_rule_17_gb300 as gdn
+
+    monkeypatch.setattr(gdn, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(gdn, "_lib", None)
+    with pytest.raises(gdn.GdnError):
+        gdn.load()

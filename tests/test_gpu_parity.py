@@ -1,0 +1,202 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs, at the five specified workloads and at edge cases."""
+import numpy as np
+import pytest
+
+import gdn_synth
+import oracle
+from tests.gpu_helpers import DeviceProblem, assert_parity, compare
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_delta_rule_17_gb300 import build
+
+    build.build()
+    oracle.build()
+
+
+def run_and_check(p, heads=None, label="", **dp_kw):
+    dp = DeviceProblem(p, **dp_kw)
+    dp.run()
+    torch.cuda.synchronize()
+    import gated_delta_rule_17_gb300 as gdn
+
+    gdn.check()
+    o_ref, s_ref = oracle.token_loop(p, heads=heads)
+    o, s = dp.out_np(), dp.state_np()
+    res = assert_parity(o, s, o_ref, s_ref, heads=heads, label=label or p.name)
+    return dp, o, s, res
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_config_full_parity(cfg):
+    p = gdn_synth.config_problem(cfg)
+    dp, o, s, _ = run_and_check(p, label=f"config {cfg}")
+    assert np.isfinite(o).all()
+
+
+def test_config2_full_size_sampled_heads():
+    # B=4 T=8192 nk=16 nv=32 with a N(0,0.02) carried state, the benchmarked launch
+    p = gdn_synth.config_problem(2)
+    heads = [0, 1, 13, 31]
+    dp, o, s, _ = run_and_check(p, heads=heads, label="config 2")
+    assert np.isfinite(o).all() and np.isfinite(s).all()
+
+
+def test_config3_varlen_state_table_sampled_heads():
+    p = gdn_synth.config_problem(3)
+    assert p.meta["state_table"]
+    heads = [0, 7, 47]
+    run_and_check(p, heads=heads, label="config 3")
+
+
+def test_config4_long_context_sampled_heads():
+    p = gdn_synth.config_problem(4)
+    run_and_check(p, heads=[3, 30], label="config 4")
+
+
+@pytest.mark.parametrize("gate", ["zero", "weak"])
+def test_weak_decay_cross_chunk_path(gate):
+    # with g = 0 or a very weak decay the state carried across chunks dominates
+    kw = dict(gate_zero=True) if gate == "zero" else dict(gate_mu=-5.0, gate_sigma=0.5)
+    p = gdn_synth.make_problem(seed=2001, B=1, T=4096, nk=16, nv=32, h0_std=0.02, **kw)
+    run_and_check(p, label=f"weak decay {gate}")
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 200])
+def test_ragged_tail_dense(T):
+    p = gdn_synth.make_problem(seed=3000 + T, B=2, T=T, nk=1, nv=2, h0_std=0.02)
+    run_and_check(p, label=f"dense T={T}")
+
+
+def test_wide_batch_uses_full_width_slices():
+    # B*nv above half the SM count selects the 128-column slice per CTA
+    p = gdn_synth.make_problem(seed=3100, B=3, T=130, nk=16, nv=32, h0_std=0.02)
+    run_and_check(p, heads=[0, 17, 31], label="wide batch")
+
+
+def test_varlen_edge_lengths_packed_strides():
+    # empty and 1-token sequences, exact multiples of 64, padded rows, g/beta at 2*nv
+    lens = [0, 1, 64, 65, 130, 0, 7]
+    p = gdn_synth.make_problem(seed=3200, B=len(lens), lengths=lens, nk=2, nv=4, h0_std=0.02,
+                               pad_qk=8, pad_v=16, gb_stride=8)
+    dp, o, s, _ = run_and_check(p, label="varlen edges", out_pad=24)
+    # the padding columns of out are never written
+    pad = dp.out[:, p.nv * p.dv:].float()
+    assert torch.isnan(pad).all()
+    # empty sequences keep their state exactly
+    for sidx, n in enumerate(lens):
+        if n == 0:
+            assert np.array_equal(s[sidx], p.h0[sidx].astype(np.float64))
+
+
+def test_bitwise_deterministic():
+    p = gdn_synth.config_problem(1)
+    dp = DeviceProblem(p)
+    dp.run()
+    a_out, a_st = dp.out.clone(), dp.state.clone()
+    dp.reset()
+    dp.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a_out.view(torch.int16), dp.out.view(torch.int16))
+    assert torch.equal(a_st, dp.state)
+
+
+def test_split_sequence_carry():
+    # T1 (not a multiple of 64) then T2 with the carried state == T1 + T2 at once
+    T1, T2 = 100, 157
+    p = gdn_synth.make_problem(seed=3300, B=1, T=T1 + T2, nk=2, nv=4, h0_std=0.02, gate_mu=-4.0,
+                               gate_sigma=0.5)
+    whole = DeviceProblem(p)
+    whole.run()
+    first = gdn_synth.make_problem(seed=3300, B=1, T=T1 + T2, nk=2, nv=4, h0_std=0.02, gate_mu=-4.0,
+                                   gate_sigma=0.5)
+    for name in ("q", "k", "v", "g", "beta"):
+        setattr(first, name, getattr(p, name)[:T1])
+    first.T = T1
+    second = gdn_synth.make_problem(seed=3300, B=1, T=T1 + T2, nk=2, nv=4, h0_std=0.02, gate_mu=-4.0,
+                                    gate_sigma=0.5)
+    for name in ("q", "k", "v", "g", "beta"):
+        setattr(second, name, getattr(p, name)[T1:])
+    second.T = T2
+    a = DeviceProblem(first)
+    a.run()
+    torch.cuda.synchronize()
+    second.h0 = a.state.cpu().numpy()
+    b = DeviceProblem(second)
+    b.run()
+    torch.cuda.synchronize()
+    o_split = np.concatenate([a.out_np(), b.out_np()])
+    o_ref, s_ref = oracle.token_loop(p)
+    assert_parity(o_split, b.state_np(), o_ref, s_ref, label="split carry")
+    out_rel, _, st_rel = compare(o_split, b.state_np(), whole.out_np(), whole.state_np())
+    assert out_rel < 1e-2 and st_rel < 1e-3
+
+
+def test_gqa_duplication_bitwise():
+    p = gdn_synth.make_problem(seed=3400, B=1, T=300, nk=2, nv=4, h0_std=0.02)
+    dup = gdn_synth.make_problem(seed=3400, B=1, T=300, nk=4, nv=4, h0_std=0.02)
+    for name in ("q", "k"):
+        src = getattr(p, name).reshape(p.rows, 2, 128)
+        setattr(dup, name, np.repeat(src, 2, axis=1).reshape(p.rows, 4 * 128).copy())
+    dup.v, dup.g, dup.beta, dup.h0 = p.v, p.g, p.beta, p.h0
+    a, b = DeviceProblem(p), DeviceProblem(dup)
+    a.run()
+    b.run()
+    torch.cuda.synchronize()
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+    assert torch.equal(a.state, b.state)
+
+
+def test_malformed_cu_seqlens_reported_and_recoverable():
+    import gated_delta_rule_17_gb300 as gdn
+
+    p = gdn_synth.make_problem(seed=3500, B=3, lengths=[10, 20, 30], nk=1, nv=2)
+    dp = DeviceProblem(p)
+    dp.cu = torch.tensor([0, 25, 20, 60], dtype=torch.int32, device="cuda")  # decreasing offset
+    dp.run()
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.check()
+    assert ei.value.code == gdn.GDN_ERR_DEVICE_STATUS
+    # the status word was cleared and the library keeps working
+    good = DeviceProblem(p)
+    good.run()
+    gdn.check()
+    o_ref, s_ref = oracle.token_loop(p)
+    assert_parity(good.out_np(), good.state_np(), o_ref, s_ref, label="after bad call")
+
+
+def test_workspace_entry_point_and_launch_count():
+    import gated_delta_rule_17_gb300 as gdn
+
+    p = gdn_synth.make_problem(seed=3600, B=3, lengths=[100, 5, 300], nk=2, nv=4, h0_std=0.02)
+    dp = DeviceProblem(p)
+    nbytes = gdn.workspace_bytes(p.B, p.T, p.nv, varlen=True)
+    assert nbytes >= 4 * p.B
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dp.run(workspace=ws)
+    assert gdn.last_launch_count() == 2
+    gdn.check()
+    o_ref, s_ref = oracle.token_loop(p)
+    assert_parity(dp.out_np(), dp.state_np(), o_ref, s_ref, label="workspace entry point")
+    dense = DeviceProblem(gdn_synth.make_problem(seed=3601, B=1, T=70, nk=1, nv=1))
+    dense.run()
+    assert gdn.last_launch_count() == 1
+
+
+def test_host_validation_rejects_before_launch():
+    import gated_delta_rule_17_gb300 as gdn
+
+    p = gdn_synth.make_problem(seed=3700, B=1, T=64, nk=2, nv=4)
+    dp = DeviceProblem(p)
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.prefill(dp.q, dp.k, dp.v, dp.g, dp.beta, dp.state, dp.out, nk=2, nv=3, B=1, T=64)
+    assert ei.value.code == gdn.GDN_ERR_UNSUPPORTED and "multiple" in str(ei.value)
+    with pytest.raises(gdn.GdnError):
+        gdn.prefill(dp.q, dp.k, dp.v, dp.g.double(), dp.beta, dp.state, dp.out, nk=2, nv=4, B=1, T=64)
