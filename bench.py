@@ -30,7 +30,7 @@ METRIC = "GDN prefill tokens/s (nv=32,dk=dv=128,T=8192) and % of roofline, 1×GB
 FLOP_PER_TOKEN_HEAD = 139_136  # W.S, Kd^T u, Q.S_c, KK^T, solve, QK^T, A.u (dk=dv=128, C=64)
 KERNEL_SOURCES = ["gated_delta_rule_17_gb300/csrc/gdn_chunk_kernel.cuh", "gated_delta_rule_17_gb300/csrc/tc.cuh",
                   "gated_delta_rule_17_gb300/csrc/gdn_api.cu"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_chunk_kernel_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_chunk_kernel_B4_T8192_nv32_full.md")
 
 
 def algorithmic_bytes(p) -> int:
@@ -62,15 +62,17 @@ def measured_peaks():
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch from an ncu capture, if taken on the current kernel source."""
+    """DRAM bytes per launch from the committed ncu summary, if it was captured on
+    the current kernel source and this workload (else None)."""
     try:
         with open(TRAFFIC_FILE) as fh:
-            d = json.load(fh)
-    except (OSError, ValueError):
+            fields = dict(line.split(": ", 1) for line in fh.read().splitlines() if ": " in line
+                          and line.split(": ", 1)[0] in ("traffic_bytes_per_launch", "kernel_sha", "workload"))
+    except OSError:
         return None
-    if d.get("kernel_sha") != kernel_sha() or d.get("workload") != workload:
+    if fields.get("kernel_sha") != kernel_sha() or fields.get("workload") != workload:
         return None
-    return d.get("traffic_bytes_per_launch")
+    return int(fields["traffic_bytes_per_launch"])
 
 
 class ClockSampler:

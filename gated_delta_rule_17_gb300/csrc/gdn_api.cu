@@ -15,7 +15,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/gdn_prefill.h"
+#include "gdn_prefill.h"
 #include "gdn_chunk_kernel.cuh"
 
 namespace {
