@@ -11,11 +11,12 @@ import ctypes
 import os
 import threading
 
-__all__ = ["prefill", "workspace_bytes", "check", "last_launch_count", "lib_path", "load", "GdnError",
+__all__ = ["prefill", "prefill_noalloc", "NOALLOC_MAX_SEQS", "workspace_bytes", "check", "last_launch_count", "lib_path", "load", "GdnError",
            "Strides", "GDN_OK", "GDN_ERR_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
            "GDN_ERR_DEVICE_STATUS", "GDN_ERR_TIMEOUT"]
 
 GDN_OK, GDN_ERR_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_STATUS, GDN_ERR_TIMEOUT = range(6)
+NOALLOC_MAX_SEQS = 16384  # GDN_NOALLOC_MAX_SEQS in include/gdn_prefill.h
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libgdn_gb300.so")
@@ -62,6 +63,8 @@ def load():
             lib.gdn_last_error.restype = ctypes.c_char_p
             lib.gdn_last_launch_count.argtypes = []
             lib.gdn_last_launch_count.restype = i
+            lib.gdn_prefill_noalloc.argtypes = common + [vp]
+            lib.gdn_prefill_noalloc.restype = i
             del i64
             _lib = lib
     return _lib
@@ -103,7 +106,7 @@ def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = N
     [B, nv, dk, dv] updated in place, or (``state_is_table``) an int64 CUDA tensor of
     B device addresses of [nv, dk, dv] fp32 states. Dense batches give ``B`` and ``T``
     (rows = B*T); varlen batches give ``cu_seqlens`` (int32 CUDA [B+1]).
-    ``workspace`` (uint8 CUDA tensor) selects the allocation-free entry point.
+    ``workspace`` (uint8 CUDA tensor) passes caller-provided scratch (``gdn_prefill_ex``).
     """
     import torch
 
@@ -142,6 +145,35 @@ def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = N
     else:
         rc = lib.gdn_prefill_ex(*args, workspace.data_ptr() if workspace.numel() else None,
                                 workspace.numel() * workspace.element_size(), stream)
+    if rc != GDN_OK:
+        _raise(rc)
+
+
+def prefill_noalloc(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = None,
+                    T: int | None = None, cu_seqlens=None, state_is_table: bool = False, stream=None,
+                    dk: int = 128, dv: int = 128) -> None:
+    """``prefill`` through ``gdn_prefill_noalloc``: the library allocates no device
+    memory during the call (its varlen schedule lives in a static device array of
+    ``NOALLOC_MAX_SEQS`` entries). For callers that cannot allocate mid-call.
+    Calls that overlap on the GPU race on that shared array."""
+    import torch
+
+    lib = load()
+    if cu_seqlens is not None:
+        B = cu_seqlens.numel() - 1
+        T = q.shape[0]
+    elif B is None or T is None:
+        raise GdnError(GDN_ERR_ARG, "dense batches need B and T")
+    st = Strides(_row_stride(q, "q", nk * dk), _row_stride(k, "k", nk * dk), _row_stride(v, "v", nv * dv),
+                 _row_stride(g, "g", nv), _row_stride(beta, "beta", nv), _row_stride(out, "out", nv * dv),
+                 1 if state_is_table else 0)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = lib.gdn_prefill_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(),
+                                 state.data_ptr(), out.data_ptr(), B, T, nk, nv, dk, dv, ctypes.byref(st),
+                                 None if cu_seqlens is None else cu_seqlens.data_ptr(), stream)
     if rc != GDN_OK:
         _raise(rc)
 

@@ -204,6 +204,33 @@ size_t workspace_bytes(int B, int varlen) {
   return (static_cast<size_t>(B) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
 }
 
+// ---- allocation-free entry point -------------------------------------------------
+// Scratch for gdn_prefill_noalloc: the varlen schedule (one int32 per
+// sequence) lives in this file-scope device array instead of a workspace.
+// Every GPU that loads the library holds it until the process exits.
+constexpr int kNoAllocMaxSeqs = GDN_NOALLOC_MAX_SEQS;
+static __device__ __align__(256) int32_t g_noalloc_order[kNoAllocMaxSeqs];
+int32_t* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_order on the current device, looked up once
+// per device. In host code the array's name only stands in for the symbol;
+// the kernel must be given the address cudaGetSymbolAddress returns.
+int noalloc_scratch(int32_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(GDN_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_order);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress(schedule scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -255,6 +282,25 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
     if (e != cudaSuccess && rc == GDN_OK) rc = fail(GDN_ERR_CUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
   }
   return rc;
+}
+
+int gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
+                        const gdn_strides_t* strides, const int32_t* cu_seqlens, void* stream) {
+  g_err[0] = 0;
+  g_launches = 0;
+  Resolved r;
+  if (int rc = validate(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, dk, dv, strides, &r)) return rc;
+  if (B == 0 || T == 0) return GDN_OK;
+  int32_t* order = nullptr;
+  if (cu_seqlens) {
+    if (B > kNoAllocMaxSeqs)
+      return fail(GDN_ERR_UNSUPPORTED, "gdn_prefill_noalloc handles at most %d sequences per varlen call, got B = %d",
+                  kNoAllocMaxSeqs, B);
+    if (int rc = noalloc_scratch(&order)) return rc;
+  }
+  return launch(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, r, cu_seqlens, order,
+                static_cast<cudaStream_t>(stream));
 }
 
 int gdn_prefill_check(void* stream) {

@@ -111,6 +111,27 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
                    const gdn_strides_t* strides, const int32_t* cu_seqlens, void* workspace,
                    size_t workspace_bytes, void* stream);
 
+/* Allocation-free variant of gdn_prefill for callers that cannot allocate
+ * device memory during the call -- for example a serving process whose
+ * device memory is reserved up front by its own allocator, or a latency
+ * bound loop where a cudaMalloc could block or fail. It has no counterpart
+ * in the GDN prefill op; it exists only so those callers can use the library.
+ * Same arguments and semantics as gdn_prefill. The varlen schedule it needs
+ * lives in a static device array of GDN_NOALLOC_MAX_SEQS int32 entries (64
+ * KiB) that each GPU holds from library load until process exit; varlen
+ * calls with B > GDN_NOALLOC_MAX_SEQS return GDN_ERR_UNSUPPORTED, dense
+ * calls have no limit. It calls no cudaMalloc, cudaFree or other allocating
+ * routine. The first call on a device looks up that array's device address
+ * (cudaGetSymbolAddress) with the device current; make that first call
+ * before any stream capture. All calls on a device share the one array and
+ * it keeps the last call's contents (every entry a call uses is rewritten
+ * by that call): calls that overlap on the GPU, e.g. on two streams, race on
+ * it and must be serialised by the caller. */
+#define GDN_NOALLOC_MAX_SEQS 16384
+int gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                        void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
+                        const gdn_strides_t* strides, const int32_t* cu_seqlens, void* stream);
+
 /* Synchronise `stream`, then read and clear the current device's status word
  * that kernels set on malformed cu_seqlens (GDN_ERR_DEVICE_STATUS) or on an
  * expired bounded wait (GDN_ERR_TIMEOUT). The word is shared by all calls on
