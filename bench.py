@@ -28,7 +28,7 @@ import gdn_synth  # noqa: E402
 
 METRIC = "GDN prefill tokens/s (nv=32,dk=dv=128,T=8192) and % of roofline, 1×GB300"
 FLOP_PER_TOKEN_HEAD = 139_136  # W.S, Kd^T u, Q.S_c, KK^T, solve, QK^T, A.u (dk=dv=128, C=64)
-KERNEL_SOURCES = ["gated_delta_rule_17_gb300/csrc/gdn_chunk_kernel.cuh", "gated_delta_rule_17_gb300/csrc/tc.cuh",
+KERNEL_SOURCES = ["gated_delta_rule_17_gb300/csrc/gdn_prefill_kernel.cuh", "gated_delta_rule_17_gb300/csrc/tc.cuh",
                   "gated_delta_rule_17_gb300/csrc/gdn_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gdn_chunk_kernel_B4_T8192_nv32_full.md")
 
@@ -323,7 +323,7 @@ def run_gpu(args, world, rank, local):
                    "state": "carried from step to step (in place)"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved_gbs / hbm_peak, "traffic": traffic,
-                     "kernel": "gdn_chunk_kernel", "kernel_ms": kern_ms, "algorithmic_bytes": abytes,
+                     "kernel": "gdn_prefill_kernel", "kernel_ms": kern_ms, "algorithmic_bytes": abytes,
                      "algorithmic_flops": aflops, "tflops": aflops / (kern_ms / 1e3) / 1e12,
                      "roofline_ms": roofline_ms, "frac_of_roofline_time": roofline_ms / kern_ms,
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"},

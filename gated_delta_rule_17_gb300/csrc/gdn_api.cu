@@ -16,7 +16,7 @@
 #include <mutex>
 
 #include "gdn_prefill.h"
-#include "gdn_chunk_kernel.cuh"
+#include "gdn_prefill_kernel.cuh"
 
 namespace {
 
@@ -72,11 +72,8 @@ int device_info(DeviceInfo** out) {
     if (major != 10 || minor != 3)
       return fail(GDN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    e = cudaFuncSetAttribute(gdn::gdn_chunk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gdn::Plan<128>::DYN_SMEM);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gdn::gdn_chunk_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               gdn::Plan<64>::DYN_SMEM);
+    e = cudaFuncSetAttribute(gdn::gdn_prefill_kernel<>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gdn::Plan::DYN_SMEM);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
@@ -182,16 +179,11 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
     gdn_schedule_kernel<<<(B + 255) / 256, 256, 0, stream>>>(cu, B, T, order, d->status);
     ++launches;
   }
-  // v-column slices: split each head's 128 state columns in two when a
-  // 128-column CTA per (sequence, head) would leave over half the SMs idle.
-  const int64_t chains = static_cast<int64_t>(B) * nv;
-  const bool split = chains * 2 <= d->sms;
-  const int64_t grid = chains * (split ? 2 : 1);
+  // one CTA per (sequence, v-head); CTAs of the same sequence and GQA group are
+  // adjacent so their shared q/k tiles meet in L2
+  const int64_t grid = static_cast<int64_t>(B) * nv;
   if (grid > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "grid of %lld CTAs too large", (long long)grid);
-  if (split)
-    gdn::gdn_chunk_kernel<64><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan<64>::DYN_SMEM, stream>>>(mq, mk, mv, p);
-  else
-    gdn::gdn_chunk_kernel<128><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan<128>::DYN_SMEM, stream>>>(mq, mk, mv, p);
+  gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, p);
   ++launches;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));

@@ -69,6 +69,15 @@ def test_weak_decay_cross_chunk_path(gate):
     run_and_check(p, label=f"weak decay {gate}")
 
 
+def test_strong_decay_wide_gate_range():
+    # g ~ -softplus(N(3,1)) spans > 120 nats within a chunk: the kernel then
+    # evaluates every decay e^{gc_i - gc_j} directly instead of factorising it
+    p = gdn_synth.make_problem(seed=2100, B=2, T=300, nk=2, nv=4, h0_std=0.02, gate_mu=3.0)
+    gc_range = -p.g[:64, 0].astype(np.float64).sum()
+    assert gc_range > 120
+    run_and_check(p, label="wide gate range")
+
+
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 200])
 def test_ragged_tail_dense(T):
     p = gdn_synth.make_problem(seed=3000 + T, B=2, T=T, nk=1, nv=2, h0_std=0.02)
