@@ -48,6 +48,8 @@ constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr uint32_t kBarProducer = 1;  // named barrier ids
 constexpr uint32_t kBarConsumer = 2;
+constexpr uint32_t kBarCrewX = 3;     // producer crew X (warps 0-3 of the producer)
+constexpr int kCrewThreads = kProducerThreads / 2;
 
 // Status bits written to the per-device status word.
 constexpr unsigned kStatusBadSeqlens = 1u;
@@ -195,6 +197,9 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
   const int quad = pw & 3;   // tensor-memory lane quarter of this warp
   const int half = pw >> 2;  // which half of a 64-column accumulator it reads
   const bool leader = ptid == 0;
+  const bool crew_x = pw < 4;                  // crews X and Y each hold one warp per sub-partition
+  const int cx = (pw & 3) * 32 + lane;         // thread index within its crew
+  const int cy = cx;
   uint8_t* sm = x.sm;
   float* lf = reinterpret_cast<float*>(sm + P::LF);
   float* lt = reinterpret_cast<float*>(sm + P::LT);
@@ -241,7 +246,11 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     issue_v(0);
     if (x.nchunks > 1) issue_kq(1);
   }
-  if (pw == 0) load_gates(0);
+  if (pw == 4) {  // crew Y stages the gates; the join barrier publishes them
+    load_gates(0);
+    tc::cp_async_wait_all();
+  }
+  tc::named_barrier(kBarProducer, kProducerThreads);
 
   for (int c = 0; c < x.nchunks; ++c) {
     const int b = c & 1;
@@ -252,7 +261,6 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 
     // ---- gates: in-chunk cumulative log-gate and the per-token scales ----------------
     if (pw == 0) {
-      tc::cp_async_wait_all();
       const float* st = x.s_gstage + b * 128;
       const float g0 = st[2 * lane], g1 = st[2 * lane + 1];
       const float b0 = st[64 + 2 * lane], b1 = st[64 + 2 * lane + 1];
@@ -288,7 +296,6 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         x.s_elast[b] = __expf(glast);
         *x.s_fast = (gfirst - glast) <= 120.f;
       }
-      if (c + 1 < x.nchunks) load_gates(c + 1);
     }
 
     // ---- Gram matrices [K;Q] K^T (bf16, M=128, N=64, K=128) ----------------------------
@@ -303,66 +310,34 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       tc::mma_commit(x.mb_g);
     }
 
-    // ---- Kd = e^{gc_last-gc} K (fp16, rows t) for the consumer's state update --------
-    // KD[b] was last read by the state update of chunk c-2, which finished before
-    // this group handed over chunk c-1.
-    {
-      uint4 raw[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
-        raw[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16));
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
-        float f[8];
-        unpack_bf16x8(raw[r], f);
-        *reinterpret_cast<uint4*>(sm + kd_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
-            t < clen ? pack_half8(f, x.s_edec[t]) : make_uint4(0, 0, 0, 0);
-      }
-    }
-
-    // ---- Q~ = e^gc Q / sqrt(dk) (fp16, rows t), once the spine of chunk c-1 read Q~ --
-    if (c > 0 && !group_wait(x, p, x.mb_c1, (c - 1) & 1, kBarProducer, kProducerThreads, leader)) break;
-    {
-      uint4 raw[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
-        raw[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + 8192 + tc::sw128(t, (cc & 7) * 16));
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
-        float f[8];
-        unpack_bf16x8(raw[r], f);
-        *reinterpret_cast<uint4*>(sm + P::QT + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
-            t < clen ? pack_half8(f, x.s_eg[t] * kInvSqrtD) : make_uint4(0, 0, 0, 0);
-      }
-    }
-
-    // ---- L (fp32, for the inverse) from K K^T; A (fp16 hi + lo) from Q K^T --------------
-    if (!group_wait(x, p, x.mb_g, b, kBarProducer, kProducerThreads, leader)) break;
-    bool ok = true;
+    // ---- L (fp32) from K K^T (lanes 0-63) and A (fp16 hi + lo) from Q K^T (lanes 64-127) --
+    bool ok = (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
+    if (quad >= 2 && c > 0)  // A is rewritten only after the spine of chunk c-1 used it
+      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c2, (c - 1) & 1, kWaitLimitNs);
+    tc::fence_after_sync();
     {
       uint32_t d[32];
-      if (quad >= 2 && c > 0)  // A is rewritten only after the spine of chunk c-1 used it
-        ok = (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c2, (c - 1) & 1, kWaitLimitNs);
-      tc::fence_after_sync();
       tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + half * 32, d);
       tc::tmem_ld_wait();
       const bool fast = *x.s_fast != 0;
       if (quad < 2) {  // L_tj = beta_t e^{gc_t - gc_j} k_t.k_j for j < t
         const int t = quad * 32 + lane;
         const bool live = t < clen;
-        const float gt = x.s_gc[t], bt = x.s_beta[t], be = bt * x.s_E[t];
         float l[32];
+        if (fast) {
+          const float be = x.s_beta[t] * x.s_E[t];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int j = half * 32 + e;
-          const float dec = fast ? be * x.s_F[j] : bt * __expf(gt - x.s_gc[j]);
-          l[e] = (j < t && live) ? dec * __uint_as_float(d[e]) : 0.f;
+          for (int e = 0; e < 32; ++e) {
+            const int j = half * 32 + e;
+            l[e] = (j < t && live) ? be * x.s_F[j] * __uint_as_float(d[e]) : 0.f;
+          }
+        } else {
+          const float gt = x.s_gc[t], bt = x.s_beta[t];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = half * 32 + e;
+            l[e] = (j < t && live) ? bt * __expf(gt - x.s_gc[j]) * __uint_as_float(d[e]) : 0.f;
+          }
         }
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4)
@@ -376,19 +351,27 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         }
       } else if (ok) {  // A_ij = e^{gc_i - gc_j} q_i.k_j / sqrt(dk) for j <= i
         const int i = (quad - 2) * 32 + lane;
-        const float gi = x.s_gc[i], ei = x.s_E[i] * kInvSqrtD;
+        float a[32];
+        if (fast) {
+          const float ei = x.s_E[i] * kInvSqrtD;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = half * 32 + e;
+            a[e] = (j <= i) ? ei * x.s_F[j] * __uint_as_float(d[e]) : 0.f;
+          }
+        } else {
+          const float gi = x.s_gc[i];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = half * 32 + e;
+            a[e] = (j <= i) ? __expf(gi - x.s_gc[j]) * kInvSqrtD * __uint_as_float(d[e]) : 0.f;
+          }
+        }
 #pragma unroll
         for (int j8 = 0; j8 < 4; ++j8) {
           uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = half * 32 + j8 * 8 + 2 * e;
-            const float d0 = fast ? ei * x.s_F[j] : __expf(gi - x.s_gc[j]) * kInvSqrtD;
-            const float d1 = fast ? ei * x.s_F[j + 1] : __expf(gi - x.s_gc[j + 1]) * kInvSqrtD;
-            const float a0 = (j <= i) ? d0 * __uint_as_float(d[j8 * 8 + 2 * e]) : 0.f;
-            const float a1 = (j + 1 <= i) ? d1 * __uint_as_float(d[j8 * 8 + 2 * e + 1]) : 0.f;
-            split_half2(a0, a1, hi[e], lo[e]);
-          }
+          for (int e = 0; e < 4; ++e) split_half2(a[j8 * 8 + 2 * e], a[j8 * 8 + 2 * e + 1], hi[e], lo[e]);
           const uint32_t o = tc::sw128(i, (half * 32 + j8 * 8) * 2);
           *reinterpret_cast<uint4*>(sm + P::A16 + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(sm + P::A16 + 8192 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -404,83 +387,136 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       break;
     }
 
-    // ---- T = (I + L)^{-1} in fp32, in place over L ------------------------------------
-    // (a) the two diagonal 32 x 32 blocks: one column per thread, right-looking
-    //     substitution; column m of the block comes from the transposed copy as
-    //     broadcast loads.
-    if (pw < 2) {
-      const int r0 = 32 * pw;
-      const float* ltb = lt + pw * 1024;
-      float xv[32];
+    // Crew X (producer warps 0-3, one per SM sub-partition) inverts L while crew Y
+    // (warps 4-7) builds the Kd and Q~ tiles and prefetches the next chunk's gates.
+    if (crew_x) {
+      // ---- T = (I + L)^{-1} in fp32, in place over L -------------------------------------
+      // (a) the two diagonal 32 x 32 blocks: one column per thread, right-looking
+      //     substitution; column m of the block comes from the transposed copy as
+      //     broadcast loads.
+      if (pw < 2) {
+        const int r0 = 32 * pw;
+        const float* ltb = lt + pw * 1024;
+        float xv[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) xv[i] = (i == lane) ? 1.f : 0.f;
+        for (int i = 0; i < 32; ++i) xv[i] = (i == lane) ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < 31; ++m) {
-        float lc[32];
+        for (int m = 0; m < 31; ++m) {
+          float lc[32];
 #pragma unroll
-        for (int i4 = (m + 1) >> 2; i4 < 8; ++i4) {
-          const float4 v4 = *reinterpret_cast<const float4*>(ltb + m * 32 + 4 * i4);
-          lc[4 * i4] = v4.x;
-          lc[4 * i4 + 1] = v4.y;
-          lc[4 * i4 + 2] = v4.z;
-          lc[4 * i4 + 3] = v4.w;
+          for (int i4 = (m + 1) >> 2; i4 < 8; ++i4) {
+            const float4 v4 = *reinterpret_cast<const float4*>(ltb + m * 32 + 4 * i4);
+            lc[4 * i4] = v4.x;
+            lc[4 * i4 + 1] = v4.y;
+            lc[4 * i4 + 2] = v4.z;
+            lc[4 * i4 + 3] = v4.w;
+          }
+          const float xm = xv[m];
+#pragma unroll
+          for (int i = m + 1; i < 32; ++i) xv[i] = fmaf(-lc[i], xm, xv[i]);
         }
-        const float xm = xv[m];
 #pragma unroll
-        for (int i = m + 1; i < 32; ++i) xv[i] = fmaf(-lc[i], xm, xv[i]);
+        for (int i = 0; i < 32; ++i) lf[lf_idx(r0 + i, r0 + lane)] = xv[i];
       }
+      tc::named_barrier(kBarCrewX, kCrewThreads);
+      // (b) lower-left 32 x 32: X = L[32:64, 0:32] T[0:32, 0:32];
+      //     T[32:64, 0:32] = -T[32:64, 32:64] X   (2 x 4 outputs per thread, 4 warps)
+      {
+        const int r0 = (cx >> 3) * 2, c0 = (cx & 7) * 4;
+        float la[32], lb[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) lf[lf_idx(r0 + i, r0 + lane)] = xv[i];
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 va = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r0, 4 * i4));
+          const float4 vb = *reinterpret_cast<const float4*>(lf + lf_idx(33 + r0, 4 * i4));
+          la[4 * i4] = va.x; la[4 * i4 + 1] = va.y; la[4 * i4 + 2] = va.z; la[4 * i4 + 3] = va.w;
+          lb[4 * i4] = vb.x; lb[4 * i4 + 1] = vb.y; lb[4 * i4 + 2] = vb.z; lb[4 * i4 + 3] = vb.w;
+        }
+        float4 xa = make_float4(0.f, 0.f, 0.f, 0.f), xb = xa;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+          const float4 tv = *reinterpret_cast<const float4*>(lf + lf_idx(m, c0));
+          xa.x = fmaf(la[m], tv.x, xa.x); xa.y = fmaf(la[m], tv.y, xa.y);
+          xa.z = fmaf(la[m], tv.z, xa.z); xa.w = fmaf(la[m], tv.w, xa.w);
+          xb.x = fmaf(lb[m], tv.x, xb.x); xb.y = fmaf(lb[m], tv.y, xb.y);
+          xb.z = fmaf(lb[m], tv.z, xb.z); xb.w = fmaf(lb[m], tv.w, xb.w);
+        }
+        *reinterpret_cast<float4*>(xp + r0 * 32 + c0) = xa;
+        *reinterpret_cast<float4*>(xp + (r0 + 1) * 32 + c0) = xb;
+      }
+      tc::named_barrier(kBarCrewX, kCrewThreads);
+      {
+        const int r0 = (cx >> 3) * 2, c0 = (cx & 7) * 4;
+        float ta[32], tb[32];
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 va = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r0, 32 + 4 * i4));
+          const float4 vb = *reinterpret_cast<const float4*>(lf + lf_idx(33 + r0, 32 + 4 * i4));
+          ta[4 * i4] = va.x; ta[4 * i4 + 1] = va.y; ta[4 * i4 + 2] = va.z; ta[4 * i4 + 3] = va.w;
+          tb[4 * i4] = vb.x; tb[4 * i4 + 1] = vb.y; tb[4 * i4 + 2] = vb.z; tb[4 * i4 + 3] = vb.w;
+        }
+        float4 ya = make_float4(0.f, 0.f, 0.f, 0.f), yb = ya;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+          const float4 xv = *reinterpret_cast<const float4*>(xp + m * 32 + c0);
+          ya.x = fmaf(ta[m], xv.x, ya.x); ya.y = fmaf(ta[m], xv.y, ya.y);
+          ya.z = fmaf(ta[m], xv.z, ya.z); ya.w = fmaf(ta[m], xv.w, ya.w);
+          yb.x = fmaf(tb[m], xv.x, yb.x); yb.y = fmaf(tb[m], xv.y, yb.y);
+          yb.z = fmaf(tb[m], xv.z, yb.z); yb.w = fmaf(tb[m], xv.w, yb.w);
+        }
+        *reinterpret_cast<float4*>(lf + lf_idx(32 + r0, c0)) = make_float4(-ya.x, -ya.y, -ya.z, -ya.w);
+        *reinterpret_cast<float4*>(lf + lf_idx(33 + r0, c0)) = make_float4(-yb.x, -yb.y, -yb.z, -yb.w);
+      }
+      tc::named_barrier(kBarCrewX, kCrewThreads);
+    } else {
+      // ---- Kd = e^{gc_last-gc} K (fp16, rows t) for the consumer's state update ------
+      // KD[b] was last read by the state update of chunk c-2, which finished before
+      // this group handed over chunk c-1.
+      {
+        uint4 raw[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int it = cy + r * kCrewThreads, t = it & 63, cc = it >> 6;
+          raw[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16));
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int it = cy + r * kCrewThreads, t = it & 63, cc = it >> 6;
+          float f[8];
+          unpack_bf16x8(raw[r], f);
+          *reinterpret_cast<uint4*>(sm + kd_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
+              t < clen ? pack_half8(f, x.s_edec[t]) : make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (pw == 4 && c + 1 < x.nchunks) load_gates(c + 1);
+      // ---- Q~ = e^gc Q / sqrt(dk) (fp16, rows t), once the spine of chunk c-1 read Q~ --
+      if (c > 0) ok = (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
+      {
+        uint4 raw[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int it = cy + r * kCrewThreads, t = it & 63, cc = it >> 6;
+          raw[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + 8192 + tc::sw128(t, (cc & 7) * 16));
+        }
+        if (ok) {
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const int it = cy + r * kCrewThreads, t = it & 63, cc = it >> 6;
+            float f[8];
+            unpack_bf16x8(raw[r], f);
+            *reinterpret_cast<uint4*>(sm + P::QT + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
+                t < clen ? pack_half8(f, x.s_eg[t] * kInvSqrtD) : make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      if (pw == 4) tc::cp_async_wait_all();
     }
-    tc::named_barrier(kBarProducer, kProducerThreads);
-    // (b) lower-left 32 x 32: X = L[32:64, 0:32] T[0:32, 0:32];
-    //     T[32:64, 0:32] = -T[32:64, 32:64] X   (2 x 4 outputs per thread, 4 warps)
-    if (pw < 4) {
-      const int r0 = (ptid >> 3) * 2, c0 = (ptid & 7) * 4;
-      float la[32], lb[32];
-#pragma unroll
-      for (int i4 = 0; i4 < 8; ++i4) {
-        const float4 va = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r0, 4 * i4));
-        const float4 vb = *reinterpret_cast<const float4*>(lf + lf_idx(33 + r0, 4 * i4));
-        la[4 * i4] = va.x; la[4 * i4 + 1] = va.y; la[4 * i4 + 2] = va.z; la[4 * i4 + 3] = va.w;
-        lb[4 * i4] = vb.x; lb[4 * i4 + 1] = vb.y; lb[4 * i4 + 2] = vb.z; lb[4 * i4 + 3] = vb.w;
+    if (!tc::barrier_all(kBarProducer, kProducerThreads, ok && *x.s_abort == 0)) {
+      if (leader) {
+        *x.s_abort = 1;
+        atomicOr(p.status, kStatusTimeout);
       }
-      float4 xa = make_float4(0.f, 0.f, 0.f, 0.f), xb = xa;
-#pragma unroll
-      for (int m = 0; m < 32; ++m) {
-        const float4 tv = *reinterpret_cast<const float4*>(lf + lf_idx(m, c0));
-        xa.x = fmaf(la[m], tv.x, xa.x); xa.y = fmaf(la[m], tv.y, xa.y);
-        xa.z = fmaf(la[m], tv.z, xa.z); xa.w = fmaf(la[m], tv.w, xa.w);
-        xb.x = fmaf(lb[m], tv.x, xb.x); xb.y = fmaf(lb[m], tv.y, xb.y);
-        xb.z = fmaf(lb[m], tv.z, xb.z); xb.w = fmaf(lb[m], tv.w, xb.w);
-      }
-      *reinterpret_cast<float4*>(xp + r0 * 32 + c0) = xa;
-      *reinterpret_cast<float4*>(xp + (r0 + 1) * 32 + c0) = xb;
+      break;
     }
-    tc::named_barrier(kBarProducer, kProducerThreads);
-    if (pw < 4) {
-      const int r0 = (ptid >> 3) * 2, c0 = (ptid & 7) * 4;
-      float ta[32], tb[32];
-#pragma unroll
-      for (int i4 = 0; i4 < 8; ++i4) {
-        const float4 va = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r0, 32 + 4 * i4));
-        const float4 vb = *reinterpret_cast<const float4*>(lf + lf_idx(33 + r0, 32 + 4 * i4));
-        ta[4 * i4] = va.x; ta[4 * i4 + 1] = va.y; ta[4 * i4 + 2] = va.z; ta[4 * i4 + 3] = va.w;
-        tb[4 * i4] = vb.x; tb[4 * i4 + 1] = vb.y; tb[4 * i4 + 2] = vb.z; tb[4 * i4 + 3] = vb.w;
-      }
-      float4 ya = make_float4(0.f, 0.f, 0.f, 0.f), yb = ya;
-#pragma unroll
-      for (int m = 0; m < 32; ++m) {
-        const float4 xv = *reinterpret_cast<const float4*>(xp + m * 32 + c0);
-        ya.x = fmaf(ta[m], xv.x, ya.x); ya.y = fmaf(ta[m], xv.y, ya.y);
-        ya.z = fmaf(ta[m], xv.z, ya.z); ya.w = fmaf(ta[m], xv.w, ya.w);
-        yb.x = fmaf(tb[m], xv.x, yb.x); yb.y = fmaf(tb[m], xv.y, yb.y);
-        yb.z = fmaf(tb[m], xv.z, yb.z); yb.w = fmaf(tb[m], xv.w, yb.w);
-      }
-      *reinterpret_cast<float4*>(lf + lf_idx(32 + r0, c0)) = make_float4(-ya.x, -ya.y, -ya.z, -ya.w);
-      *reinterpret_cast<float4*>(lf + lf_idx(33 + r0, c0)) = make_float4(-yb.x, -yb.y, -yb.z, -yb.w);
-    }
-    tc::named_barrier(kBarProducer, kProducerThreads);
 
     // ---- bf16 hi/lo tiles of T diag(beta) and T diag(beta e^gc) (rows t, columns j) -----
     {
