@@ -3,9 +3,10 @@
 // Host side: validates every argument before anything is enqueued (each
 // rejection names the guard, in the spirit of the GDN prefill op's named
 // guards, ssm_gdn_a3.rs `gdn_tc_spine_reject`), encodes the TMA descriptors
-// for q, k and v, and enqueues at most two kernels on the caller's stream:
-// the varlen schedule (sequences ordered by decreasing length, validating
-// cu_seqlens on the device) and the fused chunk kernel.
+// for q, k, v and the output, and enqueues at most three kernels on the
+// caller's stream: the varlen schedule (sequences ordered by decreasing
+// length and the chunk prefix over them, validating cu_seqlens on the
+// device), the chunk-parallel WY solve and the fused spine kernel.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -17,6 +18,7 @@
 
 #include "gdn_prefill.h"
 #include "gdn_prefill_kernel.cuh"
+#include "gdn_wy_kernel.cuh"
 
 namespace {
 
@@ -75,6 +77,8 @@ int device_info(DeviceInfo** out) {
     e = cudaFuncSetAttribute(gdn::gdn_prefill_kernel<>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gdn::Plan::DYN_SMEM);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    e = cudaFuncSetAttribute(gdn::gdn_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gdn::WyPlan::DYN_SMEM);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
     d.attrs = true;
@@ -84,19 +88,25 @@ int device_info(DeviceInfo** out) {
 }
 
 // Sequences ordered by decreasing length (ties by index), so the longest
-// chains start first; also validates cu_seqlens. One thread per sequence.
-__global__ void gdn_schedule_kernel(const int32_t* cu, int B, int T, int32_t* order, unsigned* status) {
+// chains start first, and cu_chunks[s] = the number of 64-token chunks in
+// sequences 0..s-1 (a negative length counts as none); also validates
+// cu_seqlens. One thread per sequence.
+__global__ void gdn_schedule_kernel(const int32_t* cu, int B, int T, int32_t* order, int32_t* cu_chunks,
+                                    unsigned* status) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= B) return;
   const int a = cu[s], b = cu[s + 1];
   if (a < 0 || b < a || b > T || (s == 0 && a != 0) || (s == B - 1 && b != T)) atomicOr(status, gdn::kStatusBadSeqlens);
   const int len = b - a;
-  int rank = 0;
+  int rank = 0, before = 0;
   for (int o = 0; o < B; ++o) {
     const int lo = cu[o + 1] - cu[o];
     rank += (lo > len) || (lo == len && o < s);
+    if (o <= s && lo > 0) before += (lo + gdn::kChunk - 1) / gdn::kChunk;
   }
   order[rank] = s;
+  cu_chunks[s + 1] = before;
+  if (s == 0) cu_chunks[0] = 0;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -149,25 +159,52 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
 }
 
 int launch(const void* q, const void* k, const void* v, const float* g, const float* beta, void* state, void* out,
-           int B, int T, int nk, int nv, const Resolved& r, const int32_t* cu, int32_t* order, cudaStream_t stream) {
+           int B, int T, int nk, int nv, const Resolved& r, const int32_t* cu, int32_t* sched, cudaStream_t stream) {
   DeviceInfo* d = nullptr;
   if (int rc = device_info(&d)) return rc;
   const int64_t rows = cu ? static_cast<int64_t>(T) : static_cast<int64_t>(B) * T;
   if (rows > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "%lld token rows exceed the 2^31 TMA coordinate range", (long long)rows);
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mt;
   if (int rc = make_map(&mq, q, static_cast<int64_t>(nk) * gdn::kDim, rows, r.q, "q")) return rc;
   if (int rc = make_map(&mk, k, static_cast<int64_t>(nk) * gdn::kDim, rows, r.k, "k")) return rc;
   if (int rc = make_map(&mv, v, static_cast<int64_t>(nv) * gdn::kDim, rows, r.v, "v")) return rc;
+  // the output rows, read back as 16-bit T diag(beta) tiles
+  if (int rc = make_map(&mt, out, static_cast<int64_t>(nv) * gdn::kDim, rows, r.out, "out")) return rc;
+  int32_t* order = cu ? sched : nullptr;
+  int32_t* cu_chunks = cu ? sched + B : nullptr;
+
+  gdn::WyParams w;
+  w.g = g;
+  w.beta = beta;
+  w.tb = static_cast<uint16_t*>(out);
+  w.cu_seqlens = cu;
+  w.cu_chunks = cu_chunks;
+  w.status = d->status;
+  w.g_stride = r.g;
+  w.beta_stride = r.beta;
+  w.out_stride = r.out;
+  w.B = B;
+  w.T = T;
+  w.nk = nk;
+  w.nv = nv;
+  w.chunks_per_seq = (T + gdn::kChunk - 1) / gdn::kChunk;
+  // dense: every chunk of every sequence; varlen: an upper bound on the chunk
+  // count (sum of ceil(len / 64) <= T / 64 + B), the excess CTAs exit at once
+  const int64_t wy_chunks = cu ? static_cast<int64_t>(T) / gdn::kChunk + B + 1
+                               : static_cast<int64_t>(w.chunks_per_seq) * B;
+  w.items = wy_chunks * nv;
+  // persistent: a few CTAs per SM walk the items
+  const int64_t wy_grid = w.items < static_cast<int64_t>(d->sms) * gdn::kWyCtasPerSm
+                              ? w.items : static_cast<int64_t>(d->sms) * gdn::kWyCtasPerSm;
+
   gdn::ChunkParams p;
   p.g = g;
-  p.beta = beta;
   p.state = state;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.cu_seqlens = cu;
   p.order = order;
   p.status = d->status;
   p.g_stride = r.g;
-  p.beta_stride = r.beta;
   p.out_stride = r.out;
   p.B = B;
   p.T = T;
@@ -176,14 +213,17 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   p.state_is_table = r.table;
   int launches = 0;
   if (cu) {
-    gdn_schedule_kernel<<<(B + 255) / 256, 256, 0, stream>>>(cu, B, T, order, d->status);
+    gdn_schedule_kernel<<<(B + 255) / 256, 256, 0, stream>>>(cu, B, T, order, cu_chunks, d->status);
     ++launches;
   }
+  gdn::gdn_wy_kernel<<<static_cast<unsigned>(wy_grid), gdn::kWyThreads, gdn::WyPlan::DYN_SMEM, stream>>>(mk, w);
+  ++launches;
   // one CTA per (sequence, v-head); CTAs of the same sequence and GQA group are
   // adjacent so their shared q/k tiles meet in L2
   const int64_t grid = static_cast<int64_t>(B) * nv;
   if (grid > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "grid of %lld CTAs too large", (long long)grid);
-  gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, p);
+  gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt,
+                                                                                                      p);
   ++launches;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
@@ -191,17 +231,19 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   return GDN_OK;
 }
 
+// varlen: the sequence order (B int32) followed by the chunk prefix (B + 1 int32)
 size_t workspace_bytes(int B, int varlen) {
   if (!varlen || B <= 0) return 0;
-  return (static_cast<size_t>(B) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+  return ((2 * static_cast<size_t>(B) + 1) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
 }
 
 // ---- allocation-free entry point -------------------------------------------------
-// Scratch for gdn_prefill_noalloc: the varlen schedule (one int32 per
-// sequence) lives in this file-scope device array instead of a workspace.
-// Every GPU that loads the library holds it until the process exits.
+// Scratch for gdn_prefill_noalloc: the varlen schedule (the sequence order
+// and the chunk prefix, 2B + 1 int32) lives in this file-scope device array
+// instead of a workspace. Every GPU that loads the library holds it until the
+// process exits.
 constexpr int kNoAllocMaxSeqs = GDN_NOALLOC_MAX_SEQS;
-static __device__ __align__(256) int32_t g_noalloc_order[kNoAllocMaxSeqs];
+static __device__ __align__(256) int32_t g_noalloc_order[2 * kNoAllocMaxSeqs + 1];
 int32_t* g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of g_noalloc_order on the current device, looked up once

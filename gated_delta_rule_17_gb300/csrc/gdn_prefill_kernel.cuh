@@ -1,14 +1,15 @@
-// Fused chunked gated-delta-rule prefill kernel for sm_103a (warp-specialised).
+// Fused chunked gated-delta-rule prefill spine kernel for sm_103a
+// (warp-specialised).
 //
 // One CTA owns one (sequence, v-head) and walks its 64-token chunks in order.
-// It runs the three stages of the GDN prefill op (ssm_gdn_a3.rs, doc comment
-// of `gdn_prefill_fla`) on chip, split between two warp groups:
+// With T diag(beta) of every chunk already solved by the chunk-parallel WY
+// kernel, it runs the rest of the GDN prefill op (ssm_gdn_a3.rs, doc comment of
+// `gdn_prefill_fla`) on chip, split between two warp groups:
 //
-//   producer (8 warps), chunk c+1:  WY stage
-//     gc = cumsum(g);  L_ij = beta_i e^{gc_i-gc_j} k_i.k_j (j < i);
-//     T = (I + L)^{-1};  U = T diag(beta) V;  W = T diag(beta e^gc) K;
-//     and the operand tiles the spine needs (e^gc Q / sqrt(dk), e^{gc_last-gc} K,
-//     A_ij = e^{gc_i-gc_j} q_i.k_j / sqrt(dk) for j <= i)
+//   producer (8 warps), chunk c+1:  WY products and operand tiles
+//     U = (T diag beta) V;  W = (T diag beta) diag(e^gc) K;
+//     e^gc Q / sqrt(dk), e^{gc_last-gc} K, and
+//     A_ij = e^{gc_i-gc_j} q_i.k_j / sqrt(dk) for j <= i
 //   consumer (4 warps), chunk c:    state spine and output
 //     u = U - W S;  S <- e^{gc_last} S + (diag(e^{gc_last-gc}) K)^T u;
 //     O = diag(e^gc) Q S / sqrt(dk) + A u          (S: state entering chunk c)
@@ -20,27 +21,24 @@
 // owns one v column, so the output rows are written with coalesced stores.
 // The fp32 state S^T lives in tensor memory as the accumulator of dS^T.
 //
-// Precision: the Gram matrices use the exact bf16 inputs; U and W use bf16 hi+lo
-// splits of T diag(beta) and T diag(beta e^gc) against the exact V and K tiles;
-// the spine uses fp16 operands with fp32
-// accumulation, and A u uses fp16 hi+lo splits of both factors (the largest
-// outputs must be accurate to ~1e-4 before the final bf16 rounding).
+// Precision: T diag(beta) arrives as an fp16 hi + lo pair; U and W multiply
+// both halves with fp16 copies of V (exact for |v| < 65504) and of e^gc K.
+// The spine uses fp16 operands with fp32 accumulation, and A u uses fp16
+// hi + lo splits of both factors (the largest outputs must be accurate to
+// ~1e-4 before the final bf16 rounding).
 //
-// Tail rows of a chunk (past the end of the sequence) are treated as k = v =
-// 0, beta = 0, g = 0 and their outputs are not stored. Every wait on an
-// mbarrier is bounded; on expiry the CTA records a status bit and unwinds.
+// The WY kernel leaves each chunk's T diag(beta) rows in the output rows of
+// the same tokens and head; this kernel reads them (by TMA) before it writes
+// the outputs there. Tail rows of a chunk (past the end of the sequence) are
+// treated as k = v = 0, g = 0: their T diag(beta) rows, which belong to other
+// tokens, only reach columns of u^T that are zeroed before use, and their
+// outputs are not stored. Every wait on an mbarrier is bounded; on expiry the
+// CTA records a status bit and unwinds.
 #pragma once
-#include <cuda.h>
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-#include <cstdint>
-
-#include "tc.cuh"
+#include "gdn_common.cuh"
 
 namespace gdn {
 
-constexpr int kDim = 128;   // dk == dv
-constexpr int kChunk = 64;  // tokens per chunk
 constexpr int kConsumerWarps = 4;
 constexpr int kProducerWarps = 8;
 constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
@@ -48,22 +46,15 @@ constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr uint32_t kBarProducer = 1;  // named barrier ids
 constexpr uint32_t kBarConsumer = 2;
-constexpr uint32_t kBarCrewX = 3;     // producer crew X (warps 0-3 of the producer)
-constexpr int kCrewThreads = kProducerThreads / 2;
-
-// Status bits written to the per-device status word.
-constexpr unsigned kStatusBadSeqlens = 1u;
-constexpr unsigned kStatusTimeout = 2u;
 
 struct ChunkParams {
   const float* g;
-  const float* beta;
   void* state;                // float[B][nv][128][128], or float*[B] when state_is_table
   __nv_bfloat16* out;
   const int32_t* cu_seqlens;  // null for dense batches
   const int32_t* order;       // varlen: sequences by decreasing length (null: identity)
   unsigned* status;
-  int64_t g_stride, beta_stride, out_stride;
+  int64_t g_stride, out_stride;
   int B, T, nk, nv;
   int state_is_table;
 };
@@ -73,22 +64,20 @@ struct ChunkParams {
 // (the layout TMA writes); the same bytes serve as a K-major operand whose
 // rows are M/N, or as an MN-major operand whose rows are K.
 struct Plan {
-  static constexpr int KQ0 = 0;            // raw bf16 [K;Q] (2 blocks x 128 rows), chunk parity 0
-  static constexpr int KQ1 = KQ0 + 32768;  // ... chunk parity 1
-  static constexpr int VR = KQ1 + 32768;   // raw bf16 V (2 blocks x 64 rows)
-  static constexpr int LF = VR + 16384;    // fp32 64 x 64 L, overwritten by T
-  static constexpr int LT = LF + 16384;    // fp32 2 x 32 x 32 diagonal blocks of L, transposed (8 KB),
-  static constexpr int XP = LT + 4096;     //   whose upper half is reused for 32 x 32 partial products
-  static constexpr int TB = XP + 4096;     // bf16 T diag(beta) hi, lo; T diag(beta e^gc) hi, lo
-  static constexpr int W16 = TB + 32768;   // fp16 -W^T, rows k (128 x 64)
-  static constexpr int QT = W16 + 16384;   // fp16 e^gc Q / sqrt(dk), rows t (64 x 128)
-  static constexpr int KD0 = QT + 16384;   // fp16 e^{gc_last-gc} K, rows t, chunk parity 0
+  static constexpr int KQ0 = 0;            // raw bf16 [K;Q] (2 blocks x 128 rows), chunk parity 0; K becomes
+  static constexpr int KQ1 = KQ0 + 32768;  //   fp16 e^gc K and Q fp16 e^gc Q / sqrt(dk) in place; ... parity 1
+  static constexpr int V0 = KQ1 + 32768;   // raw bf16 V (2 blocks x 64 rows), made fp16 in place
+  static constexpr int V1 = V0 + 16384;
+  static constexpr int TB0 = V1 + 16384;   // fp16 T diag(beta) hi, lo (64 x 64 each, rows t)
+  static constexpr int TB1 = TB0 + 16384;
+  static constexpr int W16 = TB1 + 16384;  // fp16 -W^T, rows k (128 x 64)
+  static constexpr int KD0 = W16 + 16384;  // fp16 e^{gc_last-gc} K, rows t, chunk parity 0
   static constexpr int KD1 = KD0 + 16384;  // ... chunk parity 1
-  static constexpr int A16 = KD1 + 16384;  // fp16 A hi, lo (64 x 64 each)
-  static constexpr int BYTES = A16 + 16384;
+  static constexpr int A0 = KD1 + 16384;   // fp16 A hi, lo (64 x 64 each), chunk parity 0
+  static constexpr int A1 = A0 + 16384;    // ... chunk parity 1
+  static constexpr int BYTES = A1 + 16384;
   static constexpr int DYN_SMEM = BYTES + 1024;  // slack for 1024-byte alignment
-  static_assert(DYN_SMEM <= 227 * 1024 - 4096, "shared memory budget");
-  static_assert(TB % 1024 == 0 && W16 % 1024 == 0 && KD0 % 1024 == 0 && A16 % 1024 == 0, "tile alignment");
+  static_assert(DYN_SMEM <= 227 * 1024 - 8192, "shared memory budget");
 
   // Tensor-memory columns (512 x 32-bit, lanes = rows).
   static constexpr uint32_t COL_S = 0;     // fp32 S^T [v][k], 128 columns
@@ -100,57 +89,6 @@ struct Plan {
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
-// fp32 64 x 64 work matrix with 16-byte chunks XOR-swizzled by row, so that
-// float4 accesses by threads on different rows hit different banks.
-__device__ __forceinline__ int lf_idx(int r, int c) {
-  return r * 64 + ((((c >> 2) ^ r) & 15) << 2) + (c & 3);
-}
-
-__device__ __forceinline__ void unpack_bf16x8(const uint4 raw, float (&f)[8]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
-  __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint4 pack_half8(const float (&f)[8], float s) {
-  return make_uint4(pack_half2(f[0] * s, f[1] * s), pack_half2(f[2] * s, f[3] * s),
-                    pack_half2(f[4] * s, f[5] * s), pack_half2(f[6] * s, f[7] * s));
-}
-
-__device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-// (a, b) = hi + lo with hi = fp16(x), lo = fp16(x - hi): about 22 significant bits.
-__device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 x = __floats2half2_rn(a, b);
-  const float2 xf = __half22float2(x);
-  const __half2 y = __floats2half2_rn(a - xf.x, b - xf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&x);
-  lo = *reinterpret_cast<const uint32_t*>(&y);
-}
-
-// (a, b) = hi + lo with hi = bf16(x), lo = bf16(x - hi): about 16 significant bits.
-__device__ __forceinline__ void split_bf162(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 x = __floats2bfloat162_rn(a, b);
-  const float2 xf = __bfloat1622float2(x);
-  const __nv_bfloat162 y = __floats2bfloat162_rn(a - xf.x, b - xf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&x);
-  lo = *reinterpret_cast<const uint32_t*>(&y);
-}
-
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
-constexpr float kInvSqrtD = 0.08838834764831845f;  // 1 / sqrt(128)
-
 // Per-CTA state shared by the two warp groups.
 struct Ctx {
   uint8_t* sm;       // 1024-aligned dynamic shared memory
@@ -159,15 +97,15 @@ struct Ctx {
   int64_t row0, len; // first packed row and length of the sequence
   int nchunks, h, kh;
   float* state;      // this (sequence, head)'s fp32 [128][128] state, k-major
-  // producer-side per-token scales of the current chunk
-  float *s_gc, *s_eg, *s_edec, *s_ebg, *s_beta;
+  // producer-side per-token scales, two gate sets by chunk parity ([2][64] each)
+  float *s_gc, *s_eg, *s_edec;
   float *s_E, *s_F;     // e^{gc - m}, e^{m - gc} about the chunk's mid gate m
-  int* s_fast;          // 1 when the chunk's gate range allows the factorised decays
-  float* s_gstage;      // [2][2][64] g and beta of the next chunk, staged by cp.async
+  int* s_fast;          // [2] 1 when the chunk's gate range allows the factorised decays
+  float* s_gstage;      // [2][64] g of a chunk, staged by cp.async
   uint16_t* s_ostage;   // [4 warps][8][32] bf16 output staging of the consumer
-  float* s_elast;    // [2] e^{gc_last} by chunk parity (read by the consumer)
+  float* s_elast;       // [3] e^{gc_last} by chunk index mod 3 (read by the consumer)
   volatile int* s_abort;
-  uint32_t mb_kq0, mb_kq1, mb_v, mb_g, mb_uw, mb_c1, mb_c2, mb_hand, mb_cu;
+  uint32_t mb_kq0, mb_kq1, mb_v0, mb_v1, mb_g, mb_uw, mb_c1, mb_c2, mb_hand, mb_cu0, mb_cu1;
 };
 
 // All threads of a group wait on one mbarrier phase; the outcome is made
@@ -188,22 +126,20 @@ __device__ __forceinline__ bool group_wait(const Ctx& x, const ChunkParams& p, u
 }
 
 // ---------------------------------------------------------------------------------
-// Producer: the WY stage of each chunk, one chunk ahead of the consumer.
+// Producer: the WY products and operand tiles of each chunk, one chunk ahead of
+// the consumer. Warp 4 also scans the gates of the chunk after, so every chunk
+// starts with its gate set ready.
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p, const CUtensorMap* tmap_q,
-                                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_v, int ptid) {
+                                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                              const CUtensorMap* tmap_t, int ptid) {
   using P = Plan;
   const int pw = ptid >> 5, lane = ptid & 31;
   const int quad = pw & 3;   // tensor-memory lane quarter of this warp
   const int half = pw >> 2;  // which half of a 64-column accumulator it reads
   const bool leader = ptid == 0;
-  const bool crew_x = pw < 4;                  // crews X and Y each hold one warp per sub-partition
-  const int cx = (pw & 3) * 32 + lane;         // thread index within its crew
-  const int cy = cx;
+  const int hq = half * 64 + (quad & 1) * 32 + lane;  // index among the 4 warps of its lane-quarter pair
   uint8_t* sm = x.sm;
-  float* lf = reinterpret_cast<float*>(sm + P::LF);
-  float* lt = reinterpret_cast<float*>(sm + P::LT);
-  float* xp = reinterpret_cast<float*>(sm + P::XP);
 
   auto issue_kq = [&](int c) {
     const uint32_t dst = x.sbase + ((c & 1) ? P::KQ1 : P::KQ0);
@@ -215,91 +151,92 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     tc::tma_load_2d(dst + 8192, tmap_q, x.kh * kDim, y, mb);
     tc::tma_load_2d(dst + 16384 + 8192, tmap_q, x.kh * kDim + 64, y, mb);
   };
-  auto issue_v = [&](int c) {
+  // the V tile and the T diag(beta) hi/lo tiles of chunk c, into buffer c & 1
+  auto issue_vt = [&](int c) {
+    const uint32_t vd = x.sbase + ((c & 1) ? P::V1 : P::V0), td = x.sbase + ((c & 1) ? P::TB1 : P::TB0);
+    const uint32_t mb = (c & 1) ? x.mb_v1 : x.mb_v0;
     const int32_t y = static_cast<int32_t>(x.row0 + static_cast<int64_t>(c) * kChunk);
-    tc::mbar_arrive_expect_tx(x.mb_v, 16384);
-    tc::tma_load_2d(x.sbase + P::VR, tmap_v, x.h * kDim, y, x.mb_v);
-    tc::tma_load_2d(x.sbase + P::VR + 8192, tmap_v, x.h * kDim + 64, y, x.mb_v);
+    tc::mbar_arrive_expect_tx(mb, 32768);
+    tc::tma_load_2d(vd, tmap_v, x.h * kDim, y, mb);
+    tc::tma_load_2d(vd + 8192, tmap_v, x.h * kDim + 64, y, mb);
+    tc::tma_load_2d(td, tmap_t, x.h * kDim, y, mb);
+    tc::tma_load_2d(td + 8192, tmap_t, x.h * kDim + 64, y, mb);
   };
-  // gates of tokens 2*lane and 2*lane+1 of chunk c, copied to shared memory
-  // (stage c & 1) without a register round trip (producer warp 0 only)
+  // gates of chunk c (one warp, producer warp 4): the log-gates of tokens 2*lane and
+  // 2*lane+1 are copied to stage c & 1 by cp.async two chunks ahead, then scanned
+  // into gate set c & 1 one chunk ahead
   auto load_gates = [&](int c) {
-    float* st = x.s_gstage + (c & 1) * 128;
+    float* st = x.s_gstage + (c & 1) * kChunk;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int tt = 2 * lane + e;
       const int64_t t = static_cast<int64_t>(c) * kChunk + tt;
-      if (t < x.len) {
-        const int64_t r = x.row0 + t;
-        tc::cp_async_4(tc::smem_u32(st + tt), p.g + r * p.g_stride + x.h);
-        tc::cp_async_4(tc::smem_u32(st + 64 + tt), p.beta + r * p.beta_stride + x.h);
-      } else {
+      if (t < x.len)
+        tc::cp_async_4(tc::smem_u32(st + tt), p.g + (x.row0 + t) * p.g_stride + x.h);
+      else
         st[tt] = 0.f;
-        st[64 + tt] = 0.f;
-      }
     }
     tc::cp_async_commit();
+  };
+  auto scan_gates = [&](int c) {  // after the copy of chunk c's gates has completed
+    const int gs = (c & 1) * kChunk;
+    __syncwarp();
+    const float* st = x.s_gstage + gs;
+    const GatePrefix gp = gate_prefix(st[2 * lane], st[2 * lane + 1]);
+    // e^{gc_i - gc_j} = E_i F_j with E = e^{gc - m}, F = e^{m - gc} and m the
+    // middle of the chunk's gate range
+    const float mid = 0.5f * (gp.first + gp.last);
+    x.s_gc[gs + 2 * lane] = gp.gca;
+    x.s_gc[gs + 2 * lane + 1] = gp.gcb;
+    x.s_eg[gs + 2 * lane] = __expf(gp.gca);
+    x.s_eg[gs + 2 * lane + 1] = __expf(gp.gcb);
+    x.s_edec[gs + 2 * lane] = __expf(gp.last - gp.gca);
+    x.s_edec[gs + 2 * lane + 1] = __expf(gp.last - gp.gcb);
+    x.s_E[gs + 2 * lane] = __expf(gp.gca - mid);
+    x.s_E[gs + 2 * lane + 1] = __expf(gp.gcb - mid);
+    x.s_F[gs + 2 * lane] = __expf(mid - gp.gca);
+    x.s_F[gs + 2 * lane + 1] = __expf(mid - gp.gcb);
+    if (lane == 0) {
+      x.s_elast[c % 3] = __expf(gp.last);
+      x.s_fast[c & 1] = (gp.first - gp.last) <= kFactorisedRange;
+    }
+  };
+  auto fail = [&]() {
+    *x.s_abort = 1;
+    atomicOr(p.status, kStatusTimeout);
   };
 
   if (leader) {
     issue_kq(0);
-    issue_v(0);
-    if (x.nchunks > 1) issue_kq(1);
+    issue_vt(0);
+    if (x.nchunks > 1) {
+      issue_kq(1);
+      issue_vt(1);
+    }
   }
-  if (pw == 4) {  // crew Y stages the gates; the join barrier publishes them
+  if (pw == 4) {
     load_gates(0);
     tc::cp_async_wait_all();
+    scan_gates(0);
+    if (x.nchunks > 1) load_gates(1);
   }
   tc::named_barrier(kBarProducer, kProducerThreads);
+  bool ok = true;
 
   for (int c = 0; c < x.nchunks; ++c) {
     const int b = c & 1;
+    const int gs = b * kChunk;  // this chunk's gate set
+    const uint32_t use = (c >> 1) & 1;  // phase parity of this chunk's double-buffered tiles
     const int64_t rem = x.len - static_cast<int64_t>(c) * kChunk;
     const int clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
     const uint32_t kq_off = b ? P::KQ1 : P::KQ0;
     const uint32_t kd_off = b ? P::KD1 : P::KD0;
+    const uint32_t v_off = b ? P::V1 : P::V0;
+    const uint32_t tb_off = b ? P::TB1 : P::TB0;
+    const uint32_t a_off = b ? P::A1 : P::A0;
 
-    // ---- gates: in-chunk cumulative log-gate and the per-token scales ----------------
-    if (pw == 0) {
-      const float* st = x.s_gstage + b * 128;
-      const float g0 = st[2 * lane], g1 = st[2 * lane + 1];
-      const float b0 = st[64 + 2 * lane], b1 = st[64 + 2 * lane + 1];
-      const float pair = g0 + g1;
-      float incl = pair;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const float gca = incl - pair + g0, gcb = incl;
-      const float glast = __shfl_sync(0xffffffffu, incl, 31);
-      const float gfirst = __shfl_sync(0xffffffffu, gca, 0);
-      // e^{gc_i - gc_j} = e^{gc_i - m} e^{m - gc_j} with m the middle of the chunk's
-      // gate range; both factors stay within e^{+-60} when the range is <= 120.
-      const float mid = 0.5f * (gfirst + glast);
-      const float ea = __expf(gca), eb = __expf(gcb);
-      x.s_gc[2 * lane] = gca;
-      x.s_gc[2 * lane + 1] = gcb;
-      x.s_eg[2 * lane] = ea;
-      x.s_eg[2 * lane + 1] = eb;
-      x.s_edec[2 * lane] = __expf(glast - gca);
-      x.s_edec[2 * lane + 1] = __expf(glast - gcb);
-      x.s_ebg[2 * lane] = b0 * ea;
-      x.s_ebg[2 * lane + 1] = b1 * eb;
-      x.s_beta[2 * lane] = b0;
-      x.s_beta[2 * lane + 1] = b1;
-      x.s_E[2 * lane] = __expf(gca - mid);
-      x.s_E[2 * lane + 1] = __expf(gcb - mid);
-      x.s_F[2 * lane] = __expf(mid - gca);
-      x.s_F[2 * lane + 1] = __expf(mid - gcb);
-      if (lane == 0) {
-        x.s_elast[b] = __expf(glast);
-        *x.s_fast = (gfirst - glast) <= 120.f;
-      }
-    }
-
-    // ---- Gram matrices [K;Q] K^T (bf16, M=128, N=64, K=128) ----------------------------
-    if (!group_wait(x, p, b ? x.mb_kq1 : x.mb_kq0, (c >> 1) & 1, kBarProducer, kProducerThreads, leader)) break;
+    // ---- Gram matrix [K;Q] K^T (bf16, M=128, N=64, K=128); lanes 64-127 hold Q K^T ---
+    if (!group_wait(x, p, b ? x.mb_kq1 : x.mb_kq0, use, kBarProducer, kProducerThreads, leader)) break;
     if (leader) {
       constexpr uint32_t idesc = tc::idesc_f16(128, 64, tc::kBF16, false, false);
 #pragma unroll
@@ -309,62 +246,56 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       }
       tc::mma_commit(x.mb_g);
     }
+    // The spine of chunk c-1 has read its Q~ and -W^T (and so finished chunk c-2,
+    // whose Kd and A buffers this chunk reuses): the K/Q buffer of chunk c-1 is free
+    // for chunk c+1, and -W^T may be rewritten.
+    if (c > 0) {
+      ok = (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
+      if (leader && ok && c + 1 < x.nchunks) issue_kq(c + 1);
+    }
 
-    // ---- L (fp32) from K K^T (lanes 0-63) and A (fp16 hi + lo) from Q K^T (lanes 64-127) --
-    bool ok = (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
-    if (quad >= 2 && c > 0)  // A is rewritten only after the spine of chunk c-1 used it
-      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c2, (c - 1) & 1, kWaitLimitNs);
-    tc::fence_after_sync();
-    {
-      uint32_t d[32];
-      tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + half * 32, d);
-      tc::tmem_ld_wait();
-      const bool fast = *x.s_fast != 0;
-      if (quad < 2) {  // L_tj = beta_t e^{gc_t - gc_j} k_t.k_j for j < t
-        const int t = quad * 32 + lane;
-        const bool live = t < clen;
-        float l[32];
-        if (fast) {
-          const float be = x.s_beta[t] * x.s_E[t];
+    if (quad < 2) {
+      // ---- V -> fp16 in place (rows t; tail rows zeroed), lane quarters 0, 1 -----------
+      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_v1 : x.mb_v0, use, kWaitLimitNs);
+      if (ok) {
+        uint4 raw[8];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = half * 32 + e;
-            l[e] = (j < t && live) ? be * x.s_F[j] * __uint_as_float(d[e]) : 0.f;
-          }
-        } else {
-          const float gt = x.s_gc[t], bt = x.s_beta[t];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = half * 32 + e;
-            l[e] = (j < t && live) ? bt * __expf(gt - x.s_gc[j]) * __uint_as_float(d[e]) : 0.f;
-          }
+        for (int r = 0; r < 8; ++r) {
+          const int it = hq + r * 128, t = it & 63, cc = it >> 6;
+          raw[r] = *reinterpret_cast<const uint4*>(sm + v_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16));
         }
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4)
-          *reinterpret_cast<float4*>(lf + lf_idx(t, half * 32 + j4 * 4)) =
-              make_float4(l[4 * j4], l[4 * j4 + 1], l[4 * j4 + 2], l[4 * j4 + 3]);
-        // the diagonal 32 x 32 block of L, transposed, for the inverse's first phase
-        if (quad == half) {
-          float* dst = lt + quad * 1024 + lane;
-#pragma unroll
-          for (int m = 0; m < 32; ++m) dst[m * 32] = l[m];
+        for (int r = 0; r < 8; ++r) {
+          const int it = hq + r * 128, t = it & 63, cc = it >> 6;
+          float f[8];
+          unpack_bf16x8(raw[r], f);
+          *reinterpret_cast<uint4*>(sm + v_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
+              t < clen ? pack_half8(f, 1.f) : make_uint4(0, 0, 0, 0);
         }
-      } else if (ok) {  // A_ij = e^{gc_i - gc_j} q_i.k_j / sqrt(dk) for j <= i
-        const int i = (quad - 2) * 32 + lane;
+      }
+    } else {
+      // ---- A (fp16 hi + lo) from Q K^T, lanes 64-127 ------------------------------------
+      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
+      tc::fence_after_sync();
+      if (ok) {
+        uint32_t d[32];
+        tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + half * 32, d);
+        tc::tmem_ld_wait();
+        const int i = (quad - 2) * 32 + lane;  // A_ij = e^{gc_i - gc_j} q_i.k_j / sqrt(dk), j <= i
         float a[32];
-        if (fast) {
-          const float ei = x.s_E[i] * kInvSqrtD;
+        if (x.s_fast[b] != 0) {
+          const float ei = x.s_E[gs + i] * kInvSqrtD;
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int j = half * 32 + e;
-            a[e] = (j <= i) ? ei * x.s_F[j] * __uint_as_float(d[e]) : 0.f;
+            a[e] = (j <= i) ? ei * x.s_F[gs + j] * __uint_as_float(d[e]) : 0.f;
           }
         } else {
-          const float gi = x.s_gc[i];
+          const float gi = x.s_gc[gs + i];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int j = half * 32 + e;
-            a[e] = (j <= i) ? __expf(gi - x.s_gc[j]) * kInvSqrtD * __uint_as_float(d[e]) : 0.f;
+            a[e] = (j <= i) ? __expf(gi - x.s_gc[gs + j]) * kInvSqrtD * __uint_as_float(d[e]) : 0.f;
           }
         }
 #pragma unroll
@@ -373,210 +304,80 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 #pragma unroll
           for (int e = 0; e < 4; ++e) split_half2(a[j8 * 8 + 2 * e], a[j8 * 8 + 2 * e + 1], hi[e], lo[e]);
           const uint32_t o = tc::sw128(i, (half * 32 + j8 * 8) * 2);
-          *reinterpret_cast<uint4*>(sm + P::A16 + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(sm + P::A16 + 8192 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(sm + a_off + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm + a_off + 8192 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
-    }
-    tc::fence_before_sync();
-    if (!tc::barrier_all(kBarProducer, kProducerThreads, ok && *x.s_abort == 0)) {
-      if (leader) {
-        *x.s_abort = 1;
-        atomicOr(p.status, kStatusTimeout);
-      }
-      break;
     }
 
-    // Crew X (producer warps 0-3, one per SM sub-partition) inverts L while crew Y
-    // (warps 4-7) builds the Kd and Q~ tiles and prefetches the next chunk's gates.
-    if (crew_x) {
-      // ---- T = (I + L)^{-1} in fp32, in place over L -------------------------------------
-      // (a) the two diagonal 32 x 32 blocks: one column per thread, right-looking
-      //     substitution; column m of the block comes from the transposed copy as
-      //     broadcast loads.
-      if (pw < 2) {
-        const int r0 = 32 * pw;
-        const float* ltb = lt + pw * 1024;
-        float xv[32];
+    // ---- once the Gram MMA has read K and Q, in place (fp16, rows t, tail rows zeroed):
+    //      K -> e^gc K and Q -> Q~ = e^gc Q / sqrt(dk); and Kd = e^{gc_last-gc} K (KD[b]).
+    ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
+    if (ok) {
+      uint4 rk[4], rq[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) xv[i] = (i == lane) ? 1.f : 0.f;
-#pragma unroll
-        for (int m = 0; m < 31; ++m) {
-          float lc[32];
-#pragma unroll
-          for (int i4 = (m + 1) >> 2; i4 < 8; ++i4) {
-            const float4 v4 = *reinterpret_cast<const float4*>(ltb + m * 32 + 4 * i4);
-            lc[4 * i4] = v4.x;
-            lc[4 * i4 + 1] = v4.y;
-            lc[4 * i4 + 2] = v4.z;
-            lc[4 * i4 + 3] = v4.w;
-          }
-          const float xm = xv[m];
-#pragma unroll
-          for (int i = m + 1; i < 32; ++i) xv[i] = fmaf(-lc[i], xm, xv[i]);
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) lf[lf_idx(r0 + i, r0 + lane)] = xv[i];
+      for (int r = 0; r < 4; ++r) {
+        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
+        const uint32_t o = kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16);
+        rk[r] = *reinterpret_cast<const uint4*>(sm + o);
+        rq[r] = *reinterpret_cast<const uint4*>(sm + o + 8192);
       }
-      tc::named_barrier(kBarCrewX, kCrewThreads);
-      // (b) lower-left 32 x 32: X = L[32:64, 0:32] T[0:32, 0:32];
-      //     T[32:64, 0:32] = -T[32:64, 32:64] X   (2 x 4 outputs per thread, 4 warps)
-      {
-        const int r0 = (cx >> 3) * 2, c0 = (cx & 7) * 4;
-        float la[32], lb[32];
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 va = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r0, 4 * i4));
-          const float4 vb = *reinterpret_cast<const float4*>(lf + lf_idx(33 + r0, 4 * i4));
-          la[4 * i4] = va.x; la[4 * i4 + 1] = va.y; la[4 * i4 + 2] = va.z; la[4 * i4 + 3] = va.w;
-          lb[4 * i4] = vb.x; lb[4 * i4 + 1] = vb.y; lb[4 * i4 + 2] = vb.z; lb[4 * i4 + 3] = vb.w;
-        }
-        float4 xa = make_float4(0.f, 0.f, 0.f, 0.f), xb = xa;
-#pragma unroll
-        for (int m = 0; m < 32; ++m) {
-          const float4 tv = *reinterpret_cast<const float4*>(lf + lf_idx(m, c0));
-          xa.x = fmaf(la[m], tv.x, xa.x); xa.y = fmaf(la[m], tv.y, xa.y);
-          xa.z = fmaf(la[m], tv.z, xa.z); xa.w = fmaf(la[m], tv.w, xa.w);
-          xb.x = fmaf(lb[m], tv.x, xb.x); xb.y = fmaf(lb[m], tv.y, xb.y);
-          xb.z = fmaf(lb[m], tv.z, xb.z); xb.w = fmaf(lb[m], tv.w, xb.w);
-        }
-        *reinterpret_cast<float4*>(xp + r0 * 32 + c0) = xa;
-        *reinterpret_cast<float4*>(xp + (r0 + 1) * 32 + c0) = xb;
-      }
-      tc::named_barrier(kBarCrewX, kCrewThreads);
-      {
-        const int r0 = (cx >> 3) * 2, c0 = (cx & 7) * 4;
-        float ta[32], tb[32];
-#pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 va = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r0, 32 + 4 * i4));
-          const float4 vb = *reinterpret_cast<const float4*>(lf + lf_idx(33 + r0, 32 + 4 * i4));
-          ta[4 * i4] = va.x; ta[4 * i4 + 1] = va.y; ta[4 * i4 + 2] = va.z; ta[4 * i4 + 3] = va.w;
-          tb[4 * i4] = vb.x; tb[4 * i4 + 1] = vb.y; tb[4 * i4 + 2] = vb.z; tb[4 * i4 + 3] = vb.w;
-        }
-        float4 ya = make_float4(0.f, 0.f, 0.f, 0.f), yb = ya;
-#pragma unroll
-        for (int m = 0; m < 32; ++m) {
-          const float4 xv = *reinterpret_cast<const float4*>(xp + m * 32 + c0);
-          ya.x = fmaf(ta[m], xv.x, ya.x); ya.y = fmaf(ta[m], xv.y, ya.y);
-          ya.z = fmaf(ta[m], xv.z, ya.z); ya.w = fmaf(ta[m], xv.w, ya.w);
-          yb.x = fmaf(tb[m], xv.x, yb.x); yb.y = fmaf(tb[m], xv.y, yb.y);
-          yb.z = fmaf(tb[m], xv.z, yb.z); yb.w = fmaf(tb[m], xv.w, yb.w);
-        }
-        *reinterpret_cast<float4*>(lf + lf_idx(32 + r0, c0)) = make_float4(-ya.x, -ya.y, -ya.z, -ya.w);
-        *reinterpret_cast<float4*>(lf + lf_idx(33 + r0, c0)) = make_float4(-yb.x, -yb.y, -yb.z, -yb.w);
-      }
-      tc::named_barrier(kBarCrewX, kCrewThreads);
-    } else {
-      // ---- Kd = e^{gc_last-gc} K (fp16, rows t) for the consumer's state update ------
-      // KD[b] was last read by the state update of chunk c-2, which finished before
-      // this group handed over chunk c-1.
-      {
-        uint4 raw[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int it = cy + r * kCrewThreads, t = it & 63, cc = it >> 6;
-          raw[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16));
-        }
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int it = cy + r * kCrewThreads, t = it & 63, cc = it >> 6;
-          float f[8];
-          unpack_bf16x8(raw[r], f);
-          *reinterpret_cast<uint4*>(sm + kd_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
-              t < clen ? pack_half8(f, x.s_edec[t]) : make_uint4(0, 0, 0, 0);
-        }
-      }
-      if (pw == 4 && c + 1 < x.nchunks) load_gates(c + 1);
-      // ---- Q~ = e^gc Q / sqrt(dk) (fp16, rows t), once the spine of chunk c-1 read Q~ --
-      if (c > 0) ok = (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
-      {
-        uint4 raw[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int it = cy + r * kCrewThreads, t = it & 63, cc = it >> 6;
-          raw[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + 8192 + tc::sw128(t, (cc & 7) * 16));
-        }
-        if (ok) {
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const int it = cy + r * kCrewThreads, t = it & 63, cc = it >> 6;
-            float f[8];
-            unpack_bf16x8(raw[r], f);
-            *reinterpret_cast<uint4*>(sm + P::QT + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
-                t < clen ? pack_half8(f, x.s_eg[t] * kInvSqrtD) : make_uint4(0, 0, 0, 0);
-          }
-        }
-      }
-      if (pw == 4) tc::cp_async_wait_all();
-    }
-    if (!tc::barrier_all(kBarProducer, kProducerThreads, ok && *x.s_abort == 0)) {
-      if (leader) {
-        *x.s_abort = 1;
-        atomicOr(p.status, kStatusTimeout);
-      }
-      break;
-    }
-
-    // ---- bf16 hi/lo tiles of T diag(beta) and T diag(beta e^gc) (rows t, columns j) -----
-    {
-      const int t = ptid >> 2, j0 = (ptid & 3) * 16;
-#pragma unroll
-      for (int h8 = 0; h8 < 2; ++h8) {
-        const int jb = j0 + h8 * 8;
-        const float4 ta = *reinterpret_cast<const float4*>(lf + lf_idx(t, jb));
-        const float4 tb = *reinterpret_cast<const float4*>(lf + lf_idx(t, jb + 4));
-        const float4 ba = *reinterpret_cast<const float4*>(x.s_beta + jb);
-        const float4 bb4 = *reinterpret_cast<const float4*>(x.s_beta + jb + 4);
-        const float4 ea = *reinterpret_cast<const float4*>(x.s_ebg + jb);
-        const float4 eb4 = *reinterpret_cast<const float4*>(x.s_ebg + jb + 4);
-        const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
-        const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb4.x, bb4.y, bb4.z, bb4.w};
-        const float ev[8] = {ea.x, ea.y, ea.z, ea.w, eb4.x, eb4.y, eb4.z, eb4.w};
-        uint32_t bh[4], bl[4], wh[4], wl[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          split_bf162(tv[2 * e] * bv[2 * e], tv[2 * e + 1] * bv[2 * e + 1], bh[e], bl[e]);
-          split_bf162(tv[2 * e] * ev[2 * e], tv[2 * e + 1] * ev[2 * e + 1], wh[e], wl[e]);
-        }
-        const uint32_t o = tc::sw128(t, jb * 2);
-        *reinterpret_cast<uint4*>(sm + P::TB + o) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
-        *reinterpret_cast<uint4*>(sm + P::TB + 8192 + o) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
-        *reinterpret_cast<uint4*>(sm + P::TB + 16384 + o) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4*>(sm + P::TB + 24576 + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      for (int r = 0; r < 4; ++r) {
+        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
+        const bool live = t < clen;
+        const uint32_t o = kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16);
+        float f[8];
+        unpack_bf16x8(rk[r], f);
+        *reinterpret_cast<uint4*>(sm + o) = live ? pack_half8(f, x.s_eg[gs + t]) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sm + kd_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
+            live ? pack_half8(f, x.s_edec[gs + t]) : make_uint4(0, 0, 0, 0);
+        unpack_bf16x8(rq[r], f);
+        *reinterpret_cast<uint4*>(sm + o + 8192) =
+            live ? pack_half8(f, x.s_eg[gs + t] * kInvSqrtD) : make_uint4(0, 0, 0, 0);
       }
     }
     tc::fence_proxy_async();
+    tc::fence_before_sync();
+    if (!tc::barrier_all(kBarProducer, kProducerThreads, ok && *x.s_abort == 0)) {
+      if (leader) fail();
+      break;
+    }
 
-    // ---- U^T = V^T (T diag beta)^T and W^T = K^T (T diag(beta e^gc))^T, hi + lo each ----
+    // ---- U^T = V^T (T diag beta)^T and W^T = (e^gc K)^T (T diag beta)^T, hi + lo ---------
     // U^T goes to the chunk-parity half of the U columns, free once the consumer has
-    // read u of chunk c-2 (it signals every chunk; waiting for chunk c-1 covers it).
-    if (!group_wait(x, p, x.mb_v, b, kBarProducer, kProducerThreads, leader)) break;  // V tile of chunk c
-    if (c >= 2 && !group_wait(x, p, x.mb_cu, (c - 1) & 1, kBarProducer, kProducerThreads, leader)) break;
+    // read u of chunk c-2 (it signals each parity on its own barrier).
+    if (c >= 2 && !group_wait(x, p, b ? x.mb_cu1 : x.mb_cu0, ((c - 2) >> 1) & 1, kBarProducer, kProducerThreads,
+                              leader))
+      break;
     if (leader) {
       tc::fence_after_sync();
-      constexpr uint32_t id = tc::idesc_f16(128, 64, tc::kBF16, true, false);
+      constexpr uint32_t id = tc::idesc_f16(128, 64, tc::kF16, true, false);
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
 #pragma unroll
         for (int st = 0; st < 4; ++st)
-          tc::mma_f16(x.tmem + P::COL_U + 64 * b, tc::desc_sw128(x.sbase + P::VR + st * 2048, 8192, 1024),
-                      tc::desc_sw128(x.sbase + P::TB + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
+          tc::mma_f16(x.tmem + P::COL_U + 64 * b, tc::desc_sw128(x.sbase + v_off + st * 2048, 8192, 1024),
+                      tc::desc_sw128(x.sbase + tb_off + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
       }
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
 #pragma unroll
         for (int st = 0; st < 4; ++st)
           tc::mma_f16(x.tmem + P::COL_GW, tc::desc_sw128(x.sbase + kq_off + st * 2048, 16384, 1024),
-                      tc::desc_sw128(x.sbase + P::TB + 16384 + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
+                      tc::desc_sw128(x.sbase + tb_off + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
       }
       tc::mma_commit(x.mb_uw);
     }
-    if (!group_wait(x, p, x.mb_uw, b, kBarProducer, kProducerThreads, leader)) break;
-    if (leader) {  // this chunk's raw tiles are consumed: prefetch ahead
-      if (c + 1 < x.nchunks) issue_v(c + 1);
-      if (c + 2 < x.nchunks) issue_kq(c + 2);
+    // ---- meanwhile: the gates of the next chunk, into the other gate set (their copy
+    //      was started a chunk ago), and the copy of the gates of the chunk after -------
+    if (pw == 4 && c + 1 < x.nchunks) {
+      tc::cp_async_wait_all();
+      scan_gates(c + 1);
+      if (c + 2 < x.nchunks) load_gates(c + 2);
     }
+    if (!group_wait(x, p, x.mb_uw, b, kBarProducer, kProducerThreads, leader)) break;
+    if (leader && c + 2 < x.nchunks) issue_vt(c + 2);  // this chunk's V and T tiles are consumed
 
     // ---- -W^T as the spine's fp16 B operand (rows k, columns t) -----------------------
     {
@@ -635,6 +436,8 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     const int64_t rem = x.len - static_cast<int64_t>(c) * kChunk;
     const int clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
     const uint32_t kd_off = b ? P::KD1 : P::KD0;
+    const uint32_t kq_off = b ? P::KQ1 : P::KQ0;  // Q~ sits in the Q half of the K/Q tile
+    const uint32_t a_off = b ? P::A1 : P::A0;
     const uint32_t col_u = P::COL_U + 64 * b;
 
     if (!group_wait(x, p, x.mb_hand, b, kBarConsumer, kConsumerThreads, leader)) break;
@@ -647,13 +450,15 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
         const uint32_t a = x.tmem + P::COL_ST + st * 8;
         tc::mma_f16_ts(x.tmem + col_u, a, tc::desc_sw128(x.sbase + P::W16 + st * 2048, 16384, 1024), id_u, 1);
         tc::mma_f16_ts(x.tmem + P::COL_O, a,
-                       tc::desc_sw128(x.sbase + P::QT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024), id_o, st > 0);
+                       tc::desc_sw128(x.sbase + kq_off + (st >> 2) * 16384 + 8192 + (st & 3) * 32, 16, 1024), id_o,
+                       st > 0);
       }
       tc::mma_commit(x.mb_c1);
     }
-    // meanwhile: S^T <- e^{gc_last} S^T, the decay half of the state update
-    {
-      const float el = x.s_elast[b];
+    // meanwhile (first chunk only): S^T <- e^{gc_last} S^T, the decay half of the
+    // state update; later chunks get it from the previous chunk's last pass
+    if (c == 0) {
+      const float el = x.s_elast[0];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t s[32];
@@ -675,8 +480,13 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
         tc::tmem_ld32(lanes + col_u + h2 * 32, u);
         tc::tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          split_half2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1]), hi[e], lo[e]);
+        for (int e = 0; e < 16; ++e) {
+          // columns past the end of the sequence are zeroed: their U and W rows came
+          // from other tokens' T diag(beta) rows
+          const int t = h2 * 32 + 2 * e;
+          split_half2(t < clen ? __uint_as_float(u[2 * e]) : 0.f, t + 1 < clen ? __uint_as_float(u[2 * e + 1]) : 0.f,
+                      hi[e], lo[e]);
+        }
         tc::tmem_st16u(lanes + P::COL_UT + h2 * 16, hi);
         tc::tmem_st16u(lanes + P::COL_UT + 32 + h2 * 16, lo);
       }
@@ -687,14 +497,14 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     // ---- S^T += u^T Kd (the write half of the update) and O^T += u^T A^T (hi/lo x3) -------
     if (leader) {
       tc::fence_after_sync();
-      tc::mbar_arrive(x.mb_cu);  // the U columns of this chunk parity are free again
+      tc::mbar_arrive(b ? x.mb_cu1 : x.mb_cu0);  // the U columns of this chunk parity are free again
       constexpr uint32_t id_s = tc::idesc_f16(128, 128, tc::kF16, false, true);
       constexpr uint32_t id_o = tc::idesc_f16(128, 64, tc::kF16, false, false);
 #pragma unroll
       for (int st = 0; st < 4; ++st) {
         const uint32_t u_hi = x.tmem + P::COL_UT + st * 8, u_lo = x.tmem + P::COL_UT + 32 + st * 8;
-        const uint64_t a_hi = tc::desc_sw128(x.sbase + P::A16 + st * 32, 16, 1024);
-        const uint64_t a_lo = tc::desc_sw128(x.sbase + P::A16 + 8192 + st * 32, 16, 1024);
+        const uint64_t a_hi = tc::desc_sw128(x.sbase + a_off + st * 32, 16, 1024);
+        const uint64_t a_lo = tc::desc_sw128(x.sbase + a_off + 8192 + st * 32, 16, 1024);
         tc::mma_f16_ts(x.tmem + P::COL_S, u_hi, tc::desc_sw128(x.sbase + kd_off + st * 2048, 8192, 1024), id_s, 1);
         tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_hi, id_o, 1);
         tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_lo, id_o, 1);
@@ -704,8 +514,10 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     }
     if (!group_wait(x, p, x.mb_c2, b, kBarConsumer, kConsumerThreads, leader)) break;
 
-    // ---- next chunk's fp16 S^T operand, and this chunk's output rows -------------------
+    // ---- next chunk's fp16 S^T operand and decayed state, and this chunk's output ------
     {
+      const bool more = c + 1 < x.nchunks;
+      const float el = more ? x.s_elast[(c + 1) % 3] : 1.f;  // published by the hand-off of chunk c
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t s[32], st[16];
@@ -714,6 +526,11 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
 #pragma unroll
         for (int e = 0; e < 16; ++e) st[e] = pack_half2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]));
         tc::tmem_st16u(lanes + P::COL_ST + q4 * 16, st);
+        if (more) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[e] = __float_as_uint(el * __uint_as_float(s[e]));
+          tc::tmem_st32(lanes + P::COL_S + q4 * 32, s);
+        }
       }
       // O^T holds one value column per thread; an 8-row x 32-column staging tile per
       // warp turns it into 16-byte row segments for coalesced global stores.
@@ -760,14 +577,15 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
 template <int kUnused = 0>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, const ChunkParams p) {
+                   const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_t,
+                   const ChunkParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(16) float s_gc[kChunk], s_eg[kChunk], s_edec[kChunk], s_ebg[kChunk], s_beta[kChunk];
-  __shared__ __align__(16) float s_E[kChunk], s_F[kChunk], s_gstage[2 * 2 * kChunk];
-  __shared__ float s_elast[2];
-  __shared__ int s_fast;
+  __shared__ __align__(16) float s_gc[2 * kChunk], s_eg[2 * kChunk], s_edec[2 * kChunk];
+  __shared__ __align__(16) float s_E[2 * kChunk], s_F[2 * kChunk], s_gstage[2 * kChunk];
+  __shared__ float s_elast[3];
+  __shared__ int s_fast[2];
   __shared__ __align__(16) uint16_t s_ostage[kConsumerWarps * 256];
-  __shared__ __align__(8) uint64_t s_mb[9];
+  __shared__ __align__(8) uint64_t s_mb[11];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -804,30 +622,30 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.s_gc = s_gc;
   x.s_eg = s_eg;
   x.s_edec = s_edec;
-  x.s_ebg = s_ebg;
-  x.s_beta = s_beta;
   x.s_elast = s_elast;
   x.s_E = s_E;
   x.s_F = s_F;
-  x.s_fast = &s_fast;
+  x.s_fast = s_fast;
   x.s_gstage = s_gstage;
   x.s_ostage = s_ostage;
   x.s_abort = &s_abort;
   x.mb_kq0 = tc::smem_u32(&s_mb[0]);
   x.mb_kq1 = tc::smem_u32(&s_mb[1]);
-  x.mb_v = tc::smem_u32(&s_mb[2]);
-  x.mb_g = tc::smem_u32(&s_mb[3]);
-  x.mb_uw = tc::smem_u32(&s_mb[4]);
-  x.mb_c1 = tc::smem_u32(&s_mb[5]);
-  x.mb_c2 = tc::smem_u32(&s_mb[6]);
-  x.mb_hand = tc::smem_u32(&s_mb[7]);
-  x.mb_cu = tc::smem_u32(&s_mb[8]);
+  x.mb_v0 = tc::smem_u32(&s_mb[2]);
+  x.mb_v1 = tc::smem_u32(&s_mb[3]);
+  x.mb_g = tc::smem_u32(&s_mb[4]);
+  x.mb_uw = tc::smem_u32(&s_mb[5]);
+  x.mb_c1 = tc::smem_u32(&s_mb[6]);
+  x.mb_c2 = tc::smem_u32(&s_mb[7]);
+  x.mb_hand = tc::smem_u32(&s_mb[8]);
+  x.mb_cu0 = tc::smem_u32(&s_mb[9]);
+  x.mb_cu1 = tc::smem_u32(&s_mb[10]);
 
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), Plan::TMEM_COLS);
   if (tid == 0) {
     s_abort = 0;
 #pragma unroll
-    for (int i = 0; i < 9; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), 1);
+    for (int i = 0; i < 11; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), 1);
     tc::mbar_fence_init();
   }
   tc::fence_before_sync();
@@ -838,7 +656,7 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   if (warp < kConsumerWarps)
     consumer_role(x, p, tid);
   else
-    producer_role(x, p, &tmap_q, &tmap_k, &tmap_v, tid - kConsumerThreads);
+    producer_role(x, p, &tmap_q, &tmap_k, &tmap_v, &tmap_t, tid - kConsumerThreads);
 
   tc::fence_before_sync();
   __syncthreads();

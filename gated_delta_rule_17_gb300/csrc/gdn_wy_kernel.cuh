@@ -1,0 +1,445 @@
+// Chunk-parallel WY solve of the GDN prefill for sm_103a.
+//
+// The first of the three stages of the GDN prefill op (ssm_gdn_a3.rs, doc
+// comment of `gdn_prefill_fla`: the per-chunk solve of (I + L) U = beta V and
+// (I + L) W = beta e^gc K) depends on no state, so it runs for every (chunk,
+// v-head) at once. For each such item the kernel computes
+//
+//     gc = cumsum(g);  L_tj = beta_t e^{gc_t - gc_j} k_t.k_j  (j < t);
+//     T = (I + L)^{-1}   (fp32, blocked, on the CUDA cores)
+//
+// and writes T diag(beta) as an fp16 hi + lo pair (about 22 significant bits)
+// for the spine kernel, which forms U = (T diag beta) V and
+// W = (T diag beta) diag(e^gc) K on the tensor cores.
+//
+// Hand-off: row t of a chunk's T diag(beta) (64 hi then 64 lo fp16 values,
+// 256 bytes) is written over the output slice of the same token and head,
+// out[row, h, 0:128], which the spine kernel reads back before it overwrites
+// it with that token's output. The op therefore needs no scratch buffer, and
+// no row outside the batch's own output is touched.
+//
+// The kernel is persistent: a few CTAs per SM each walk a strided list of
+// items, and while one item is being solved the K tile (TMA) and the gates
+// (cp.async) of the CTA's next item are already in flight. Items are ordered
+// head-fastest, so the v-heads that share a key head read its K tile close
+// together in time (the second read hits L2).
+#pragma once
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+constexpr int kWyThreads = 128;
+constexpr int kWyCtasPerSm = 4;
+
+struct WyParams {
+  const float* g;
+  const float* beta;
+  uint16_t* tb;               // the output tensor, reused for the fp16 T diag(beta) rows
+  const int32_t* cu_seqlens;  // null for dense batches
+  const int32_t* cu_chunks;   // varlen: chunk prefix over the sequences, [B + 1]
+  unsigned* status;
+  int64_t g_stride, beta_stride, out_stride;
+  int64_t items;              // dense: chunks * nv; varlen: an upper bound on it
+  int B, T, nk, nv;
+  int chunks_per_seq;         // dense batches: ceil(T / 64)
+};
+
+struct WyPlan {
+  static constexpr int K0 = 0;              // raw bf16 K tile (2 blocks x 64 rows), item parity 0;
+  static constexpr int K1 = 16384;          //   once its Gram MMA is done it holds the inverse's scratch
+  static constexpr int LF = 32768;          // fp32 64 x 64 L, overwritten by T
+  static constexpr int BYTES = LF + 16384;
+  static constexpr int DYN_SMEM = BYTES + 1024;  // slack for 1024-byte alignment
+  // scratch inside the item's own (consumed) K tile
+  static constexpr int S_LT = 0;       // fp32 4 x 16 x 16 diagonal blocks of L, transposed
+  static constexpr int S_X16 = 4096;   // fp32 2 x 16 x 16 partial products
+  static constexpr int S_X32 = 8192;   // fp32 32 x 32 partial product, rows padded to 36 floats
+  static constexpr uint32_t TMEM_COLS = 64;  // K K^T, M = 64
+};
+
+struct WyItem {
+  int64_t row0;
+  int clen;  // tokens of the chunk; 0 for an item that writes nothing
+  int h, kh;
+};
+
+// Item -> (rows, head). Items of malformed sequences (reported by the schedule
+// kernel) keep a valid tile position but write nothing.
+__device__ __forceinline__ WyItem wy_locate(const WyParams& p, int64_t item) {
+  WyItem w;
+  w.h = static_cast<int>(item % p.nv);
+  w.kh = w.h / (p.nv / p.nk);
+  w.row0 = 0;
+  w.clen = 0;
+  const int64_t xc = item / p.nv;
+  if (p.cu_seqlens) {
+    int lo = 0, hi = p.B;  // cu_chunks[lo] <= xc < cu_chunks[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.cu_chunks[mid] <= xc) lo = mid; else hi = mid;
+    }
+    const int a = p.cu_seqlens[lo], e = p.cu_seqlens[lo + 1];
+    const int64_t c = xc - p.cu_chunks[lo];
+    if (a < 0 || e < a || e > p.T || c < 0) return w;
+    const int64_t rem = static_cast<int64_t>(e - a) - c * kChunk;
+    if (rem <= 0) return w;
+    w.row0 = a + c * kChunk;
+    w.clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
+  } else {
+    const int64_t s = xc / p.chunks_per_seq, c = xc % p.chunks_per_seq;
+    const int64_t rem = static_cast<int64_t>(p.T) - c * kChunk;
+    w.row0 = s * p.T + c * kChunk;
+    w.clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
+  }
+  return w;
+}
+
+__global__ void __launch_bounds__(kWyThreads, kWyCtasPerSm)
+gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
+  using P = WyPlan;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(16) float s_gc[kChunk], s_beta[kChunk], s_E[kChunk], s_F[kChunk];
+  __shared__ __align__(16) float s_gstage[2][2 * kChunk];  // g, beta of an item, by parity
+  __shared__ int s_fast;
+  __shared__ __align__(8) uint64_t s_mb[3];
+  __shared__ uint32_t s_tmem;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  int64_t items = p.items;
+  if (p.cu_seqlens) {
+    const int64_t have = static_cast<int64_t>(p.cu_chunks[p.B]) * p.nv;
+    if (have < items) items = have;
+  }
+  if (static_cast<int64_t>(blockIdx.x) >= items) return;
+
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = tc::smem_u32(sm);
+  float* lf = reinterpret_cast<float*>(sm + P::LF);
+  const uint32_t mb_g = tc::smem_u32(&s_mb[2]);
+
+  // TMA of an item's K tile into buffer `kb` (thread 32), and cp.async of its
+  // gates into stage `kb` (warp 1)
+  auto prefetch = [&](const WyItem& w, int kb) {
+    if (tid == 32) {
+      const uint32_t mb = tc::smem_u32(&s_mb[kb]);
+      tc::mbar_arrive_expect_tx(mb, 16384);
+      const uint32_t dst = sbase + (kb ? P::K1 : P::K0);
+      tc::tma_load_2d(dst, &tmap_k, w.kh * kDim, static_cast<int32_t>(w.row0), mb);
+      tc::tma_load_2d(dst + 8192, &tmap_k, w.kh * kDim + 64, static_cast<int32_t>(w.row0), mb);
+    }
+    if (warp == 1) {
+      float* st = s_gstage[kb];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = 2 * lane + e;
+        if (t < w.clen) {
+          const int64_t r = w.row0 + t;
+          tc::cp_async_4(tc::smem_u32(st + t), p.g + r * p.g_stride + w.h);
+          tc::cp_async_4(tc::smem_u32(st + kChunk + t), p.beta + r * p.beta_stride + w.h);
+        } else {
+          st[t] = 0.f;
+          st[kChunk + t] = 0.f;
+        }
+      }
+      tc::cp_async_commit();
+    }
+  };
+
+  if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), P::TMEM_COLS);
+  if (tid == 32) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), 1);
+    tc::mbar_fence_init();
+  }
+  WyItem cur = wy_locate(p, blockIdx.x);
+  prefetch(cur, 0);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  bool ok = true, failed = false;
+
+  int n = 0;
+  for (int64_t it = blockIdx.x; it < items; it += gridDim.x, ++n) {
+    const int kb = n & 1;
+    const uint32_t kuse = (n >> 1) & 1;  // phase parity of this item's K buffer
+    const uint32_t k_off = kb ? P::K1 : P::K0;
+    float* lt = reinterpret_cast<float*>(sm + k_off + P::S_LT);
+    float* x16 = reinterpret_cast<float*>(sm + k_off + P::S_X16);
+    float* x32 = reinterpret_cast<float*>(sm + k_off + P::S_X32);
+    const int clen = cur.clen;
+
+    // ---- the next item's tiles go in flight while this one is solved ------------------
+    const int64_t nx = it + gridDim.x;
+    WyItem nxt = cur;
+    if (nx < items) {
+      nxt = wy_locate(p, nx);
+      prefetch(nxt, kb ^ 1);
+    }
+
+    // ---- gates (warp 1; padding tokens: g = 0, beta = 0) -------------------------------
+    if (warp == 1) {
+      if (nx < items) tc::cp_async_wait_1(); else tc::cp_async_wait_all();
+      __syncwarp();
+      const float* st = s_gstage[kb];
+      const GatePrefix gp = gate_prefix(st[2 * lane], st[2 * lane + 1]);
+      const float mid = 0.5f * (gp.first + gp.last);
+      s_gc[2 * lane] = gp.gca;
+      s_gc[2 * lane + 1] = gp.gcb;
+      s_beta[2 * lane] = st[kChunk + 2 * lane];
+      s_beta[2 * lane + 1] = st[kChunk + 2 * lane + 1];
+      s_E[2 * lane] = __expf(gp.gca - mid);
+      s_E[2 * lane + 1] = __expf(gp.gcb - mid);
+      s_F[2 * lane] = __expf(mid - gp.gca);
+      s_F[2 * lane + 1] = __expf(mid - gp.gcb);
+      if (lane == 0) s_fast = (gp.first - gp.last) <= kFactorisedRange;
+    }
+
+    // ---- K K^T (bf16, M = 64, N = 64, K = 128) into tensor memory ----------------------
+    if (tid == 0) {
+      ok = tc::mbar_wait_timed(tc::smem_u32(&s_mb[kb]), kuse, kWaitLimitNs);
+      if (ok) {
+        tc::fence_after_sync();
+        constexpr uint32_t idesc = tc::idesc_f16(64, 64, tc::kBF16, false, false);
+#pragma unroll
+        for (int st = 0; st < 8; ++st) {
+          const uint32_t a = sbase + k_off + (st >> 2) * 8192 + (st & 3) * 32;
+          tc::mma_f16(tmem, tc::desc_sw128(a, 16, 1024), tc::desc_sw128(a, 16, 1024), idesc, st > 0);
+        }
+        tc::mma_commit(mb_g);
+      }
+    }
+    if (!__syncthreads_and(ok)) {
+      failed = true;
+      break;
+    }
+    ok = tc::mbar_wait_timed(mb_g, n & 1, kWaitLimitNs);
+    if (!__syncthreads_and(ok)) {
+      failed = true;
+      break;
+    }
+    tc::fence_after_sync();
+
+    // ---- L (fp32): row t = 16 warp + l sits in lane 32 warp + l (M = 64 layout) --------
+    {
+      uint32_t d[2][32];
+      tc::tmem_ld32(tmem + ((warp * 32u) << 16), d[0]);
+      tc::tmem_ld32(tmem + ((warp * 32u) << 16) + 32, d[1]);
+      tc::tmem_ld_wait();
+      if (lane < 16) {
+        const int t = 16 * warp + lane;
+        const bool live = t < clen;
+        const bool fast = s_fast != 0;
+        const float bt = live ? s_beta[t] : 0.f, be = bt * s_E[t], gt = s_gc[t];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float l[32];
+          if (fast) {
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const float4 f4 = *reinterpret_cast<const float4*>(s_F + hf * 32 + 4 * e4);
+              const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int e = 4 * e4 + q, j = hf * 32 + e;
+                l[e] = j < t ? be * fv[q] * __uint_as_float(d[hf][e]) : 0.f;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int j = hf * 32 + e;
+              l[e] = j < t ? bt * __expf(gt - s_gc[j]) * __uint_as_float(d[hf][e]) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4)
+            *reinterpret_cast<float4*>(lf + lf_idx(t, hf * 32 + j4 * 4)) =
+                make_float4(l[4 * j4], l[4 * j4 + 1], l[4 * j4 + 2], l[4 * j4 + 3]);
+          // this row's part of its diagonal 16 x 16 block (block `warp`), transposed
+          if ((warp >> 1) == hf) {
+            float* dst = lt + warp * 256 + lane;
+            if (warp & 1) {
+#pragma unroll
+              for (int m = 0; m < 16; ++m) dst[m * 16] = l[16 + m];
+            } else {
+#pragma unroll
+              for (int m = 0; m < 16; ++m) dst[m * 16] = l[m];
+            }
+          }
+        }
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+
+    // ---- T = (I + L)^{-1} in fp32, in place over L ---------------------------------------
+    // (a) the four diagonal 16 x 16 blocks: one column per thread (lanes 0-15 of
+    //     warp w invert block w), right-looking substitution; column m of a block
+    //     comes from its transposed copy as broadcast loads.
+    if (lane < 16) {
+      const int r0 = 16 * warp;
+      const float* ltb = lt + warp * 256;
+      float xv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xv[i] = (i == lane) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < 15; ++m) {
+        float lc[16];
+#pragma unroll
+        for (int i4 = (m + 1) >> 2; i4 < 4; ++i4) {
+          const float4 v4 = *reinterpret_cast<const float4*>(ltb + m * 16 + 4 * i4);
+          lc[4 * i4] = v4.x;
+          lc[4 * i4 + 1] = v4.y;
+          lc[4 * i4 + 2] = v4.z;
+          lc[4 * i4 + 3] = v4.w;
+        }
+        const float xm = xv[m];
+#pragma unroll
+        for (int i = m + 1; i < 16; ++i) xv[i] = fmaf(-lc[i], xm, xv[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) lf[lf_idx(r0 + i, r0 + lane)] = xv[i];
+    }
+    __syncthreads();
+    // (b) the 16 x 16 blocks (1,0) and (3,2) of T: X = L_{i,i-1} T_{i-1,i-1}, then
+    //     T_{i,i-1} = -T_ii X; threads 0-63 take block (1,0), 64-127 block (3,2),
+    //     1 x 4 outputs each.
+    {
+      const int blk = tid >> 6, r = (tid >> 2) & 15, c0 = (tid & 3) * 4;
+      const int rr = 32 * blk + 16 + r, cb = 32 * blk;
+      float lrow[16];
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(rr, cb + 4 * i4));
+        lrow[4 * i4] = v4.x; lrow[4 * i4 + 1] = v4.y; lrow[4 * i4 + 2] = v4.z; lrow[4 * i4 + 3] = v4.w;
+      }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float4 tv = *reinterpret_cast<const float4*>(lf + lf_idx(cb + m, cb + c0));
+        acc.x = fmaf(lrow[m], tv.x, acc.x); acc.y = fmaf(lrow[m], tv.y, acc.y);
+        acc.z = fmaf(lrow[m], tv.z, acc.z); acc.w = fmaf(lrow[m], tv.w, acc.w);
+      }
+      *reinterpret_cast<float4*>(x16 + blk * 256 + r * 16 + c0) = acc;
+    }
+    __syncthreads();
+    {
+      const int blk = tid >> 6, r = (tid >> 2) & 15, c0 = (tid & 3) * 4;
+      const int rr = 32 * blk + 16 + r, cb = 32 * blk + 16;
+      float trow[16];
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(rr, cb + 4 * i4));
+        trow[4 * i4] = v4.x; trow[4 * i4 + 1] = v4.y; trow[4 * i4 + 2] = v4.z; trow[4 * i4 + 3] = v4.w;
+      }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {  // T_ii[r][m] = 0 for m > r
+        const float4 xv = *reinterpret_cast<const float4*>(x16 + blk * 256 + m * 16 + c0);
+        acc.x = fmaf(trow[m], xv.x, acc.x); acc.y = fmaf(trow[m], xv.y, acc.y);
+        acc.z = fmaf(trow[m], xv.z, acc.z); acc.w = fmaf(trow[m], xv.w, acc.w);
+      }
+      *reinterpret_cast<float4*>(lf + lf_idx(rr, cb - 16 + c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    }
+    __syncthreads();
+    // (c) lower-left 32 x 32: X = L[32:64, 0:32] T[0:32, 0:32]. Lane = row, warp w
+    //     takes columns 8w..8w+7, for which T[m][c] = 0 unless m >= 8w.
+    {
+      const int r = lane, c0 = 8 * warp;
+      float lrow[32];
+#pragma unroll
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 4 * i4));
+        lrow[4 * i4] = v4.x; lrow[4 * i4 + 1] = v4.y; lrow[4 * i4 + 2] = v4.z; lrow[4 * i4 + 3] = v4.w;
+      }
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        if (m >= c0) {  // warp-uniform
+          const float4 ta = *reinterpret_cast<const float4*>(lf + lf_idx(m, c0));
+          const float4 tb = *reinterpret_cast<const float4*>(lf + lf_idx(m, c0 + 4));
+          acc[0] = fmaf(lrow[m], ta.x, acc[0]); acc[1] = fmaf(lrow[m], ta.y, acc[1]);
+          acc[2] = fmaf(lrow[m], ta.z, acc[2]); acc[3] = fmaf(lrow[m], ta.w, acc[3]);
+          acc[4] = fmaf(lrow[m], tb.x, acc[4]); acc[5] = fmaf(lrow[m], tb.y, acc[5]);
+          acc[6] = fmaf(lrow[m], tb.z, acc[6]); acc[7] = fmaf(lrow[m], tb.w, acc[7]);
+        }
+      }
+      *reinterpret_cast<float4*>(x32 + r * 36 + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(x32 + r * 36 + c0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    __syncthreads();
+    // (d) T[32:64, 0:32] = -T[32:64, 32:64] X. Lane = row, warp w takes columns 8w..8w+7.
+    {
+      const int r = lane, c0 = 8 * warp;
+      float trow[32];
+#pragma unroll
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 32 + 4 * i4));
+        trow[4 * i4] = v4.x; trow[4 * i4 + 1] = v4.y; trow[4 * i4 + 2] = v4.z; trow[4 * i4 + 3] = v4.w;
+      }
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {  // T[32+r][32+m] = 0 for m > r
+        const float4 xa = *reinterpret_cast<const float4*>(x32 + m * 36 + c0);
+        const float4 xb = *reinterpret_cast<const float4*>(x32 + m * 36 + c0 + 4);
+        acc[0] = fmaf(trow[m], xa.x, acc[0]); acc[1] = fmaf(trow[m], xa.y, acc[1]);
+        acc[2] = fmaf(trow[m], xa.z, acc[2]); acc[3] = fmaf(trow[m], xa.w, acc[3]);
+        acc[4] = fmaf(trow[m], xb.x, acc[4]); acc[5] = fmaf(trow[m], xb.y, acc[5]);
+        acc[6] = fmaf(trow[m], xb.z, acc[6]); acc[7] = fmaf(trow[m], xb.w, acc[7]);
+      }
+      *reinterpret_cast<float4*>(lf + lf_idx(32 + r, c0)) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+      *reinterpret_cast<float4*>(lf + lf_idx(32 + r, c0 + 4)) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
+    }
+    __syncthreads();
+
+    // ---- T diag(beta) as fp16 hi + lo over the output rows of the chunk ------------------
+    // Thread pair (2t, 2t+1) writes row t: 32 columns each, hi at [0, 64), lo at [64, 128).
+    {
+      const int t = tid >> 1, j0 = (tid & 1) * 32;
+      if (t < clen) {
+        uint16_t* dst = p.tb + (cur.row0 + t) * p.out_stride + static_cast<int64_t>(cur.h) * kDim;
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const int jb = j0 + q8 * 8;
+          const float4 ta = *reinterpret_cast<const float4*>(lf + lf_idx(t, jb));
+          const float4 tb = *reinterpret_cast<const float4*>(lf + lf_idx(t, jb + 4));
+          const float4 ba = *reinterpret_cast<const float4*>(s_beta + jb);
+          const float4 bb = *reinterpret_cast<const float4*>(s_beta + jb + 4);
+          uint32_t hi[4], lo[4];
+          split_half2(ta.x * ba.x, ta.y * ba.y, hi[0], lo[0]);
+          split_half2(ta.z * ba.z, ta.w * ba.w, hi[1], lo[1]);
+          split_half2(tb.x * bb.x, tb.y * bb.y, hi[2], lo[2]);
+          split_half2(tb.z * bb.z, tb.w * bb.w, hi[3], lo[3]);
+          *reinterpret_cast<uint4*>(dst + jb) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(dst + 64 + jb) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+    }
+    // this item's K buffer (now scratch) is refilled by TMA two items on
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    cur = nxt;
+  }
+
+  if (failed) {
+    if (tid == 0) atomicOr(p.status, kStatusTimeout);
+    // give any copy or MMA still in flight time to land before the CTA exits
+    const uint64_t t0 = tc::globaltimer_ns();
+    while (tc::globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+  } else if (warp == 1) {
+    tc::cp_async_wait_all();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, P::TMEM_COLS);
+  }
+}
+
+}  // namespace gdn

@@ -271,6 +271,8 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst_saddr, const void* src) 
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// all but the most recently committed group have completed
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // ---- TMA ----------------------------------------------------------------------
 // 2-D tiled bulk tensor load into shared memory, completing on an mbarrier.

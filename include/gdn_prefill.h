@@ -13,8 +13,11 @@
  * and leaving S_T there. It is evaluated in chunks of 64 tokens in WY form:
  * a per-chunk triangular solve (the op's recompute_wu stage), a serial state
  * spine over chunks (its chunk_delta_h stage) and the chunk-parallel output
- * (its chunk_fwd_o stage). Here the three stages run inside one kernel per
- * (sequence, v-head, v-column slice), so the stage hand-offs stay on chip.
+ * (its chunk_fwd_o stage). Here the triangular solve runs chunk-parallel in
+ * one kernel (a CTA per chunk and v-head) and hands T diag(beta) to a second,
+ * fused kernel (a CTA per sequence and v-head) that forms the WY products,
+ * runs the spine and writes the output, so the state and the other stage
+ * hand-offs stay on chip.
  *
  * All entry points are plain C; pointers marked "device" are CUDA device
  * (or managed) addresses on the current device, `stream` is a cudaStream_t
@@ -73,7 +76,12 @@ typedef struct {
  *   h_state_inout : device fp32 state, see state_is_table; read as S_0 and
  *             overwritten with S_T of each sequence, k-major ([dk][dv]).
  *   out     : device bf16 [rows][nv][dv] at row stride strides->out;
- *             every row of every sequence is written, nothing else.
+ *             every row of every sequence is written, nothing else. The
+ *             call also uses these rows as its hand-off between the two
+ *             kernels (each chunk's T diag(beta) sits in its own tokens'
+ *             rows until their outputs replace it), so `out` must not
+ *             overlap any input, and its contents are defined only once the
+ *             stream has passed the call.
  *   B, T    : dense (cu_seqlens == NULL): B sequences of T tokens, row
  *             r = b*T + t. Varlen: B sequences packed into T rows in total,
  *             sequence s owns rows [cu_seqlens[s], cu_seqlens[s+1]).
@@ -85,9 +93,10 @@ typedef struct {
  *             affected sequences write nothing and gdn_prefill_check reports
  *             GDN_ERR_DEVICE_STATUS.
  *   stream  : cudaStream_t as void*.
- * Numerics: products run on the tensor cores with fp16 operands and fp32
- * accumulation; the state is carried in fp32. Inputs must keep |v|, |S| and
- * intermediate values inside the fp16 range (about 6.5e4).
+ * Numerics: products run on the tensor cores with fp16 operands (split into
+ * hi + lo pairs where the output needs it) and fp32 accumulation; the
+ * triangular solve and the state are carried in fp32. Inputs must keep |v|,
+ * |S| and intermediate values inside the fp16 range (about 6.5e4).
  * Allocation: needs gdn_prefill_workspace_bytes() of device scratch, which
  * this call allocates and frees stream-ordered (cudaMallocAsync /
  * cudaFreeAsync); use gdn_prefill_ex to supply it instead.
@@ -99,7 +108,8 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
                 const gdn_strides_t* strides, const int32_t* cu_seqlens, void* stream);
 
 /* Bytes of device scratch gdn_prefill_ex needs for these sizes (0 for dense
- * batches; a per-sequence schedule for varlen ones). */
+ * batches; for varlen ones a schedule of 2B + 1 int32: the sequence order
+ * and the chunk prefix over the sequences, rounded up to 256 bytes). */
 size_t gdn_prefill_workspace_bytes(int B, int T, int nv, int dk, int dv, int varlen);
 
 /* gdn_prefill with caller-provided scratch: `workspace` is a device buffer
@@ -117,8 +127,8 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
  * bound loop where a cudaMalloc could block or fail. It has no counterpart
  * in the GDN prefill op; it exists only so those callers can use the library.
  * Same arguments and semantics as gdn_prefill. The varlen schedule it needs
- * lives in a static device array of GDN_NOALLOC_MAX_SEQS int32 entries (64
- * KiB) that each GPU holds from library load until process exit; varlen
+ * lives in a static device array of 2 * GDN_NOALLOC_MAX_SEQS + 1 int32
+ * entries (128 KiB) that each GPU holds from library load until process exit; varlen
  * calls with B > GDN_NOALLOC_MAX_SEQS return GDN_ERR_UNSUPPORTED, dense
  * calls have no limit. It calls no cudaMalloc, cudaFree or other allocating
  * routine. The first call on a device looks up that array's device address

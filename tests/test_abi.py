@@ -111,7 +111,7 @@ def test_empty_problem_is_a_no_op(lib):
 def test_workspace_sizes(lib):
     assert lib.gdn_prefill_workspace_bytes(4, 8192, 32, 128, 128, 0) == 0
     assert lib.gdn_prefill_workspace_bytes(8, 64000, 48, 128, 128, 1) == 256
-    assert lib.gdn_prefill_workspace_bytes(100, 64000, 48, 128, 128, 1) == 512
+    assert lib.gdn_prefill_workspace_bytes(100, 64000, 48, 128, 128, 1) == 1024
 
 
 def test_ex_rejects_small_workspace(lib):
