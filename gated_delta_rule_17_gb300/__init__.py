@@ -11,7 +11,8 @@ import ctypes
 import os
 import threading
 
-__all__ = ["prefill", "prefill_noalloc", "NOALLOC_MAX_SEQS", "workspace_bytes", "check", "last_launch_count", "lib_path", "load", "GdnError",
+__all__ = ["prefill", "prefill_noalloc", "NOALLOC_MAX_SEQS", "workspace_bytes", "check", "last_launch_count",
+           "set_timing_events", "lib_path", "load", "GdnError",
            "Strides", "GDN_OK", "GDN_ERR_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
            "GDN_ERR_DEVICE_STATUS", "GDN_ERR_TIMEOUT"]
 
@@ -65,6 +66,8 @@ def load():
             lib.gdn_last_launch_count.restype = i
             lib.gdn_prefill_noalloc.argtypes = common + [vp]
             lib.gdn_prefill_noalloc.restype = i
+            lib.gdn_set_timing_events.argtypes = [vp, vp, vp]
+            lib.gdn_set_timing_events.restype = None
             del i64
             _lib = lib
     return _lib
@@ -193,3 +196,12 @@ def check(stream=None) -> None:
 
 def last_launch_count() -> int:
     return int(load().gdn_last_launch_count())
+
+
+def set_timing_events(before_wy=None, before_spine=None, after_spine=None) -> None:
+    """Have later calls on this thread record these torch.cuda.Events (or None) before
+    the WY-solve kernel, between the kernels and after the spine kernel. torch creates
+    an event's CUDA handle on its first record, so record each once beforehand."""
+    def handle(e):
+        return None if e is None else e.cuda_event
+    load().gdn_set_timing_events(handle(before_wy), handle(before_spine), handle(after_spine))

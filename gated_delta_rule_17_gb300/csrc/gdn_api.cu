@@ -24,6 +24,7 @@ namespace {
 
 thread_local char g_err[512] = "";
 thread_local int g_launches = 0;
+thread_local cudaEvent_t g_timing[3] = {nullptr, nullptr, nullptr};  // gdn_set_timing_events
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -192,7 +193,9 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   // count (sum of ceil(len / 64) <= T / 64 + B), the excess CTAs exit at once
   const int64_t wy_chunks = cu ? static_cast<int64_t>(T) / gdn::kChunk + B + 1
                                : static_cast<int64_t>(w.chunks_per_seq) * B;
-  w.items = wy_chunks * nv;
+  if (wy_chunks * nv + static_cast<int64_t>(d->sms) * gdn::kWyCtasPerSm > INT32_MAX)
+    return fail(GDN_ERR_UNSUPPORTED, "%lld (chunk, head) items exceed the 2^31 item range", (long long)(wy_chunks * nv));
+  w.items = static_cast<int>(wy_chunks * nv);
   // persistent: a few CTAs per SM walk the items
   const int64_t wy_grid = w.items < static_cast<int64_t>(d->sms) * gdn::kWyCtasPerSm
                               ? w.items : static_cast<int64_t>(d->sms) * gdn::kWyCtasPerSm;
@@ -216,8 +219,10 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
     gdn_schedule_kernel<<<(B + 255) / 256, 256, 0, stream>>>(cu, B, T, order, cu_chunks, d->status);
     ++launches;
   }
+  if (g_timing[0]) cudaEventRecord(g_timing[0], stream);
   gdn::gdn_wy_kernel<<<static_cast<unsigned>(wy_grid), gdn::kWyThreads, gdn::WyPlan::DYN_SMEM, stream>>>(mk, w);
   ++launches;
+  if (g_timing[1]) cudaEventRecord(g_timing[1], stream);
   // one CTA per (sequence, v-head); CTAs of the same sequence and GQA group are
   // adjacent so their shared q/k tiles meet in L2
   const int64_t grid = static_cast<int64_t>(B) * nv;
@@ -225,6 +230,7 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt,
                                                                                                       p);
   ++launches;
+  if (g_timing[2]) cudaEventRecord(g_timing[2], stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   g_launches = launches;
@@ -360,5 +366,11 @@ int gdn_prefill_check(void* stream) {
 const char* gdn_last_error(void) { return g_err; }
 
 int gdn_last_launch_count(void) { return g_launches; }
+
+void gdn_set_timing_events(void* before_wy, void* before_spine, void* after_spine) {
+  g_timing[0] = static_cast<cudaEvent_t>(before_wy);
+  g_timing[1] = static_cast<cudaEvent_t>(before_spine);
+  g_timing[2] = static_cast<cudaEvent_t>(after_spine);
+}
 
 }  // extern "C"

@@ -59,6 +59,16 @@ __device__ __forceinline__ void split_half2(float a, float b, uint32_t& hi, uint
   lo = *reinterpret_cast<const uint32_t*>(&y);
 }
 
+// (a, b) = hi + lo with hi = bf16(x), lo = bf16(x - hi): about 16 significant bits,
+// with fp32's exponent range.
+__device__ __forceinline__ void split_bf162(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 x = __floats2bfloat162_rn(a, b);
+  const float2 xf = __bfloat1622float2(x);
+  const __nv_bfloat162 y = __floats2bfloat162_rn(a - xf.x, b - xf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&x);
+  lo = *reinterpret_cast<const uint32_t*>(&y);
+}
+
 // Inclusive in-chunk prefix of the log-gates held by one warp, lane l holding
 // tokens 2l and 2l+1 (padding tokens carry g = 0).
 struct GatePrefix {

@@ -65,13 +65,13 @@ struct ChunkParams {
 // rows are M/N, or as an MN-major operand whose rows are K.
 struct Plan {
   static constexpr int KQ0 = 0;            // raw bf16 [K;Q] (2 blocks x 128 rows), chunk parity 0; K becomes
-  static constexpr int KQ1 = KQ0 + 32768;  //   fp16 e^gc K and Q fp16 e^gc Q / sqrt(dk) in place; ... parity 1
+  static constexpr int KQ1 = KQ0 + 32768;  //   fp16 e^gc K in place; ... parity 1
   static constexpr int V0 = KQ1 + 32768;   // raw bf16 V (2 blocks x 64 rows), made fp16 in place
   static constexpr int V1 = V0 + 16384;
-  static constexpr int TB0 = V1 + 16384;   // fp16 T diag(beta) hi, lo (64 x 64 each, rows t)
-  static constexpr int TB1 = TB0 + 16384;
-  static constexpr int W16 = TB1 + 16384;  // fp16 -W^T, rows k (128 x 64)
-  static constexpr int KD0 = W16 + 16384;  // fp16 e^{gc_last-gc} K, rows t, chunk parity 0
+  static constexpr int TB = V1 + 16384;    // fp16 T diag(beta) hi, lo (64 x 64 each, rows t)
+  static constexpr int W16 = TB + 16384;   // fp16 -W^T, rows k (128 x 64)
+  static constexpr int QT = W16 + 16384;   // fp16 e^gc Q / sqrt(dk), rows t (64 x 128)
+  static constexpr int KD0 = QT + 16384;   // fp16 e^{gc_last-gc} K, rows t, chunk parity 0
   static constexpr int KD1 = KD0 + 16384;  // ... chunk parity 1
   static constexpr int A0 = KD1 + 16384;   // fp16 A hi, lo (64 x 64 each), chunk parity 0
   static constexpr int A1 = A0 + 16384;    // ... chunk parity 1
@@ -105,7 +105,7 @@ struct Ctx {
   uint16_t* s_ostage;   // [4 warps][8][32] bf16 output staging of the consumer
   float* s_elast;       // [3] e^{gc_last} by chunk index mod 3 (read by the consumer)
   volatile int* s_abort;
-  uint32_t mb_kq0, mb_kq1, mb_v0, mb_v1, mb_g, mb_uw, mb_c1, mb_c2, mb_hand, mb_cu0, mb_cu1;
+  uint32_t mb_kq0, mb_kq1, mb_v0, mb_v1, mb_t, mb_g, mb_uw, mb_c1, mb_c20, mb_c21, mb_hand, mb_cu0, mb_cu1;
 };
 
 // All threads of a group wait on one mbarrier phase; the outcome is made
@@ -137,7 +137,9 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
   const int pw = ptid >> 5, lane = ptid & 31;
   const int quad = pw & 3;   // tensor-memory lane quarter of this warp
   const int half = pw >> 2;  // which half of a 64-column accumulator it reads
-  const bool leader = ptid == 0;
+  const bool leader = ptid == 0;              // Gram and U MMAs, the prologue's copies
+  const bool w_issuer = ptid == 5 * 32;        // W MMAs (producer warp 5)
+  const bool t_issuer = ptid == 7 * 32;        // prefetch copies in the loop (producer warp 7)
   const int hq = half * 64 + (quad & 1) * 32 + lane;  // index among the 4 warps of its lane-quarter pair
   uint8_t* sm = x.sm;
 
@@ -151,16 +153,21 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     tc::tma_load_2d(dst + 8192, tmap_q, x.kh * kDim, y, mb);
     tc::tma_load_2d(dst + 16384 + 8192, tmap_q, x.kh * kDim + 64, y, mb);
   };
-  // the V tile and the T diag(beta) hi/lo tiles of chunk c, into buffer c & 1
-  auto issue_vt = [&](int c) {
-    const uint32_t vd = x.sbase + ((c & 1) ? P::V1 : P::V0), td = x.sbase + ((c & 1) ? P::TB1 : P::TB0);
+  // the V tile of chunk c, into buffer c & 1
+  auto issue_v = [&](int c) {
+    const uint32_t vd = x.sbase + ((c & 1) ? P::V1 : P::V0);
     const uint32_t mb = (c & 1) ? x.mb_v1 : x.mb_v0;
     const int32_t y = static_cast<int32_t>(x.row0 + static_cast<int64_t>(c) * kChunk);
-    tc::mbar_arrive_expect_tx(mb, 32768);
+    tc::mbar_arrive_expect_tx(mb, 16384);
     tc::tma_load_2d(vd, tmap_v, x.h * kDim, y, mb);
     tc::tma_load_2d(vd + 8192, tmap_v, x.h * kDim + 64, y, mb);
-    tc::tma_load_2d(td, tmap_t, x.h * kDim, y, mb);
-    tc::tma_load_2d(td + 8192, tmap_t, x.h * kDim + 64, y, mb);
+  };
+  // the T diag(beta) hi/lo tiles of chunk c (single buffer)
+  auto issue_t = [&](int c) {
+    const int32_t y = static_cast<int32_t>(x.row0 + static_cast<int64_t>(c) * kChunk);
+    tc::mbar_arrive_expect_tx(x.mb_t, 16384);
+    tc::tma_load_2d(x.sbase + P::TB, tmap_t, x.h * kDim, y, x.mb_t);
+    tc::tma_load_2d(x.sbase + P::TB + 8192, tmap_t, x.h * kDim + 64, y, x.mb_t);
   };
   // gates of chunk c (one warp, producer warp 4): the log-gates of tokens 2*lane and
   // 2*lane+1 are copied to stage c & 1 by cp.async two chunks ahead, then scanned
@@ -208,10 +215,11 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 
   if (leader) {
     issue_kq(0);
-    issue_vt(0);
+    issue_v(0);
+    issue_t(0);
     if (x.nchunks > 1) {
       issue_kq(1);
-      issue_vt(1);
+      issue_v(1);
     }
   }
   if (pw == 4) {
@@ -232,7 +240,6 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     const uint32_t kq_off = b ? P::KQ1 : P::KQ0;
     const uint32_t kd_off = b ? P::KD1 : P::KD0;
     const uint32_t v_off = b ? P::V1 : P::V0;
-    const uint32_t tb_off = b ? P::TB1 : P::TB0;
     const uint32_t a_off = b ? P::A1 : P::A0;
 
     // ---- Gram matrix [K;Q] K^T (bf16, M=128, N=64, K=128); lanes 64-127 hold Q K^T ---
@@ -246,13 +253,9 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       }
       tc::mma_commit(x.mb_g);
     }
-    // The spine of chunk c-1 has read its Q~ and -W^T (and so finished chunk c-2,
-    // whose Kd and A buffers this chunk reuses): the K/Q buffer of chunk c-1 is free
-    // for chunk c+1, and -W^T may be rewritten.
-    if (c > 0) {
-      ok = (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
-      if (leader && ok && c + 1 < x.nchunks) issue_kq(c + 1);
-    }
+    // this chunk's Kd and A buffers were last read by the spine of chunk c-2
+    ok = true;
+    if (c >= 2) ok = (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_c21 : x.mb_c20, ((c - 2) >> 1) & 1, kWaitLimitNs);
 
     if (quad < 2) {
       // ---- V -> fp16 in place (rows t; tail rows zeroed), lane quarters 0, 1 -----------
@@ -310,31 +313,26 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       }
     }
 
-    // ---- once the Gram MMA has read K and Q, in place (fp16, rows t, tail rows zeroed):
-    //      K -> e^gc K and Q -> Q~ = e^gc Q / sqrt(dk); and Kd = e^{gc_last-gc} K (KD[b]).
+    // ---- once the Gram MMA has read K: K -> e^gc K (fp16, in place, rows t) and --------
+    //      Kd = e^{gc_last-gc} K (KD[b]); tail rows zeroed
     ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
     if (ok) {
-      uint4 rk[4], rq[4];
+      uint4 rk[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
-        const uint32_t o = kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16);
-        rk[r] = *reinterpret_cast<const uint4*>(sm + o);
-        rq[r] = *reinterpret_cast<const uint4*>(sm + o + 8192);
+        rk[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16));
       }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
         const bool live = t < clen;
-        const uint32_t o = kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16);
         float f[8];
         unpack_bf16x8(rk[r], f);
-        *reinterpret_cast<uint4*>(sm + o) = live ? pack_half8(f, x.s_eg[gs + t]) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sm + kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16)) =
+            live ? pack_half8(f, x.s_eg[gs + t]) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(sm + kd_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
             live ? pack_half8(f, x.s_edec[gs + t]) : make_uint4(0, 0, 0, 0);
-        unpack_bf16x8(rq[r], f);
-        *reinterpret_cast<uint4*>(sm + o + 8192) =
-            live ? pack_half8(f, x.s_eg[gs + t] * kInvSqrtD) : make_uint4(0, 0, 0, 0);
       }
     }
     tc::fence_proxy_async();
@@ -350,34 +348,63 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     if (c >= 2 && !group_wait(x, p, b ? x.mb_cu1 : x.mb_cu0, ((c - 2) >> 1) & 1, kBarProducer, kProducerThreads,
                               leader))
       break;
-    if (leader) {
+    if (!group_wait(x, p, x.mb_t, c & 1, kBarProducer, kProducerThreads, leader)) break;  // T diag(beta) tiles
+    // (two issuing threads; each commits its own MMAs to the two-arrival barrier mb_uw)
+    if (leader || w_issuer) {
       tc::fence_after_sync();
       constexpr uint32_t id = tc::idesc_f16(128, 64, tc::kF16, true, false);
+      const uint32_t d_col = leader ? P::COL_U + 64 * b : P::COL_GW;
+      const uint32_t a_base = leader ? x.sbase + v_off : x.sbase + kq_off;
+      const uint32_t a_lbo = leader ? 8192 : 16384;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
 #pragma unroll
         for (int st = 0; st < 4; ++st)
-          tc::mma_f16(x.tmem + P::COL_U + 64 * b, tc::desc_sw128(x.sbase + v_off + st * 2048, 8192, 1024),
-                      tc::desc_sw128(x.sbase + tb_off + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
-      }
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-#pragma unroll
-        for (int st = 0; st < 4; ++st)
-          tc::mma_f16(x.tmem + P::COL_GW, tc::desc_sw128(x.sbase + kq_off + st * 2048, 16384, 1024),
-                      tc::desc_sw128(x.sbase + tb_off + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
+          tc::mma_f16(x.tmem + d_col, tc::desc_sw128(a_base + st * 2048, a_lbo, 1024),
+                      tc::desc_sw128(x.sbase + P::TB + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
       }
       tc::mma_commit(x.mb_uw);
     }
-    // ---- meanwhile: the gates of the next chunk, into the other gate set (their copy
-    //      was started a chunk ago), and the copy of the gates of the chunk after -------
+    // ---- meanwhile: Q -> Q~ = e^gc Q / sqrt(dk) (fp16, rows t, tail rows zeroed), once
+    //      the spine of chunk c-1 has read Q~ (and -W^T) ------------------------------------
+    ok = true;
+    if (c > 0) ok = (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
+    if (ok) {
+      uint4 rq[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
+        rq[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + 8192 + tc::sw128(t, (cc & 7) * 16));
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
+        float f[8];
+        unpack_bf16x8(rq[r], f);
+        *reinterpret_cast<uint4*>(sm + P::QT + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
+            t < clen ? pack_half8(f, x.s_eg[gs + t] * kInvSqrtD) : make_uint4(0, 0, 0, 0);
+      }
+    }
+    // ---- and the gates of the next chunk, into the other gate set (their copy was
+    //      started a chunk ago), and the copy of the gates of the chunk after -----------
     if (pw == 4 && c + 1 < x.nchunks) {
       tc::cp_async_wait_all();
       scan_gates(c + 1);
       if (c + 2 < x.nchunks) load_gates(c + 2);
     }
+    tc::fence_proxy_async();
+    if (!tc::barrier_all(kBarProducer, kProducerThreads, ok && *x.s_abort == 0)) {
+      if (leader) fail();
+      break;
+    }
     if (!group_wait(x, p, x.mb_uw, b, kBarProducer, kProducerThreads, leader)) break;
-    if (leader && c + 2 < x.nchunks) issue_vt(c + 2);  // this chunk's V and T tiles are consumed
+    if (t_issuer) {  // this chunk's raw tiles are consumed: prefetch ahead
+      if (c + 2 < x.nchunks) {
+        issue_kq(c + 2);
+        issue_v(c + 2);
+      }
+      if (c + 1 < x.nchunks) issue_t(c + 1);
+    }
 
     // ---- -W^T as the spine's fp16 B operand (rows k, columns t) -----------------------
     {
@@ -436,7 +463,6 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     const int64_t rem = x.len - static_cast<int64_t>(c) * kChunk;
     const int clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
     const uint32_t kd_off = b ? P::KD1 : P::KD0;
-    const uint32_t kq_off = b ? P::KQ1 : P::KQ0;  // Q~ sits in the Q half of the K/Q tile
     const uint32_t a_off = b ? P::A1 : P::A0;
     const uint32_t col_u = P::COL_U + 64 * b;
 
@@ -450,15 +476,14 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
         const uint32_t a = x.tmem + P::COL_ST + st * 8;
         tc::mma_f16_ts(x.tmem + col_u, a, tc::desc_sw128(x.sbase + P::W16 + st * 2048, 16384, 1024), id_u, 1);
         tc::mma_f16_ts(x.tmem + P::COL_O, a,
-                       tc::desc_sw128(x.sbase + kq_off + (st >> 2) * 16384 + 8192 + (st & 3) * 32, 16, 1024), id_o,
-                       st > 0);
+                       tc::desc_sw128(x.sbase + P::QT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024), id_o, st > 0);
       }
       tc::mma_commit(x.mb_c1);
     }
-    // meanwhile (first chunk only): S^T <- e^{gc_last} S^T, the decay half of the
-    // state update; later chunks get it from the previous chunk's last pass
-    if (c == 0) {
-      const float el = x.s_elast[0];
+    // meanwhile: S^T <- e^{gc_last} S^T, the decay half of the state update (its
+    // fp16 copy, which the MMAs read, is separate)
+    {
+      const float el = x.s_elast[c % 3];
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t s[32];
@@ -510,14 +535,12 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
         tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_lo, id_o, 1);
         tc::mma_f16_ts(x.tmem + P::COL_O, u_lo, a_hi, id_o, 1);
       }
-      tc::mma_commit(x.mb_c2);
+      tc::mma_commit(b ? x.mb_c21 : x.mb_c20);
     }
-    if (!group_wait(x, p, x.mb_c2, b, kBarConsumer, kConsumerThreads, leader)) break;
+    if (!group_wait(x, p, b ? x.mb_c21 : x.mb_c20, (c >> 1) & 1, kBarConsumer, kConsumerThreads, leader)) break;
 
-    // ---- next chunk's fp16 S^T operand and decayed state, and this chunk's output ------
+    // ---- next chunk's fp16 S^T operand, and this chunk's output rows -------------------
     {
-      const bool more = c + 1 < x.nchunks;
-      const float el = more ? x.s_elast[(c + 1) % 3] : 1.f;  // published by the hand-off of chunk c
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t s[32], st[16];
@@ -526,11 +549,6 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
 #pragma unroll
         for (int e = 0; e < 16; ++e) st[e] = pack_half2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]));
         tc::tmem_st16u(lanes + P::COL_ST + q4 * 16, st);
-        if (more) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[e] = __float_as_uint(el * __uint_as_float(s[e]));
-          tc::tmem_st32(lanes + P::COL_S + q4 * 32, s);
-        }
       }
       // O^T holds one value column per thread; an 8-row x 32-column staging tile per
       // warp turns it into 16-byte row segments for coalesced global stores.
@@ -585,7 +603,7 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   __shared__ float s_elast[3];
   __shared__ int s_fast[2];
   __shared__ __align__(16) uint16_t s_ostage[kConsumerWarps * 256];
-  __shared__ __align__(8) uint64_t s_mb[11];
+  __shared__ __align__(8) uint64_t s_mb[13];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -633,19 +651,21 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.mb_kq1 = tc::smem_u32(&s_mb[1]);
   x.mb_v0 = tc::smem_u32(&s_mb[2]);
   x.mb_v1 = tc::smem_u32(&s_mb[3]);
-  x.mb_g = tc::smem_u32(&s_mb[4]);
-  x.mb_uw = tc::smem_u32(&s_mb[5]);
-  x.mb_c1 = tc::smem_u32(&s_mb[6]);
-  x.mb_c2 = tc::smem_u32(&s_mb[7]);
-  x.mb_hand = tc::smem_u32(&s_mb[8]);
-  x.mb_cu0 = tc::smem_u32(&s_mb[9]);
-  x.mb_cu1 = tc::smem_u32(&s_mb[10]);
+  x.mb_t = tc::smem_u32(&s_mb[4]);
+  x.mb_g = tc::smem_u32(&s_mb[5]);
+  x.mb_uw = tc::smem_u32(&s_mb[6]);
+  x.mb_c1 = tc::smem_u32(&s_mb[7]);
+  x.mb_c20 = tc::smem_u32(&s_mb[8]);
+  x.mb_c21 = tc::smem_u32(&s_mb[9]);
+  x.mb_hand = tc::smem_u32(&s_mb[10]);
+  x.mb_cu0 = tc::smem_u32(&s_mb[11]);
+  x.mb_cu1 = tc::smem_u32(&s_mb[12]);
 
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), Plan::TMEM_COLS);
   if (tid == 0) {
     s_abort = 0;
 #pragma unroll
-    for (int i = 0; i < 11; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), 1);
+    for (int i = 0; i < 13; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), i == 6 ? 2 : 1);  // mb_uw: two committers
     tc::mbar_fence_init();
   }
   tc::fence_before_sync();

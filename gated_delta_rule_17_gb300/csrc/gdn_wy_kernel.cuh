@@ -6,7 +6,13 @@
 // v-head) at once. For each such item the kernel computes
 //
 //     gc = cumsum(g);  L_tj = beta_t e^{gc_t - gc_j} k_t.k_j  (j < t);
-//     T = (I + L)^{-1}   (fp32, blocked, on the CUDA cores)
+//     T = (I + L)^{-1}
+//
+// The inverse is blocked: the 16 x 16 diagonal blocks and their 32 x 32
+// merges run in fp32 on the CUDA cores, and the last merge,
+// T[32:64, 0:32] = -T22 (L21 T11), runs as two tcgen05 MMAs on bf16 hi + lo
+// splits of both factors (three products each, about 16 significant bits, the
+// fp32 exponent range).
 //
 // and writes T diag(beta) as an fp16 hi + lo pair (about 22 significant bits)
 // for the spine kernel, which forms U = (T diag beta) V and
@@ -29,7 +35,7 @@
 namespace gdn {
 
 constexpr int kWyThreads = 128;
-constexpr int kWyCtasPerSm = 4;
+constexpr int kWyCtasPerSm = 3;
 
 struct WyParams {
   const float* g;
@@ -39,22 +45,30 @@ struct WyParams {
   const int32_t* cu_chunks;   // varlen: chunk prefix over the sequences, [B + 1]
   unsigned* status;
   int64_t g_stride, beta_stride, out_stride;
-  int64_t items;              // dense: chunks * nv; varlen: an upper bound on it
+  int items;                  // dense: chunks * nv; varlen: an upper bound on it (< 2^31)
   int B, T, nk, nv;
   int chunks_per_seq;         // dense batches: ceil(T / 64)
 };
 
+// Operand tiles of the final merge are 16-bit, 128-byte-swizzled rows (see
+// tc.cuh). The M = 64 MMAs only need their rows 32-63, so an A tile stores just
+// those rows and its descriptor starts 32 rows (4 KB) earlier, on bytes whose
+// products land in accumulator rows 0-31, which are never read.
 struct WyPlan {
   static constexpr int K0 = 0;              // raw bf16 K tile (2 blocks x 64 rows), item parity 0;
-  static constexpr int K1 = 16384;          //   once its Gram MMA is done it holds the inverse's scratch
+  static constexpr int K1 = 16384;          //   once its Gram MMA is done it holds the item's scratch
   static constexpr int LF = 32768;          // fp32 64 x 64 L, overwritten by T
-  static constexpr int BYTES = LF + 16384;
+  static constexpr int BT = LF + 16384;     // bf16 hi, lo of T[0:32, 0:32] (B, rows m), later of X
+  static constexpr int AT = BT + 8192;      // bf16 hi, lo of T[32:64, 32:64]: A rows 32-63 of tiles
+                                            //   based 4 KB earlier (hi) and here (lo)
+  static constexpr int BYTES = AT + 8192;
   static constexpr int DYN_SMEM = BYTES + 1024;  // slack for 1024-byte alignment
   // scratch inside the item's own (consumed) K tile
   static constexpr int S_LT = 0;       // fp32 4 x 16 x 16 diagonal blocks of L, transposed
-  static constexpr int S_X16 = 4096;   // fp32 2 x 16 x 16 partial products
-  static constexpr int S_X32 = 8192;   // fp32 32 x 32 partial product, rows padded to 36 floats
-  static constexpr uint32_t TMEM_COLS = 64;  // K K^T, M = 64
+  static constexpr int S_AL = 4096;    // bf16 hi of L[32:64, 0:32] (A rows 32-63 of a tile based at 0),
+                                       //   lo 8 KB on (tile based at 8 KB)
+  static constexpr int S_X16 = 8192;   // fp32 2 x 16 x 16 partial products
+  static constexpr uint32_t TMEM_COLS = 64;  // K K^T (M = 64), then X and T22 X (32 columns each)
 };
 
 struct WyItem {
@@ -65,30 +79,31 @@ struct WyItem {
 
 // Item -> (rows, head). Items of malformed sequences (reported by the schedule
 // kernel) keep a valid tile position but write nothing.
-__device__ __forceinline__ WyItem wy_locate(const WyParams& p, int64_t item) {
+__device__ __forceinline__ WyItem wy_locate(const WyParams& p, int item) {
   WyItem w;
-  w.h = static_cast<int>(item % p.nv);
+  const unsigned xc = static_cast<unsigned>(item) / static_cast<unsigned>(p.nv);
+  w.h = item - static_cast<int>(xc) * p.nv;
   w.kh = w.h / (p.nv / p.nk);
   w.row0 = 0;
   w.clen = 0;
-  const int64_t xc = item / p.nv;
   if (p.cu_seqlens) {
     int lo = 0, hi = p.B;  // cu_chunks[lo] <= xc < cu_chunks[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (p.cu_chunks[mid] <= xc) lo = mid; else hi = mid;
+      if (p.cu_chunks[mid] <= static_cast<int>(xc)) lo = mid; else hi = mid;
     }
     const int a = p.cu_seqlens[lo], e = p.cu_seqlens[lo + 1];
-    const int64_t c = xc - p.cu_chunks[lo];
+    const int64_t c = static_cast<int64_t>(xc) - p.cu_chunks[lo];
     if (a < 0 || e < a || e > p.T || c < 0) return w;
     const int64_t rem = static_cast<int64_t>(e - a) - c * kChunk;
     if (rem <= 0) return w;
     w.row0 = a + c * kChunk;
     w.clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
   } else {
-    const int64_t s = xc / p.chunks_per_seq, c = xc % p.chunks_per_seq;
-    const int64_t rem = static_cast<int64_t>(p.T) - c * kChunk;
-    w.row0 = s * p.T + c * kChunk;
+    const unsigned s = xc / static_cast<unsigned>(p.chunks_per_seq);
+    const int c = static_cast<int>(xc - s * static_cast<unsigned>(p.chunks_per_seq));
+    const int rem = p.T - c * kChunk;
+    w.row0 = static_cast<int64_t>(s) * p.T + c * kChunk;
     w.clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
   }
   return w;
@@ -105,12 +120,12 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  int64_t items = p.items;
+  int items = p.items;
   if (p.cu_seqlens) {
     const int64_t have = static_cast<int64_t>(p.cu_chunks[p.B]) * p.nv;
-    if (have < items) items = have;
+    if (have < items) items = static_cast<int>(have);
   }
-  if (static_cast<int64_t>(blockIdx.x) >= items) return;
+  if (static_cast<int>(blockIdx.x) >= items) return;
 
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = tc::smem_u32(sm);
@@ -151,26 +166,28 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     for (int i = 0; i < 3; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), 1);
     tc::mbar_fence_init();
   }
-  WyItem cur = wy_locate(p, blockIdx.x);
+  WyItem cur = wy_locate(p, static_cast<int>(blockIdx.x));
   prefetch(cur, 0);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
   bool ok = true, failed = false;
+  uint32_t gph = 0;  // completed phases of the MMA barrier
 
   int n = 0;
-  for (int64_t it = blockIdx.x; it < items; it += gridDim.x, ++n) {
+  for (int it = static_cast<int>(blockIdx.x); it < items; it += static_cast<int>(gridDim.x), ++n) {
     const int kb = n & 1;
     const uint32_t kuse = (n >> 1) & 1;  // phase parity of this item's K buffer
     const uint32_t k_off = kb ? P::K1 : P::K0;
     float* lt = reinterpret_cast<float*>(sm + k_off + P::S_LT);
     float* x16 = reinterpret_cast<float*>(sm + k_off + P::S_X16);
-    float* x32 = reinterpret_cast<float*>(sm + k_off + P::S_X32);
+    // A tile of L[32:64, 0:32]: descriptor base (hi; lo 8 KB on), its rows 32-63 at +4 KB
+    const uint32_t al = sbase + k_off + P::S_AL - 4096;
     const int clen = cur.clen;
 
     // ---- the next item's tiles go in flight while this one is solved ------------------
-    const int64_t nx = it + gridDim.x;
+    const int nx = it + static_cast<int>(gridDim.x);
     WyItem nxt = cur;
     if (nx < items) {
       nxt = wy_locate(p, nx);
@@ -213,7 +230,7 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
       failed = true;
       break;
     }
-    ok = tc::mbar_wait_timed(mb_g, n & 1, kWaitLimitNs);
+    ok = tc::mbar_wait_timed(mb_g, gph++ & 1, kWaitLimitNs);
     if (!__syncthreads_and(ok)) {
       failed = true;
       break;
@@ -256,6 +273,18 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
           for (int j4 = 0; j4 < 8; ++j4)
             *reinterpret_cast<float4*>(lf + lf_idx(t, hf * 32 + j4 * 4)) =
                 make_float4(l[4 * j4], l[4 * j4 + 1], l[4 * j4 + 2], l[4 * j4 + 3]);
+          // rows 32-63, columns 0-31: the A tile of the final merge (bf16 hi, lo)
+          if (hf == 0 && t >= 32) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t hi[4], lo[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) split_bf162(l[8 * q + 2 * e], l[8 * q + 2 * e + 1], hi[e], lo[e]);
+              const uint32_t o = tc::sw128(t, q * 16);
+              *reinterpret_cast<uint4*>(sm + k_off + P::S_AL - 4096 + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+              *reinterpret_cast<uint4*>(sm + k_off + P::S_AL + 4096 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+          }
           // this row's part of its diagonal 16 x 16 block (block `warp`), transposed
           if ((warp >> 1) == hf) {
             float* dst = lt + warp * 256 + lane;
@@ -343,58 +372,97 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
       *reinterpret_cast<float4*>(lf + lf_idx(rr, cb - 16 + c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
-    // (c) lower-left 32 x 32: X = L[32:64, 0:32] T[0:32, 0:32]. Lane = row, warp w
-    //     takes columns 8w..8w+7, for which T[m][c] = 0 unless m >= 8w.
+    // (c) the last merge on the tensor cores. Operands as bf16 hi + lo: T[0:32, 0:32]
+    //     (B tile, rows m) and T[32:64, 32:64] (A tile, rows 32-63); each thread
+    //     converts 8 values of one row of each.
     {
-      const int r = lane, c0 = 8 * warp;
-      float lrow[32];
+      const int r = tid >> 2, q = tid & 3;  // row 0-31, 8-column group
+      const float4 a0 = *reinterpret_cast<const float4*>(lf + lf_idx(r, 8 * q));
+      const float4 a1 = *reinterpret_cast<const float4*>(lf + lf_idx(r, 8 * q + 4));
+      const float4 b0 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 32 + 8 * q));
+      const float4 b1 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 36 + 8 * q));
+      uint32_t hi[4], lo[4];
+      split_bf162(a0.x, a0.y, hi[0], lo[0]);
+      split_bf162(a0.z, a0.w, hi[1], lo[1]);
+      split_bf162(a1.x, a1.y, hi[2], lo[2]);
+      split_bf162(a1.z, a1.w, hi[3], lo[3]);
+      *reinterpret_cast<uint4*>(sm + P::BT + tc::sw128(r, q * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(sm + P::BT + 4096 + tc::sw128(r, q * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      split_bf162(b0.x, b0.y, hi[0], lo[0]);
+      split_bf162(b0.z, b0.w, hi[1], lo[1]);
+      split_bf162(b1.x, b1.y, hi[2], lo[2]);
+      split_bf162(b1.z, b1.w, hi[3], lo[3]);
+      *reinterpret_cast<uint4*>(sm + P::AT - 4096 + tc::sw128(32 + r, q * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(sm + P::AT + tc::sw128(32 + r, q * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    // X = L[32:64, 0:32] T[0:32, 0:32] (M = 64, N = 32, K = 32): hi.hi + hi.lo + lo.hi
+    auto merge_mma = [&](uint32_t d_col, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo) {
+      tc::fence_after_sync();
+      constexpr uint32_t id = tc::idesc_f16(64, 32, tc::kBF16, false, true);
+      const uint32_t as[3] = {a_hi, a_hi, a_lo}, bs[3] = {b_hi, b_lo, b_hi};
 #pragma unroll
-      for (int i4 = 0; i4 < 8; ++i4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 4 * i4));
-        lrow[4 * i4] = v4.x; lrow[4 * i4 + 1] = v4.y; lrow[4 * i4 + 2] = v4.z; lrow[4 * i4 + 3] = v4.w;
-      }
-      float acc[8];
+      for (int pr = 0; pr < 3; ++pr)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int st = 0; st < 2; ++st)
+          tc::mma_f16(tmem + d_col, tc::desc_sw128(as[pr] + st * 32, 16, 1024),
+                      tc::desc_sw128(bs[pr] + st * 2048, 64, 1024), id, pr + st > 0);
+      tc::mma_commit(mb_g);
+    };
+    if (tid == 0) merge_mma(0, al, al + 8192, sbase + P::BT, sbase + P::BT + 4096);
+    ok = tc::mbar_wait_timed(mb_g, gph++ & 1, kWaitLimitNs);
+    if (!__syncthreads_and(ok)) {
+      failed = true;
+      break;
+    }
+    tc::fence_after_sync();
+    // X (accumulator rows 32-63: warps 2, 3, lanes 0-15) as the bf16 B tile of the
+    // second product, over the consumed T[0:32, 0:32] tile
+    if (warp >= 2) {
+      uint32_t d[32];
+      tc::tmem_ld32(tmem + ((warp * 32u) << 16), d);
+      tc::tmem_ld_wait();
+      if (lane < 16) {
+        const int m = 16 * (warp - 2) + lane;
 #pragma unroll
-      for (int m = 0; m < 32; ++m) {
-        if (m >= c0) {  // warp-uniform
-          const float4 ta = *reinterpret_cast<const float4*>(lf + lf_idx(m, c0));
-          const float4 tb = *reinterpret_cast<const float4*>(lf + lf_idx(m, c0 + 4));
-          acc[0] = fmaf(lrow[m], ta.x, acc[0]); acc[1] = fmaf(lrow[m], ta.y, acc[1]);
-          acc[2] = fmaf(lrow[m], ta.z, acc[2]); acc[3] = fmaf(lrow[m], ta.w, acc[3]);
-          acc[4] = fmaf(lrow[m], tb.x, acc[4]); acc[5] = fmaf(lrow[m], tb.y, acc[5]);
-          acc[6] = fmaf(lrow[m], tb.z, acc[6]); acc[7] = fmaf(lrow[m], tb.w, acc[7]);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            split_bf162(__uint_as_float(d[8 * q + 2 * e]), __uint_as_float(d[8 * q + 2 * e + 1]), hi[e], lo[e]);
+          *reinterpret_cast<uint4*>(sm + P::BT + tc::sw128(m, q * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm + P::BT + 4096 + tc::sw128(m, q * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
-      *reinterpret_cast<float4*>(x32 + r * 36 + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      *reinterpret_cast<float4*>(x32 + r * 36 + c0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
     __syncthreads();
-    // (d) T[32:64, 0:32] = -T[32:64, 32:64] X. Lane = row, warp w takes columns 8w..8w+7.
-    {
-      const int r = lane, c0 = 8 * warp;
-      float trow[32];
-#pragma unroll
-      for (int i4 = 0; i4 < 8; ++i4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 32 + 4 * i4));
-        trow[4 * i4] = v4.x; trow[4 * i4 + 1] = v4.y; trow[4 * i4 + 2] = v4.z; trow[4 * i4 + 3] = v4.w;
-      }
-      float acc[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int m = 0; m < 32; ++m) {  // T[32+r][32+m] = 0 for m > r
-        const float4 xa = *reinterpret_cast<const float4*>(x32 + m * 36 + c0);
-        const float4 xb = *reinterpret_cast<const float4*>(x32 + m * 36 + c0 + 4);
-        acc[0] = fmaf(trow[m], xa.x, acc[0]); acc[1] = fmaf(trow[m], xa.y, acc[1]);
-        acc[2] = fmaf(trow[m], xa.z, acc[2]); acc[3] = fmaf(trow[m], xa.w, acc[3]);
-        acc[4] = fmaf(trow[m], xb.x, acc[4]); acc[5] = fmaf(trow[m], xb.y, acc[5]);
-        acc[6] = fmaf(trow[m], xb.z, acc[6]); acc[7] = fmaf(trow[m], xb.w, acc[7]);
-      }
-      *reinterpret_cast<float4*>(lf + lf_idx(32 + r, c0)) = make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
-      *reinterpret_cast<float4*>(lf + lf_idx(32 + r, c0 + 4)) = make_float4(-acc[4], -acc[5], -acc[6], -acc[7]);
+    // T22 X (M = 64, N = 32, K = 32) into accumulator columns 32-63
+    if (tid == 0) merge_mma(32, sbase + P::AT - 4096, sbase + P::AT, sbase + P::BT, sbase + P::BT + 4096);
+    ok = tc::mbar_wait_timed(mb_g, gph++ & 1, kWaitLimitNs);
+    if (!__syncthreads_and(ok)) {
+      failed = true;
+      break;
     }
+    tc::fence_after_sync();
+    // T[32:64, 0:32] = -T22 X
+    if (warp >= 2) {
+      uint32_t d[32];
+      tc::tmem_ld32(tmem + ((warp * 32u) << 16) + 32, d);
+      tc::tmem_ld_wait();
+      if (lane < 16) {
+        const int t = 32 + 16 * (warp - 2) + lane;
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4)
+          *reinterpret_cast<float4*>(lf + lf_idx(t, 4 * j4)) =
+              make_float4(-__uint_as_float(d[4 * j4]), -__uint_as_float(d[4 * j4 + 1]),
+                          -__uint_as_float(d[4 * j4 + 2]), -__uint_as_float(d[4 * j4 + 3]));
+      }
+    }
+    tc::fence_before_sync();
     __syncthreads();
 
     // ---- T diag(beta) as fp16 hi + lo over the output rows of the chunk ------------------

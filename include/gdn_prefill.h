@@ -142,6 +142,14 @@ int gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float
                         void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
                         const gdn_strides_t* strides, const int32_t* cu_seqlens, void* stream);
 
+/* Timing hook for profiling harnesses: every later call on this host thread
+ * records the given events (cudaEvent_t as void*, created by the caller) on
+ * its stream before the WY-solve kernel, between the two kernels and after
+ * the spine kernel, so each kernel's device time can be read with
+ * cudaEventElapsedTime. Any NULL leaves that point unrecorded; all NULL
+ * switches the hook off. The events must outlive the calls that record them. */
+void gdn_set_timing_events(void* before_wy, void* before_spine, void* after_spine);
+
 /* Synchronise `stream`, then read and clear the current device's status word
  * that kernels set on malformed cu_seqlens (GDN_ERR_DEVICE_STATUS) or on an
  * expired bounded wait (GDN_ERR_TIMEOUT). The word is shared by all calls on

@@ -30,7 +30,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gdn_prefill", "gdn_prefill_ex", "gdn_prefill_workspace_bytes", "gdn_prefill_check",
-              "gdn_last_error", "gdn_last_launch_count"):
+              "gdn_last_error", "gdn_last_launch_count", "gdn_prefill_noalloc", "gdn_set_timing_events"):
         assert n in names
 
 
