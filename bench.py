@@ -363,6 +363,62 @@ def run_gpu(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_decode(args, world, rank, local):
+    """The single-token decode step at a serving batch (B sequences x 32 v-heads), one
+    token per sequence per step, state carried in place; HBM-bound on the state."""
+    import torch
+
+    import gated_delta_rule_17_gb300 as gdn
+    from gated_delta_rule_17_gb300 import build as gbuild
+
+    gbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B = args.decode_batch
+    p = gdn_synth.make_problem(seed=6100, B=B, T=args.steps + args.warmup, nk=16, nv=32, h0_std=0.02)
+    from tests.gpu_helpers import DeviceProblem
+
+    dp = DeviceProblem(p, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    views = [x.view(p.B, p.T, *x.shape[1:]) for x in (dp.q, dp.k, dp.v, dp.g, dp.beta, dp.out)]
+
+    def step(t):
+        q, k, v, g, beta, out = (x[:, t] for x in views)
+        gdn.decode(q, k, v, g, beta, dp.state, out, nk=p.nk, nv=p.nv)
+
+    for t in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+    gdn.check()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for t in range(args.warmup, args.warmup + args.steps):
+            step(t)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    gdn.check()
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    hbm_peak, _, peak_src = measured_peaks()
+    state_bytes = 2 * B * p.nv * p.dk * p.dv * 4
+    io_bytes = B * (2 * p.nk * p.dk * 2 + 2 * p.nv * p.dv * 2 + p.nv * 8)
+    achieved = (state_bytes + io_bytes) / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "GDN decode tokens/s (one token per sequence, nv=32, dk=dv=128), 1xGB300",
+            "value": world * B / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 I/O, fp32 state and arithmetic", "data": "synthetic",
+            "config": {"workload": f"decode B={B} nk=16 nv=32 dk=dv=128 h0~N(0,0.02)",
+                       "l2": f"no flush: {state_bytes / 1e6:.0f} MB of state per step", "parallelism": "1 GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "kernel": "gdn_decode_kernel",
+                         "algorithmic_bytes": state_bytes + io_bytes, "peak_source": peak_src},
+            "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -372,6 +428,9 @@ def main():
     ap.add_argument("--config", type=int, default=2, help="workload index (2 = B=4 T=8192 nv=32)")
     ap.add_argument("--ref-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="prefill", choices=["prefill", "decode"],
+                    help="prefill (the headline) or the single-token decode step")
+    ap.add_argument("--decode-batch", type=int, default=256, help="sequences per decode step")
     ap.add_argument("--profile-case", action="store_true",
                     help="the smaller case ncu's multi-pass captures use: " + PROFILE_CASE)
     args = ap.parse_args()
@@ -380,6 +439,8 @@ def main():
     world, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.op == "decode":
+        run_decode(args, world, rank, local)
     else:
         run_gpu(args, world, rank, local)
     if world > 1:

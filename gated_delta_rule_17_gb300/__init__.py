@@ -12,7 +12,7 @@ import os
 import threading
 
 __all__ = ["prefill", "prefill_noalloc", "NOALLOC_MAX_SEQS", "workspace_bytes", "check", "last_launch_count",
-           "set_timing_events", "lib_path", "load", "GdnError",
+           "set_timing_events", "decode", "lib_path", "load", "GdnError",
            "Strides", "GDN_OK", "GDN_ERR_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
            "GDN_ERR_DEVICE_STATUS", "GDN_ERR_TIMEOUT"]
 
@@ -66,6 +66,8 @@ def load():
             lib.gdn_last_launch_count.restype = i
             lib.gdn_prefill_noalloc.argtypes = common + [vp]
             lib.gdn_prefill_noalloc.restype = i
+            lib.gdn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(Strides), vp]
+            lib.gdn_decode.restype = i
             lib.gdn_set_timing_events.argtypes = [vp, vp, vp]
             lib.gdn_set_timing_events.restype = None
             del i64
@@ -177,6 +179,38 @@ def prefill_noalloc(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | 
     rc = lib.gdn_prefill_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(),
                                  state.data_ptr(), out.data_ptr(), B, T, nk, nv, dk, dv, ctypes.byref(st),
                                  None if cu_seqlens is None else cu_seqlens.data_ptr(), stream)
+    if rc != GDN_OK:
+        _raise(rc)
+
+
+def decode(q, k, v, g, beta, state, out, *, nk: int, nv: int, state_is_table: bool = False, stream=None,
+           dk: int = 128, dv: int = 128) -> None:
+    """Enqueue one single-token decode step for every row (sequence) b of q/k/v/g/beta/out:
+    the state of sequence b (``state[b]``, or the b-th pointer of a table) is advanced by
+    that token and the token's output written to ``out[b]``. Same layouts as ``prefill``."""
+    import torch
+
+    lib = load()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("g", g, torch.float32), ("beta", beta, torch.float32), ("out", out, torch.bfloat16)):
+        if t.dtype != dt:
+            raise GdnError(GDN_ERR_ARG, f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_cuda:
+            raise GdnError(GDN_ERR_ARG, f"{name} must be a CUDA tensor")
+    st = Strides(_row_stride(q, "q", nk * dk), _row_stride(k, "k", nk * dk), _row_stride(v, "v", nv * dv),
+                 _row_stride(g, "g", nv), _row_stride(beta, "beta", nv), _row_stride(out, "out", nv * dv),
+                 1 if state_is_table else 0)
+    if state_is_table:
+        if state.dtype != torch.int64:
+            raise GdnError(GDN_ERR_ARG, "a state table must be an int64 tensor of device addresses")
+    elif state.dtype != torch.float32 or not state.is_contiguous():
+        raise GdnError(GDN_ERR_ARG, "state must be a contiguous fp32 tensor [B, nv, dk, dv]")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = lib.gdn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(), state.data_ptr(),
+                        out.data_ptr(), q.shape[0], nk, nv, dk, dv, ctypes.byref(st), stream)
     if rc != GDN_OK:
         _raise(rc)
 

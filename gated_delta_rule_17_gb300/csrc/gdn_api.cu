@@ -19,6 +19,7 @@
 #include "gdn_prefill.h"
 #include "gdn_prefill_kernel.cuh"
 #include "gdn_wy_kernel.cuh"
+#include "gdn_decode_kernel.cuh"
 
 namespace {
 
@@ -360,6 +361,43 @@ int gdn_prefill_check(void* stream) {
   if (st & gdn::kStatusTimeout) return fail(GDN_ERR_TIMEOUT, "a bounded on-device wait expired (status 0x%x)", st);
   if (st & gdn::kStatusBadSeqlens)
     return fail(GDN_ERR_DEVICE_STATUS, "cu_seqlens is malformed: not non-decreasing from 0 to T (status 0x%x)", st);
+  return GDN_OK;
+}
+
+int gdn_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, void* h_state_inout,
+               void* out, int B, int nk, int nv, int dk, int dv, const gdn_strides_t* strides, void* stream) {
+  g_err[0] = 0;
+  g_launches = 0;
+  Resolved r;
+  if (int rc = validate(q, k, v, g, beta, h_state_inout, out, B, 1, nk, nv, dk, dv, strides, &r)) return rc;
+  if (B == 0) return GDN_OK;
+  DeviceInfo* d = nullptr;
+  if (int rc = device_info(&d)) return rc;
+  const int64_t grid = static_cast<int64_t>(B) * nv;
+  if (grid > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "grid of %lld CTAs too large", (long long)grid);
+  gdn::DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.g = g;
+  p.beta = beta;
+  p.state = h_state_inout;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.q_stride = r.q;
+  p.k_stride = r.k;
+  p.v_stride = r.v;
+  p.g_stride = r.g;
+  p.beta_stride = r.beta;
+  p.out_stride = r.out;
+  p.B = B;
+  p.nk = nk;
+  p.nv = nv;
+  p.state_is_table = r.table;
+  gdn::gdn_decode_kernel<<<static_cast<unsigned>(grid), gdn::kDecodeThreads, 0,
+                           static_cast<cudaStream_t>(stream)>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  g_launches = 1;
   return GDN_OK;
 }
 

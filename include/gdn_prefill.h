@@ -142,6 +142,17 @@ int gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float
                         void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
                         const gdn_strides_t* strides, const int32_t* cu_seqlens, void* stream);
 
+/* Single-token decode step, the recurrent update that follows a prefill in
+ * serving (same recurrence and state as gdn_prefill, one token per sequence):
+ * for every sequence b and value head h, with kh = h / (nv / nk),
+ *     S' = exp(g) S;  S <- S' + beta k (v - k^T S')^T;  o = S^T q / sqrt(dk)
+ * on row b of q, k, v, g, beta and out (row strides as for gdn_prefill; the
+ * state is h_state_inout[b][h], contiguous or through the pointer table).
+ * Same argument rules, numerics (fp32 state, fp32 arithmetic, bf16 output),
+ * ownership and error codes as gdn_prefill; allocates nothing; one launch. */
+int gdn_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, void* h_state_inout,
+               void* out, int B, int nk, int nv, int dk, int dv, const gdn_strides_t* strides, void* stream);
+
 /* Timing hook for profiling harnesses: every later call on this host thread
  * records the given events (cudaEvent_t as void*, created by the caller) on
  * its stream before the WY-solve kernel, between the two kernels and after
