@@ -4,7 +4,7 @@
 // One CTA owns one (sequence, v-head) and walks its 64-token chunks in order.
 // With T diag(beta) of every chunk already solved by the chunk-parallel WY
 // kernel, it runs the rest of the GDN prefill op (ssm_gdn_a3.rs, doc comment of
-// `gdn_prefill_fla`) on chip, split between two warp groups:
+// `gdn_prefill_fla`) on chip, split between three roles:
 //
 //   producer (8 warps), chunk c+1:  WY products and operand tiles
 //     U = (T diag beta) V;  W = (T diag beta) diag(e^gc) K;
@@ -13,6 +13,10 @@
 //   consumer (4 warps), chunk c:    state spine and output
 //     u = U - W S;  S <- e^{gc_last} S + (diag(e^{gc_last-gc}) K)^T u;
 //     O = diag(e^gc) Q S / sqrt(dk) + A u          (S: state entering chunk c)
+//   two issuer warps (one thread each), driven by readiness barriers the other
+//     warps arrive on: the producer's MMAs and all TMA copies, and the spine's
+//     MMAs (tcgen05.mma issue costs tens of cycles per instruction, so two
+//     streams keep the tensor pipe fed better than one)
 //
 // The spine is computed transposed, with the value index v on the 128 tensor
 // memory lanes: u^T = U^T - S^T W^T, dS^T = u^T Kd, O^T = S^T Q~^T + u^T A^T.
@@ -41,7 +45,8 @@ namespace gdn {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kProducerWarps = 8;
-constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
+constexpr int kIssuerWarps = 2;
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps + kIssuerWarps);
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr uint32_t kBarProducer = 1;  // named barrier ids
@@ -106,6 +111,9 @@ struct Ctx {
   float* s_elast;       // [3] e^{gc_last} by chunk index mod 3 (read by the consumer)
   volatile int* s_abort;
   uint32_t mb_kq0, mb_kq1, mb_v0, mb_v1, mb_t, mb_g, mb_uw, mb_c1, mb_c20, mb_c21, mb_hand, mb_cu0, mb_cu1;
+  // readiness for the issuer (one arrival per warp): V is fp16 (4), e^gc K is done and
+  // Q K^T read (8), Q~ is done (8), W read (8), S^T ready and O^T read (4), u split (4)
+  uint32_t mb_vrdy, mb_krdy, mb_qrdy, mb_wrd, mb_strdy, mb_usp;
 };
 
 // All threads of a group wait on one mbarrier phase; the outcome is made
@@ -126,49 +134,19 @@ __device__ __forceinline__ bool group_wait(const Ctx& x, const ChunkParams& p, u
 }
 
 // ---------------------------------------------------------------------------------
-// Producer: the WY products and operand tiles of each chunk, one chunk ahead of
-// the consumer. Warp 4 also scans the gates of the chunk after, so every chunk
-// starts with its gate set ready.
+// Producer: the operand tiles of each chunk, one chunk ahead of the consumer
+// (the issuer runs its MMAs). Warp 4 also scans the gates of the chunk after,
+// so every chunk starts with its gate set ready.
 // ---------------------------------------------------------------------------------
-__device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p, const CUtensorMap* tmap_q,
-                                              const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                                              const CUtensorMap* tmap_t, int ptid) {
+__device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p, int ptid) {
   using P = Plan;
   const int pw = ptid >> 5, lane = ptid & 31;
   const int quad = pw & 3;   // tensor-memory lane quarter of this warp
   const int half = pw >> 2;  // which half of a 64-column accumulator it reads
-  const bool leader = ptid == 0;              // Gram and U MMAs, the prologue's copies
-  const bool w_issuer = ptid == 5 * 32;        // W MMAs (producer warp 5)
-  const bool t_issuer = ptid == 7 * 32;        // prefetch copies in the loop (producer warp 7)
+  const bool leader = ptid == 0;
   const int hq = half * 64 + (quad & 1) * 32 + lane;  // index among the 4 warps of its lane-quarter pair
   uint8_t* sm = x.sm;
 
-  auto issue_kq = [&](int c) {
-    const uint32_t dst = x.sbase + ((c & 1) ? P::KQ1 : P::KQ0);
-    const uint32_t mb = (c & 1) ? x.mb_kq1 : x.mb_kq0;
-    const int32_t y = static_cast<int32_t>(x.row0 + static_cast<int64_t>(c) * kChunk);
-    tc::mbar_arrive_expect_tx(mb, 32768);
-    tc::tma_load_2d(dst, tmap_k, x.kh * kDim, y, mb);
-    tc::tma_load_2d(dst + 16384, tmap_k, x.kh * kDim + 64, y, mb);
-    tc::tma_load_2d(dst + 8192, tmap_q, x.kh * kDim, y, mb);
-    tc::tma_load_2d(dst + 16384 + 8192, tmap_q, x.kh * kDim + 64, y, mb);
-  };
-  // the V tile of chunk c, into buffer c & 1
-  auto issue_v = [&](int c) {
-    const uint32_t vd = x.sbase + ((c & 1) ? P::V1 : P::V0);
-    const uint32_t mb = (c & 1) ? x.mb_v1 : x.mb_v0;
-    const int32_t y = static_cast<int32_t>(x.row0 + static_cast<int64_t>(c) * kChunk);
-    tc::mbar_arrive_expect_tx(mb, 16384);
-    tc::tma_load_2d(vd, tmap_v, x.h * kDim, y, mb);
-    tc::tma_load_2d(vd + 8192, tmap_v, x.h * kDim + 64, y, mb);
-  };
-  // the T diag(beta) hi/lo tiles of chunk c (single buffer)
-  auto issue_t = [&](int c) {
-    const int32_t y = static_cast<int32_t>(x.row0 + static_cast<int64_t>(c) * kChunk);
-    tc::mbar_arrive_expect_tx(x.mb_t, 16384);
-    tc::tma_load_2d(x.sbase + P::TB, tmap_t, x.h * kDim, y, x.mb_t);
-    tc::tma_load_2d(x.sbase + P::TB + 8192, tmap_t, x.h * kDim + 64, y, x.mb_t);
-  };
   // gates of chunk c (one warp, producer warp 4): the log-gates of tokens 2*lane and
   // 2*lane+1 are copied to stage c & 1 by cp.async two chunks ahead, then scanned
   // into gate set c & 1 one chunk ahead
@@ -212,16 +190,15 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     *x.s_abort = 1;
     atomicOr(p.status, kStatusTimeout);
   };
+  // one arrival per warp on a readiness barrier of the issuer, after this warp's
+  // shared-memory writes and tensor-memory reads
+  auto signal = [&](uint32_t mbar) {
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(mbar);
+  };
 
-  if (leader) {
-    issue_kq(0);
-    issue_v(0);
-    issue_t(0);
-    if (x.nchunks > 1) {
-      issue_kq(1);
-      issue_v(1);
-    }
-  }
   if (pw == 4) {
     load_gates(0);
     tc::cp_async_wait_all();
@@ -242,17 +219,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     const uint32_t v_off = b ? P::V1 : P::V0;
     const uint32_t a_off = b ? P::A1 : P::A0;
 
-    // ---- Gram matrix [K;Q] K^T (bf16, M=128, N=64, K=128); lanes 64-127 hold Q K^T ---
-    if (!group_wait(x, p, b ? x.mb_kq1 : x.mb_kq0, use, kBarProducer, kProducerThreads, leader)) break;
-    if (leader) {
-      constexpr uint32_t idesc = tc::idesc_f16(128, 64, tc::kBF16, false, false);
-#pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        const uint32_t a = x.sbase + kq_off + (st >> 2) * 16384 + (st & 3) * 32;
-        tc::mma_f16(x.tmem + P::COL_GW, tc::desc_sw128(a, 16, 1024), tc::desc_sw128(a, 16, 1024), idesc, st > 0);
-      }
-      tc::mma_commit(x.mb_g);
-    }
+    // ---- the Gram MMA of this chunk is issued by the issuer once its tile lands ------
     // this chunk's Kd and A buffers were last read by the spine of chunk c-2
     ok = true;
     if (c >= 2) ok = (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_c21 : x.mb_c20, ((c - 2) >> 1) & 1, kWaitLimitNs);
@@ -276,6 +243,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
               t < clen ? pack_half8(f, 1.f) : make_uint4(0, 0, 0, 0);
         }
       }
+      signal(x.mb_vrdy);  // V is fp16: the U MMAs may go
     } else {
       // ---- A (fp16 hi + lo) from Q K^T, lanes 64-127 ------------------------------------
       ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
@@ -335,40 +303,11 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
             live ? pack_half8(f, x.s_edec[gs + t]) : make_uint4(0, 0, 0, 0);
       }
     }
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    if (!tc::barrier_all(kBarProducer, kProducerThreads, ok && *x.s_abort == 0)) {
-      if (leader) fail();
-      break;
-    }
+    signal(x.mb_krdy);  // e^gc K is converted and Q K^T has been read: the W MMAs may go
 
-    // ---- U^T = V^T (T diag beta)^T and W^T = (e^gc K)^T (T diag beta)^T, hi + lo ---------
-    // U^T goes to the chunk-parity half of the U columns, free once the consumer has
-    // read u of chunk c-2 (it signals each parity on its own barrier).
-    if (c >= 2 && !group_wait(x, p, b ? x.mb_cu1 : x.mb_cu0, ((c - 2) >> 1) & 1, kBarProducer, kProducerThreads,
-                              leader))
-      break;
-    if (!group_wait(x, p, x.mb_t, c & 1, kBarProducer, kProducerThreads, leader)) break;  // T diag(beta) tiles
-    // (two issuing threads; each commits its own MMAs to the two-arrival barrier mb_uw)
-    if (leader || w_issuer) {
-      tc::fence_after_sync();
-      constexpr uint32_t id = tc::idesc_f16(128, 64, tc::kF16, true, false);
-      const uint32_t d_col = leader ? P::COL_U + 64 * b : P::COL_GW;
-      const uint32_t a_base = leader ? x.sbase + v_off : x.sbase + kq_off;
-      const uint32_t a_lbo = leader ? 8192 : 16384;
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-#pragma unroll
-        for (int st = 0; st < 4; ++st)
-          tc::mma_f16(x.tmem + d_col, tc::desc_sw128(a_base + st * 2048, a_lbo, 1024),
-                      tc::desc_sw128(x.sbase + P::TB + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
-      }
-      tc::mma_commit(x.mb_uw);
-    }
     // ---- meanwhile: Q -> Q~ = e^gc Q / sqrt(dk) (fp16, rows t, tail rows zeroed), once
     //      the spine of chunk c-1 has read Q~ (and -W^T) ------------------------------------
-    ok = true;
-    if (c > 0) ok = (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
+    if (c > 0) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
     if (ok) {
       uint4 rq[4];
 #pragma unroll
@@ -385,6 +324,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
             t < clen ? pack_half8(f, x.s_eg[gs + t] * kInvSqrtD) : make_uint4(0, 0, 0, 0);
       }
     }
+    signal(x.mb_qrdy);  // the raw K/Q tile is consumed: it may be refilled
     // ---- and the gates of the next chunk, into the other gate set (their copy was
     //      started a chunk ago), and the copy of the gates of the chunk after -----------
     if (pw == 4 && c + 1 < x.nchunks) {
@@ -398,19 +338,13 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       break;
     }
     if (!group_wait(x, p, x.mb_uw, b, kBarProducer, kProducerThreads, leader)) break;
-    if (t_issuer) {  // this chunk's raw tiles are consumed: prefetch ahead
-      if (c + 2 < x.nchunks) {
-        issue_kq(c + 2);
-        issue_v(c + 2);
-      }
-      if (c + 1 < x.nchunks) issue_t(c + 1);
-    }
 
     // ---- -W^T as the spine's fp16 B operand (rows k, columns t) -----------------------
     {
       uint32_t d[32];
       tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + half * 32, d);
       tc::tmem_ld_wait();
+      signal(x.mb_wrd);  // the W columns are read: the next Gram MMA may go
       const int k = quad * 32 + lane;
 #pragma unroll
       for (int j8 = 0; j8 < 4; ++j8) {
@@ -438,7 +372,15 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
   const int quad = ctid >> 5;
   const int v = ctid;
   const bool leader = ctid == 0;
+  const int lane = ctid & 31;
   const uint32_t lanes = x.tmem + ((quad * 32u) << 16);
+  // one arrival per warp on a readiness barrier of the issuer, after this warp's
+  // tensor-memory accesses
+  auto signal = [&](uint32_t mbar) {
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(mbar);
+  };
 
   // carried-in state: fp32 S^T into tensor memory, plus its fp16 operand copy
   {
@@ -455,31 +397,16 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     }
     tc::tmem_st_wait();
   }
-  tc::fence_before_sync();
-  tc::named_barrier(kBarConsumer, kConsumerThreads);
+  signal(x.mb_strdy);  // S^T of the first chunk is ready
 
   for (int c = 0; c < x.nchunks; ++c) {
     const int b = c & 1;
     const int64_t rem = x.len - static_cast<int64_t>(c) * kChunk;
     const int clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
-    const uint32_t kd_off = b ? P::KD1 : P::KD0;
-    const uint32_t a_off = b ? P::A1 : P::A0;
     const uint32_t col_u = P::COL_U + 64 * b;
 
     if (!group_wait(x, p, x.mb_hand, b, kBarConsumer, kConsumerThreads, leader)) break;
-    // ---- u^T = U^T - S^T W^T (accumulated onto U^T) and O^T = S^T Q~^T -------------------
-    if (leader) {
-      constexpr uint32_t id_u = tc::idesc_f16(128, 64, tc::kF16, false, true);
-      constexpr uint32_t id_o = tc::idesc_f16(128, 64, tc::kF16, false, false);
-#pragma unroll
-      for (int st = 0; st < 8; ++st) {
-        const uint32_t a = x.tmem + P::COL_ST + st * 8;
-        tc::mma_f16_ts(x.tmem + col_u, a, tc::desc_sw128(x.sbase + P::W16 + st * 2048, 16384, 1024), id_u, 1);
-        tc::mma_f16_ts(x.tmem + P::COL_O, a,
-                       tc::desc_sw128(x.sbase + P::QT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024), id_o, st > 0);
-      }
-      tc::mma_commit(x.mb_c1);
-    }
+    // (the issuer runs u^T = U^T - S^T W^T onto U^T and O^T = S^T Q~^T)
     // meanwhile: S^T <- e^{gc_last} S^T, the decay half of the state update (its
     // fp16 copy, which the MMAs read, is separate)
     {
@@ -517,26 +444,8 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
       }
       tc::tmem_st_wait();
     }
-    tc::fence_before_sync();
-    tc::named_barrier(kBarConsumer, kConsumerThreads);
-    // ---- S^T += u^T Kd (the write half of the update) and O^T += u^T A^T (hi/lo x3) -------
-    if (leader) {
-      tc::fence_after_sync();
-      tc::mbar_arrive(b ? x.mb_cu1 : x.mb_cu0);  // the U columns of this chunk parity are free again
-      constexpr uint32_t id_s = tc::idesc_f16(128, 128, tc::kF16, false, true);
-      constexpr uint32_t id_o = tc::idesc_f16(128, 64, tc::kF16, false, false);
-#pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const uint32_t u_hi = x.tmem + P::COL_UT + st * 8, u_lo = x.tmem + P::COL_UT + 32 + st * 8;
-        const uint64_t a_hi = tc::desc_sw128(x.sbase + a_off + st * 32, 16, 1024);
-        const uint64_t a_lo = tc::desc_sw128(x.sbase + a_off + 8192 + st * 32, 16, 1024);
-        tc::mma_f16_ts(x.tmem + P::COL_S, u_hi, tc::desc_sw128(x.sbase + kd_off + st * 2048, 8192, 1024), id_s, 1);
-        tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_hi, id_o, 1);
-        tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_lo, id_o, 1);
-        tc::mma_f16_ts(x.tmem + P::COL_O, u_lo, a_hi, id_o, 1);
-      }
-      tc::mma_commit(b ? x.mb_c21 : x.mb_c20);
-    }
+    signal(x.mb_usp);                    // the issuer runs S^T += u^T Kd, O^T += u^T A^T
+    signal(b ? x.mb_cu1 : x.mb_cu0);     // the U columns of this chunk parity are free again
     if (!group_wait(x, p, b ? x.mb_c21 : x.mb_c20, (c >> 1) & 1, kBarConsumer, kConsumerThreads, leader)) break;
 
     // ---- next chunk's fp16 S^T operand, and this chunk's output rows -------------------
@@ -577,7 +486,7 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
       }
       tc::tmem_st_wait();
     }
-    tc::fence_before_sync();
+    signal(x.mb_strdy);  // S^T of the next chunk is ready and O^T has been read
   }
 
   if (*x.s_abort == 0) {  // carried-out state S_T, k-major
@@ -592,6 +501,154 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
   }
 }
 
+// ---------------------------------------------------------------------------------
+// Issuers: one thread each. The producer-side issuer runs, per chunk c, the Gram
+// MMA, the U and W MMAs and the copies that refill the buffers c has consumed; the
+// spine issuer runs the spine's two MMA groups of each chunk. The producer and
+// consumer warps only convert operands and signal readiness, so no warp that
+// converts waits for an instruction queue.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, const CUtensorMap* tmap_q,
+                                            const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                            const CUtensorMap* tmap_t, bool spine_side) {
+  using P = Plan;
+  auto issue_kq = [&](int c) {
+    const uint32_t dst = x.sbase + ((c & 1) ? P::KQ1 : P::KQ0);
+    const uint32_t mb = (c & 1) ? x.mb_kq1 : x.mb_kq0;
+    const int32_t y = static_cast<int32_t>(x.row0 + static_cast<int64_t>(c) * kChunk);
+    tc::mbar_arrive_expect_tx(mb, 32768);
+    tc::tma_load_2d(dst, tmap_k, x.kh * kDim, y, mb);
+    tc::tma_load_2d(dst + 16384, tmap_k, x.kh * kDim + 64, y, mb);
+    tc::tma_load_2d(dst + 8192, tmap_q, x.kh * kDim, y, mb);
+    tc::tma_load_2d(dst + 16384 + 8192, tmap_q, x.kh * kDim + 64, y, mb);
+  };
+  auto issue_v = [&](int c) {  // V tile of chunk c, into buffer c & 1
+    const uint32_t vd = x.sbase + ((c & 1) ? P::V1 : P::V0);
+    const uint32_t mb = (c & 1) ? x.mb_v1 : x.mb_v0;
+    const int32_t y = static_cast<int32_t>(x.row0 + static_cast<int64_t>(c) * kChunk);
+    tc::mbar_arrive_expect_tx(mb, 16384);
+    tc::tma_load_2d(vd, tmap_v, x.h * kDim, y, mb);
+    tc::tma_load_2d(vd + 8192, tmap_v, x.h * kDim + 64, y, mb);
+  };
+  auto issue_t = [&](int c) {  // T diag(beta) hi/lo tiles of chunk c (single buffer)
+    const int32_t y = static_cast<int32_t>(x.row0 + static_cast<int64_t>(c) * kChunk);
+    tc::mbar_arrive_expect_tx(x.mb_t, 16384);
+    tc::tma_load_2d(x.sbase + P::TB, tmap_t, x.h * kDim, y, x.mb_t);
+    tc::tma_load_2d(x.sbase + P::TB + 8192, tmap_t, x.h * kDim + 64, y, x.mb_t);
+  };
+  auto wait = [&](uint32_t mbar, uint32_t parity) -> bool {
+    if (*x.s_abort != 0) return false;
+    if (!tc::mbar_wait_timed(mbar, parity, kWaitLimitNs)) {
+      *x.s_abort = 1;
+      atomicOr(p.status, kStatusTimeout);
+      return false;
+    }
+    tc::fence_after_sync();
+    return true;
+  };
+  // Gram matrix [K;Q] K^T (bf16, M=128, N=64, K=128); lanes 64-127 hold Q K^T
+  auto gram = [&](int c) {
+    constexpr uint32_t idesc = tc::idesc_f16(128, 64, tc::kBF16, false, false);
+    const uint32_t kq = x.sbase + ((c & 1) ? P::KQ1 : P::KQ0);
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      const uint32_t a = kq + (st >> 2) * 16384 + (st & 3) * 32;
+      tc::mma_f16(x.tmem + P::COL_GW, tc::desc_sw128(a, 16, 1024), tc::desc_sw128(a, 16, 1024), idesc, st > 0);
+    }
+    tc::mma_commit(x.mb_g);
+  };
+  // U^T = V^T (T diag beta)^T (hi + lo) into the chunk-parity U columns; W^T likewise
+  // from (e^gc K)^T into the Gram columns
+  auto wy = [&](int c, bool is_u) {
+    constexpr uint32_t id = tc::idesc_f16(128, 64, tc::kF16, true, false);
+    const int b = c & 1;
+    const uint32_t d_col = is_u ? P::COL_U + 64 * b : P::COL_GW;
+    const uint32_t a_base = x.sbase + (is_u ? (b ? P::V1 : P::V0) : (b ? P::KQ1 : P::KQ0));
+    const uint32_t a_lbo = is_u ? 8192 : 16384;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+      for (int st = 0; st < 4; ++st)
+        tc::mma_f16(x.tmem + d_col, tc::desc_sw128(a_base + st * 2048, a_lbo, 1024),
+                    tc::desc_sw128(x.sbase + P::TB + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
+    }
+  };
+  // spine, first half: u^T = U^T - S^T W^T (onto U^T) and O^T = S^T Q~^T
+  auto spine1 = [&](int c) {
+    constexpr uint32_t id_u = tc::idesc_f16(128, 64, tc::kF16, false, true);
+    constexpr uint32_t id_o = tc::idesc_f16(128, 64, tc::kF16, false, false);
+    const uint32_t col_u = P::COL_U + 64 * (c & 1);
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      const uint32_t a = x.tmem + P::COL_ST + st * 8;
+      tc::mma_f16_ts(x.tmem + col_u, a, tc::desc_sw128(x.sbase + P::W16 + st * 2048, 16384, 1024), id_u, 1);
+      tc::mma_f16_ts(x.tmem + P::COL_O, a, tc::desc_sw128(x.sbase + P::QT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024),
+                     id_o, st > 0);
+    }
+    tc::mma_commit(x.mb_c1);
+  };
+  // spine, second half: S^T += u^T Kd and O^T += u^T A^T (hi/lo x3)
+  auto spine2 = [&](int c) {
+    constexpr uint32_t id_s = tc::idesc_f16(128, 128, tc::kF16, false, true);
+    constexpr uint32_t id_o = tc::idesc_f16(128, 64, tc::kF16, false, false);
+    const int b = c & 1;
+    const uint32_t kd_off = b ? P::KD1 : P::KD0, a_off = b ? P::A1 : P::A0;
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+      const uint32_t u_hi = x.tmem + P::COL_UT + st * 8, u_lo = x.tmem + P::COL_UT + 32 + st * 8;
+      const uint64_t a_hi = tc::desc_sw128(x.sbase + a_off + st * 32, 16, 1024);
+      const uint64_t a_lo = tc::desc_sw128(x.sbase + a_off + 8192 + st * 32, 16, 1024);
+      tc::mma_f16_ts(x.tmem + P::COL_S, u_hi, tc::desc_sw128(x.sbase + kd_off + st * 2048, 8192, 1024), id_s, 1);
+      tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_hi, id_o, 1);
+      tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_lo, id_o, 1);
+      tc::mma_f16_ts(x.tmem + P::COL_O, u_lo, a_hi, id_o, 1);
+    }
+    tc::mma_commit(b ? x.mb_c21 : x.mb_c20);
+  };
+
+  const int n = x.nchunks;
+  if (spine_side) {
+    for (int c = 0; c < n; ++c) {
+      // first half once the operands are handed over and S^T is ready (and O^T read)
+      if (!wait(x.mb_hand, c & 1) || !wait(x.mb_strdy, c & 1)) break;
+      spine1(c);
+      // second half once u is split
+      if (!wait(x.mb_usp, c & 1)) break;
+      spine2(c);
+    }
+    return;
+  }
+  issue_kq(0);
+  issue_v(0);
+  issue_t(0);
+  if (n > 1) {
+    issue_kq(1);
+    issue_v(1);
+  }
+  for (int c = 0; c < n; ++c) {
+    const int b = c & 1;
+    // Gram of c: its K/Q tile has landed and the W MMAs of c-1 have been read out
+    if ((c > 0 && !wait(x.mb_wrd, (c - 1) & 1)) || !wait(b ? x.mb_kq1 : x.mb_kq0, (c >> 1) & 1)) break;
+    gram(c);
+    // U of c: V is fp16, T diag(beta) has landed, and u of c-2 has been read
+    if (!wait(x.mb_vrdy, c & 1) || !wait(x.mb_t, c & 1) ||
+        (c >= 2 && !wait(b ? x.mb_cu1 : x.mb_cu0, ((c - 2) >> 1) & 1)))
+      break;
+    wy(c, true);
+    // W of c: e^gc K is converted and the Gram columns have been read
+    if (!wait(x.mb_krdy, c & 1)) break;
+    wy(c, false);
+    tc::mma_commit(x.mb_uw);
+    // refill what chunk c has consumed
+    if (!wait(x.mb_uw, c & 1) || !wait(x.mb_qrdy, c & 1)) break;
+    if (c + 2 < n) {
+      issue_kq(c + 2);
+      issue_v(c + 2);
+    }
+    if (c + 1 < n) issue_t(c + 1);
+  }
+}
+
 template <int kUnused = 0>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -603,7 +660,7 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   __shared__ float s_elast[3];
   __shared__ int s_fast[2];
   __shared__ __align__(16) uint16_t s_ostage[kConsumerWarps * 256];
-  __shared__ __align__(8) uint64_t s_mb[13];
+  __shared__ __align__(8) uint64_t s_mb[19];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -660,12 +717,20 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.mb_hand = tc::smem_u32(&s_mb[10]);
   x.mb_cu0 = tc::smem_u32(&s_mb[11]);
   x.mb_cu1 = tc::smem_u32(&s_mb[12]);
+  x.mb_vrdy = tc::smem_u32(&s_mb[13]);
+  x.mb_krdy = tc::smem_u32(&s_mb[14]);
+  x.mb_qrdy = tc::smem_u32(&s_mb[15]);
+  x.mb_wrd = tc::smem_u32(&s_mb[16]);
+  x.mb_strdy = tc::smem_u32(&s_mb[17]);
+  x.mb_usp = tc::smem_u32(&s_mb[18]);
 
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), Plan::TMEM_COLS);
   if (tid == 0) {
     s_abort = 0;
+    // arrival counts: copies and MMA commits 1, per-warp readiness 4 or 8
+    constexpr uint32_t kCount[19] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 8, 8, 8, 4, 4};
 #pragma unroll
-    for (int i = 0; i < 13; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), i == 6 ? 2 : 1);  // mb_uw: two committers
+    for (int i = 0; i < 19; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), kCount[i]);
     tc::mbar_fence_init();
   }
   tc::fence_before_sync();
@@ -675,8 +740,10 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 
   if (warp < kConsumerWarps)
     consumer_role(x, p, tid);
-  else
-    producer_role(x, p, &tmap_q, &tmap_k, &tmap_v, &tmap_t, tid - kConsumerThreads);
+  else if (warp < kConsumerWarps + kProducerWarps)
+    producer_role(x, p, tid - kConsumerThreads);
+  else if ((tid & 31) == 0)
+    issuer_role(x, p, &tmap_q, &tmap_k, &tmap_v, &tmap_t, warp == kConsumerWarps + kProducerWarps + 1);
 
   tc::fence_before_sync();
   __syncthreads();
