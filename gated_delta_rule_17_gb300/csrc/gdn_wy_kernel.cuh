@@ -24,18 +24,17 @@
 // it with that token's output. The op therefore needs no scratch buffer, and
 // no row outside the batch's own output is touched.
 //
-// The kernel is persistent: a few CTAs per SM each walk a strided list of
-// items, and while one item is being solved the K tile (TMA) and the gates
-// (cp.async) of the CTA's next item are already in flight. Items are ordered
-// head-fastest, so the v-heads that share a key head read its K tile close
-// together in time (the second read hits L2).
+// The kernel is persistent: four CTAs per SM each walk a strided list of
+// items; the copies of one CTA's item overlap the other CTAs' arithmetic. Items
+// are ordered head-fastest, so the v-heads that share a key head read its K tile
+// close together in time (the second read hits L2).
 #pragma once
 #include "gdn_common.cuh"
 
 namespace gdn {
 
 constexpr int kWyThreads = 128;
-constexpr int kWyCtasPerSm = 3;
+constexpr int kWyCtasPerSm = 4;
 
 struct WyParams {
   const float* g;
@@ -55,9 +54,9 @@ struct WyParams {
 // those rows and its descriptor starts 32 rows (4 KB) earlier, on bytes whose
 // products land in accumulator rows 0-31, which are never read.
 struct WyPlan {
-  static constexpr int K0 = 0;              // raw bf16 K tile (2 blocks x 64 rows), item parity 0;
-  static constexpr int K1 = 16384;          //   once its Gram MMA is done it holds the item's scratch
-  static constexpr int LF = 32768;          // fp32 64 x 64 L, overwritten by T
+  static constexpr int K0 = 0;              // raw bf16 K tile (2 blocks x 64 rows); once its Gram
+                                            //   MMA is done it holds the item's scratch
+  static constexpr int LF = 16384;          // fp32 64 x 64 L, overwritten by T
   static constexpr int BT = LF + 16384;     // bf16 hi, lo of T[0:32, 0:32] (B, rows m), later of X
   static constexpr int AT = BT + 8192;      // bf16 hi, lo of T[32:64, 32:64]: A rows 32-63 of tiles
                                             //   based 4 KB earlier (hi) and here (lo)
@@ -132,13 +131,12 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
   float* lf = reinterpret_cast<float*>(sm + P::LF);
   const uint32_t mb_g = tc::smem_u32(&s_mb[2]);
 
-  // TMA of an item's K tile into buffer `kb` (thread 32), and cp.async of its
-  // gates into stage `kb` (warp 1)
+  // TMA of an item's K tile (thread 32), and cp.async of its gates (warp 1)
   auto prefetch = [&](const WyItem& w, int kb) {
     if (tid == 32) {
       const uint32_t mb = tc::smem_u32(&s_mb[kb]);
       tc::mbar_arrive_expect_tx(mb, 16384);
-      const uint32_t dst = sbase + (kb ? P::K1 : P::K0);
+      const uint32_t dst = sbase + P::K0;
       tc::tma_load_2d(dst, &tmap_k, w.kh * kDim, static_cast<int32_t>(w.row0), mb);
       tc::tma_load_2d(dst + 8192, &tmap_k, w.kh * kDim + 64, static_cast<int32_t>(w.row0), mb);
     }
@@ -167,7 +165,6 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     tc::mbar_fence_init();
   }
   WyItem cur = wy_locate(p, static_cast<int>(blockIdx.x));
-  prefetch(cur, 0);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -177,26 +174,22 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
 
   int n = 0;
   for (int it = static_cast<int>(blockIdx.x); it < items; it += static_cast<int>(gridDim.x), ++n) {
-    const int kb = n & 1;
-    const uint32_t kuse = (n >> 1) & 1;  // phase parity of this item's K buffer
-    const uint32_t k_off = kb ? P::K1 : P::K0;
+    const int kb = 0;
+    const uint32_t kuse = n & 1;  // phase parity of the K-tile barrier
+    const uint32_t k_off = P::K0;
     float* lt = reinterpret_cast<float*>(sm + k_off + P::S_LT);
     float* x16 = reinterpret_cast<float*>(sm + k_off + P::S_X16);
     // A tile of L[32:64, 0:32]: descriptor base (hi; lo 8 KB on), its rows 32-63 at +4 KB
     const uint32_t al = sbase + k_off + P::S_AL - 4096;
     const int clen = cur.clen;
 
-    // ---- the next item's tiles go in flight while this one is solved ------------------
+    // ---- this item's tiles ----------------------------------------------------------
+    prefetch(cur, 0);
     const int nx = it + static_cast<int>(gridDim.x);
-    WyItem nxt = cur;
-    if (nx < items) {
-      nxt = wy_locate(p, nx);
-      prefetch(nxt, kb ^ 1);
-    }
 
     // ---- gates (warp 1; padding tokens: g = 0, beta = 0) -------------------------------
     if (warp == 1) {
-      if (nx < items) tc::cp_async_wait_1(); else tc::cp_async_wait_all();
+      tc::cp_async_wait_all();
       __syncwarp();
       const float* st = s_gstage[kb];
       const GatePrefix gp = gate_prefix(st[2 * lane], st[2 * lane + 1]);
@@ -492,7 +485,7 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
-    cur = nxt;
+    if (nx < items) cur = wy_locate(p, nx);
   }
 
   if (failed) {
