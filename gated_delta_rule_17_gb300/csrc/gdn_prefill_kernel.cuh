@@ -107,7 +107,6 @@ struct Ctx {
   float *s_E, *s_F;     // e^{gc - m}, e^{m - gc} about the chunk's mid gate m
   int* s_fast;          // [2] 1 when the chunk's gate range allows the factorised decays
   float* s_gstage;      // [2][64] g of a chunk, staged by cp.async
-  uint16_t* s_ostage;   // [4 warps][8][32] bf16 output staging of the consumer
   float* s_elast;       // [3] e^{gc_last} by chunk index mod 3 (read by the consumer)
   volatile int* s_abort;
   uint32_t mb_kq0, mb_kq1, mb_v0, mb_v1, mb_t, mb_g, mb_uw, mb_c1, mb_c20, mb_c21, mb_hand, mb_cu0, mb_cu1;
@@ -459,29 +458,21 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
         for (int e = 0; e < 16; ++e) st[e] = pack_half2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]));
         tc::tmem_st16u(lanes + P::COL_ST + q4 * 16, st);
       }
-      // O^T holds one value column per thread; an 8-row x 32-column staging tile per
-      // warp turns it into 16-byte row segments for coalesced global stores.
-      uint16_t* stg = x.s_ostage + quad * 256;
-      const int lane = ctid & 31;
-      __nv_bfloat16* orow = p.out + (x.row0 + static_cast<int64_t>(c) * kChunk) * p.out_stride +
-                            static_cast<int64_t>(x.h) * kDim + quad * 32 + (lane & 3) * 8;
-#pragma unroll
+      // O^T holds one value column per thread: for each row t, the 32 lanes of a warp
+      // store 32 consecutive bf16 values, one 64-byte segment (no shared-memory staging)
+      __nv_bfloat16* optr = p.out + (x.row0 + static_cast<int64_t>(c) * kChunk) * p.out_stride +
+                            static_cast<int64_t>(x.h) * kDim + v;
+      const int64_t ostride = p.out_stride;
+#pragma unroll 1
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t o[32];
         tc::tmem_ld32(lanes + P::COL_O + h2 * 32, o);
         tc::tmem_ld_wait();
+        const int n_rows = clen - h2 * 32;  // rows of this half inside the sequence
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const __nv_bfloat16 bv = __float2bfloat16_rn(__uint_as_float(o[blk * 8 + r]));
-            stg[r * 32 + lane] = *reinterpret_cast<const uint16_t*>(&bv);
-          }
-          __syncwarp();
-          const uint4 w = *reinterpret_cast<const uint4*>(stg + (lane >> 2) * 32 + (lane & 3) * 8);
-          const int t = h2 * 32 + blk * 8 + (lane >> 2);
-          if (t < clen) *reinterpret_cast<uint4*>(orow + static_cast<int64_t>(t) * p.out_stride) = w;
-          __syncwarp();
+        for (int e = 0; e < 32; ++e) {
+          if (e < n_rows) *optr = __float2bfloat16_rn(__uint_as_float(o[e]));
+          optr += ostride;
         }
       }
       tc::tmem_st_wait();
@@ -659,7 +650,6 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   __shared__ __align__(16) float s_E[2 * kChunk], s_F[2 * kChunk], s_gstage[2 * kChunk];
   __shared__ float s_elast[3];
   __shared__ int s_fast[2];
-  __shared__ __align__(16) uint16_t s_ostage[kConsumerWarps * 256];
   __shared__ __align__(8) uint64_t s_mb[19];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -702,7 +692,6 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.s_F = s_F;
   x.s_fast = s_fast;
   x.s_gstage = s_gstage;
-  x.s_ostage = s_ostage;
   x.s_abort = &s_abort;
   x.mb_kq0 = tc::smem_u32(&s_mb[0]);
   x.mb_kq1 = tc::smem_u32(&s_mb[1]);
