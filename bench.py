@@ -234,11 +234,13 @@ def run_gpu(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if args.profile_case:
-        p = gdn_synth.make_problem(seed=4242, B=2, T=8192, nk=16, nv=32, h0_std=0.02)
+        p = gdn_synth.make_problem(seed=4242, B=2, T=8192, nk=16, nv=32, h0_std=0.02, qk_raw=args.qk_l2norm)
         workload = PROFILE_CASE
     else:
-        p = gdn_synth.config_problem(args.config)
+        p = gdn_synth.config_problem(args.config, qk_raw=args.qk_l2norm)
         workload = gdn_synth.CONFIG_NAMES[args.config]
+    if args.qk_l2norm:
+        workload += ", raw q/k rows normalised in the kernels (fused prologue)"
     from tests.gpu_helpers import DeviceProblem
 
     dp = DeviceProblem(p, device=dev)
@@ -314,7 +316,7 @@ def run_gpu(args, world, rank, local):
             getattr(dp, n).copy_(host[n], non_blocking=True)
         dp.state.copy_(h_state, non_blocking=True)
         gdn.prefill(dp.q, dp.k, dp.v, dp.g, dp.beta, dp.state, dp.out, nk=p.nk, nv=p.nv, B=p.B, T=p.T,
-                    cu_seqlens=dp.cu, state_is_table=dp.table, workspace=ws)
+                    cu_seqlens=dp.cu, state_is_table=dp.table, workspace=ws, qk_l2norm=dp.qk_l2norm)
         h_out.copy_(dp.out, non_blocking=True)
         h_state_out.copy_(dp.state, non_blocking=True)
 
@@ -430,6 +432,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", default="prefill", choices=["prefill", "decode"],
                     help="prefill (the headline) or the single-token decode step")
+    ap.add_argument("--qk-l2norm", action="store_true",
+                    help="un-normalised q/k inputs, normalised by the fused prologue")
     ap.add_argument("--decode-batch", type=int, default=256, help="sequences per decode step")
     ap.add_argument("--profile-case", action="store_true",
                     help="the smaller case ncu's multi-pass captures use: " + PROFILE_CASE)

@@ -34,7 +34,7 @@ class GdnError(RuntimeError):
 class Strides(ctypes.Structure):
     _fields_ = [("q", ctypes.c_int64), ("k", ctypes.c_int64), ("v", ctypes.c_int64),
                 ("g", ctypes.c_int64), ("beta", ctypes.c_int64), ("out", ctypes.c_int64),
-                ("state_is_table", ctypes.c_int32)]
+                ("state_is_table", ctypes.c_int32), ("qk_l2norm", ctypes.c_int32)]
 
 
 def lib_path() -> str:
@@ -103,7 +103,7 @@ def workspace_bytes(B, T, nv, varlen, dk=128, dv=128) -> int:
 
 def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = None, T: int | None = None,
             cu_seqlens=None, state_is_table: bool = False, workspace=None, stream=None, dk: int = 128,
-            dv: int = 128) -> None:
+            dv: int = 128, qk_l2norm: bool = False) -> None:
     """Enqueue one GDN prefill on ``stream`` (default: torch's current stream).
 
     q, k: bf16 CUDA tensors [rows, nk*dk] (or [rows, nk, dk]); v: bf16 [rows, nv*dv];
@@ -112,6 +112,7 @@ def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = N
     B device addresses of [nv, dk, dv] fp32 states. Dense batches give ``B`` and ``T``
     (rows = B*T); varlen batches give ``cu_seqlens`` (int32 CUDA [B+1]).
     ``workspace`` (uint8 CUDA tensor) passes caller-provided scratch (``gdn_prefill_ex``).
+    ``qk_l2norm`` normalises every q and k head row inside the kernels (fused prologue).
     """
     import torch
 
@@ -132,7 +133,7 @@ def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = N
         raise GdnError(GDN_ERR_ARG, "dense batches need B and T")
     st = Strides(_row_stride(q, "q", nk * dk), _row_stride(k, "k", nk * dk), _row_stride(v, "v", nv * dv),
                  _row_stride(g, "g", nv), _row_stride(beta, "beta", nv), _row_stride(out, "out", nv * dv),
-                 1 if state_is_table else 0)
+                 1 if state_is_table else 0, 1 if qk_l2norm else 0)
     if state_is_table:
         if state.dtype != torch.int64:
             raise GdnError(GDN_ERR_ARG, "a state table must be an int64 tensor of device addresses")
@@ -156,7 +157,7 @@ def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = N
 
 def prefill_noalloc(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = None,
                     T: int | None = None, cu_seqlens=None, state_is_table: bool = False, stream=None,
-                    dk: int = 128, dv: int = 128) -> None:
+                    dk: int = 128, dv: int = 128, qk_l2norm: bool = False) -> None:
     """``prefill`` through ``gdn_prefill_noalloc``: the library allocates no device
     memory during the call (its varlen schedule lives in a static device array of
     ``NOALLOC_MAX_SEQS`` entries). For callers that cannot allocate mid-call.
@@ -171,7 +172,7 @@ def prefill_noalloc(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | 
         raise GdnError(GDN_ERR_ARG, "dense batches need B and T")
     st = Strides(_row_stride(q, "q", nk * dk), _row_stride(k, "k", nk * dk), _row_stride(v, "v", nv * dv),
                  _row_stride(g, "g", nv), _row_stride(beta, "beta", nv), _row_stride(out, "out", nv * dv),
-                 1 if state_is_table else 0)
+                 1 if state_is_table else 0, 1 if qk_l2norm else 0)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
@@ -184,7 +185,7 @@ def prefill_noalloc(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | 
 
 
 def decode(q, k, v, g, beta, state, out, *, nk: int, nv: int, state_is_table: bool = False, stream=None,
-           dk: int = 128, dv: int = 128) -> None:
+           dk: int = 128, dv: int = 128, qk_l2norm: bool = False) -> None:
     """Enqueue one single-token decode step for every row (sequence) b of q/k/v/g/beta/out:
     the state of sequence b (``state[b]``, or the b-th pointer of a table) is advanced by
     that token and the token's output written to ``out[b]``. Same layouts as ``prefill``."""
@@ -199,7 +200,7 @@ def decode(q, k, v, g, beta, state, out, *, nk: int, nv: int, state_is_table: bo
             raise GdnError(GDN_ERR_ARG, f"{name} must be a CUDA tensor")
     st = Strides(_row_stride(q, "q", nk * dk), _row_stride(k, "k", nk * dk), _row_stride(v, "v", nv * dv),
                  _row_stride(g, "g", nv), _row_stride(beta, "beta", nv), _row_stride(out, "out", nv * dv),
-                 1 if state_is_table else 0)
+                 1 if state_is_table else 0, 1 if qk_l2norm else 0)
     if state_is_table:
         if state.dtype != torch.int64:
             raise GdnError(GDN_ERR_ARG, "a state table must be an int64 tensor of device addresses")

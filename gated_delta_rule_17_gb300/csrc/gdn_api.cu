@@ -129,6 +129,7 @@ int make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64
 struct Resolved {
   int64_t q, k, v, g, beta, out;
   int table;
+  int l2norm;
 };
 
 int validate(const void* q, const void* k, const void* v, const float* g, const float* beta, void* state,
@@ -146,6 +147,7 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
   r->beta = st ? st->beta : nv;
   r->out = st ? st->out : static_cast<int64_t>(nv) * dv;
   r->table = st ? st->state_is_table : 0;
+  r->l2norm = st ? st->qk_l2norm : 0;
   if (r->q < static_cast<int64_t>(nk) * dk || r->q % 8) return fail(GDN_ERR_ARG, "q row stride %lld must be >= nk*dk and a multiple of 8", (long long)r->q);
   if (r->k < static_cast<int64_t>(nk) * dk || r->k % 8) return fail(GDN_ERR_ARG, "k row stride %lld must be >= nk*dk and a multiple of 8", (long long)r->k);
   if (r->v < static_cast<int64_t>(nv) * dv || r->v % 8) return fail(GDN_ERR_ARG, "v row stride %lld must be >= nv*dv and a multiple of 8", (long long)r->v);
@@ -153,6 +155,7 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
   if (r->g < nv) return fail(GDN_ERR_ARG, "g row stride %lld must be >= nv", (long long)r->g);
   if (r->beta < nv) return fail(GDN_ERR_ARG, "beta row stride %lld must be >= nv", (long long)r->beta);
   if (r->table != 0 && r->table != 1) return fail(GDN_ERR_ARG, "state_is_table must be 0 or 1");
+  if (r->l2norm != 0 && r->l2norm != 1) return fail(GDN_ERR_ARG, "qk_l2norm must be 0 or 1");
   if (B == 0 || T == 0) return GDN_OK;  // nothing to read or write
   if (!q || !k || !v || !g || !beta || !state || !out) return fail(GDN_ERR_ARG, "a required pointer is NULL");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(state))
@@ -190,6 +193,7 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   w.nk = nk;
   w.nv = nv;
   w.chunks_per_seq = (T + gdn::kChunk - 1) / gdn::kChunk;
+  w.qk_l2norm = r.l2norm;
   // dense: every chunk of every sequence; varlen: an upper bound on the chunk
   // count (sum of ceil(len / 64) <= T / 64 + B), the excess CTAs exit at once
   const int64_t wy_chunks = cu ? static_cast<int64_t>(T) / gdn::kChunk + B + 1
@@ -215,6 +219,7 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   p.nk = nk;
   p.nv = nv;
   p.state_is_table = r.table;
+  p.qk_l2norm = r.l2norm;
   int launches = 0;
   if (cu) {
     gdn_schedule_kernel<<<(B + 255) / 256, 256, 0, stream>>>(cu, B, T, order, cu_chunks, d->status);
@@ -393,6 +398,7 @@ int gdn_decode(const void* q, const void* k, const void* v, const float* g, cons
   p.nk = nk;
   p.nv = nv;
   p.state_is_table = r.table;
+  p.qk_l2norm = r.l2norm;
   gdn::gdn_decode_kernel<<<static_cast<unsigned>(grid), gdn::kDecodeThreads, 0,
                            static_cast<cudaStream_t>(stream)>>>(p);
   cudaError_t e = cudaGetLastError();

@@ -69,6 +69,19 @@ __device__ __forceinline__ void split_bf162(float a, float b, uint32_t& hi, uint
   lo = *reinterpret_cast<const uint32_t*>(&y);
 }
 
+// Fused prologue: a head row is scaled by 1 / sqrt(sum(x^2) + kL2Eps).
+constexpr float kL2Eps = 1e-6f;
+
+// Sum of squares of the 8 bf16 values in a 16-byte chunk.
+__device__ __forceinline__ float sumsq_bf16x8(const uint4 raw) {
+  float f[8];
+  unpack_bf16x8(raw, f);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s = fmaf(f[i], f[i], s);
+  return s;
+}
+
 // Inclusive in-chunk prefix of the log-gates held by one warp, lane l holding
 // tokens 2l and 2l+1 (padding tokens carry g = 0).
 struct GatePrefix {

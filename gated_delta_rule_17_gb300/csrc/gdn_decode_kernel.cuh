@@ -31,12 +31,14 @@ struct DecodeParams {
   int64_t q_stride, k_stride, v_stride, g_stride, beta_stride, out_stride;
   int B, nk, nv;
   int state_is_table;
+  int qk_l2norm;  // fused prologue: normalise the q and k rows first
 };
 
 __global__ void __launch_bounds__(kDecodeThreads)
 gdn_decode_kernel(const DecodeParams p) {
   __shared__ float s_k[kDim], s_q[kDim];
   __shared__ __align__(16) float s_part[8][kDim];  // per-k-group partial sums over k
+  __shared__ float s_norm[2][4];                   // fused prologue: per-warp sums of squares
   const int tid = threadIdx.x;
   const int vg = tid & 31, kg = tid >> 5;  // v = 4 vg .. 4 vg + 3, k = 16 kg .. 16 kg + 15
   const int h = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.nv));
@@ -49,6 +51,28 @@ gdn_decode_kernel(const DecodeParams p) {
   if (tid < kDim) {
     s_k[tid] = __bfloat162float(p.k[b * p.k_stride + kh * kDim + tid]);
     s_q[tid] = __bfloat162float(p.q[b * p.q_stride + kh * kDim + tid]);
+  }
+  if (p.qk_l2norm) {  // 1 / |k|, 1 / |q| (warps 0-3 hold the two rows)
+    __syncthreads();
+    if (tid < kDim) {
+      float sk = s_k[tid] * s_k[tid], sq = s_q[tid] * s_q[tid];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        sk += __shfl_xor_sync(0xffffffffu, sk, o);
+        sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      }
+      if ((tid & 31) == 0) {
+        s_norm[0][tid >> 5] = sk;
+        s_norm[1][tid >> 5] = sq;
+      }
+    }
+    __syncthreads();
+    if (tid < kDim) {
+      const float rk = 1.f / sqrtf(s_norm[0][0] + s_norm[0][1] + s_norm[0][2] + s_norm[0][3] + kL2Eps);
+      const float rq = 1.f / sqrtf(s_norm[1][0] + s_norm[1][1] + s_norm[1][2] + s_norm[1][3] + kL2Eps);
+      s_k[tid] *= rk;
+      s_q[tid] *= rq;
+    }
   }
   const float a = __expf(p.g[b * p.g_stride + h]);
   const float bt = p.beta[b * p.beta_stride + h];

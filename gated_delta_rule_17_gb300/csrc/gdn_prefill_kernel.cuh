@@ -51,6 +51,7 @@ constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr uint32_t kBarProducer = 1;  // named barrier ids
 constexpr uint32_t kBarConsumer = 2;
+constexpr uint32_t kBarNorm = 3;      // producer, fused prologue: row norms published
 
 struct ChunkParams {
   const float* g;
@@ -62,6 +63,7 @@ struct ChunkParams {
   int64_t g_stride, out_stride;
   int B, T, nk, nv;
   int state_is_table;
+  int qk_l2norm;              // fused prologue: normalise every q and k row first
 };
 
 // Shared-memory plan (bytes from a 1024-aligned base). Operand tiles are
@@ -103,8 +105,9 @@ struct Ctx {
   int nchunks, h, kh;
   float* state;      // this (sequence, head)'s fp32 [128][128] state, k-major
   // producer-side per-token scales, two gate sets by chunk parity ([2][64] each)
-  float *s_gc, *s_eg, *s_edec;
+  float *s_gc, *s_eg, *s_egq, *s_edec;  // gc, e^gc, e^gc / sqrt(dk), e^{gc_last - gc}
   float *s_E, *s_F;     // e^{gc - m}, e^{m - gc} about the chunk's mid gate m
+  float *s_rq, *s_rk;   // fused prologue: 1 / |q_t|, 1 / |k_t| of the current chunk
   int* s_fast;          // [2] 1 when the chunk's gate range allows the factorised decays
   float* s_gstage;      // [2][64] g of a chunk, staged by cp.async
   float* s_elast;       // [3] e^{gc_last} by chunk index mod 3 (read by the consumer)
@@ -174,6 +177,8 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     x.s_gc[gs + 2 * lane + 1] = gp.gcb;
     x.s_eg[gs + 2 * lane] = __expf(gp.gca);
     x.s_eg[gs + 2 * lane + 1] = __expf(gp.gcb);
+    x.s_egq[gs + 2 * lane] = __expf(gp.gca) * kInvSqrtD;
+    x.s_egq[gs + 2 * lane + 1] = __expf(gp.gcb) * kInvSqrtD;
     x.s_edec[gs + 2 * lane] = __expf(gp.last - gp.gca);
     x.s_edec[gs + 2 * lane + 1] = __expf(gp.last - gp.gcb);
     x.s_E[gs + 2 * lane] = __expf(gp.gca - mid);
@@ -243,10 +248,37 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         }
       }
       signal(x.mb_vrdy);  // V is fp16: the U MMAs may go
+      if (p.qk_l2norm) tc::named_barrier(kBarNorm, kProducerThreads);
     } else {
       // ---- A (fp16 hi + lo) from Q K^T, lanes 64-127 ------------------------------------
       ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
       tc::fence_after_sync();
+      if (p.qk_l2norm) {
+        // fused prologue: one raw row per thread, K rows 0-63 then Q rows 0-63, read
+        // before any thread converts the tile in place. The inverse norms are folded
+        // into this chunk's per-token factors (K: e^gc, e^{gc_last-gc}, F; Q: e^gc/sqrt(dk),
+        // E) and kept apart for the direct-decay path
+        const int row = half * 64 + (quad - 2) * 32 + lane, t = row & 63;
+        const uint32_t base = kq_off + (row >> 6) * 8192;
+        float ss = 0.f;
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            ss += sumsq_bf16x8(*reinterpret_cast<const uint4*>(sm + base + kb * 16384 + tc::sw128(t, j * 16)));
+        const float r = 1.f / sqrtf(ss + kL2Eps);
+        if (row < 64) {
+          x.s_rk[t] = r;
+          x.s_eg[gs + t] *= r;
+          x.s_edec[gs + t] *= r;
+          x.s_F[gs + t] *= r;
+        } else {
+          x.s_rq[t] = r;
+          x.s_egq[gs + t] *= r;
+          x.s_E[gs + t] *= r;
+        }
+        tc::named_barrier(kBarNorm, kProducerThreads);
+      }
       if (ok) {
         uint32_t d[32];
         tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + half * 32, d);
@@ -261,11 +293,14 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
             a[e] = (j <= i) ? ei * x.s_F[gs + j] * __uint_as_float(d[e]) : 0.f;
           }
         } else {
+          const bool norm = p.qk_l2norm != 0;
+          const float ri = (norm ? x.s_rq[i] : 1.f) * kInvSqrtD;
           const float gi = x.s_gc[gs + i];
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int j = half * 32 + e;
-            a[e] = (j <= i) ? __expf(gi - x.s_gc[gs + j]) * kInvSqrtD * __uint_as_float(d[e]) : 0.f;
+            a[e] = (j <= i) ? __expf(gi - x.s_gc[gs + j]) * ri * (norm ? x.s_rk[j] : 1.f) * __uint_as_float(d[e])
+                            : 0.f;
           }
         }
 #pragma unroll
@@ -320,7 +355,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         float f[8];
         unpack_bf16x8(rq[r], f);
         *reinterpret_cast<uint4*>(sm + P::QT + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
-            t < clen ? pack_half8(f, x.s_eg[gs + t] * kInvSqrtD) : make_uint4(0, 0, 0, 0);
+            t < clen ? pack_half8(f, x.s_egq[gs + t]) : make_uint4(0, 0, 0, 0);
       }
     }
     signal(x.mb_qrdy);  // the raw K/Q tile is consumed: it may be refilled
@@ -646,8 +681,9 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_t,
                    const ChunkParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(16) float s_gc[2 * kChunk], s_eg[2 * kChunk], s_edec[2 * kChunk];
+  __shared__ __align__(16) float s_gc[2 * kChunk], s_eg[2 * kChunk], s_egq[2 * kChunk], s_edec[2 * kChunk];
   __shared__ __align__(16) float s_E[2 * kChunk], s_F[2 * kChunk], s_gstage[2 * kChunk];
+  __shared__ __align__(16) float s_rq[kChunk], s_rk[kChunk];
   __shared__ float s_elast[3];
   __shared__ int s_fast[2];
   __shared__ __align__(8) uint64_t s_mb[19];
@@ -686,10 +722,13 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.sbase = tc::smem_u32(x.sm);
   x.s_gc = s_gc;
   x.s_eg = s_eg;
+  x.s_egq = s_egq;
   x.s_edec = s_edec;
   x.s_elast = s_elast;
   x.s_E = s_E;
   x.s_F = s_F;
+  x.s_rq = s_rq;
+  x.s_rk = s_rk;
   x.s_fast = s_fast;
   x.s_gstage = s_gstage;
   x.s_abort = &s_abort;

@@ -47,6 +47,7 @@ struct WyParams {
   int items;                  // dense: chunks * nv; varlen: an upper bound on it (< 2^31)
   int B, T, nk, nv;
   int chunks_per_seq;         // dense batches: ceil(T / 64)
+  int qk_l2norm;              // fused prologue: normalise every key row first
 };
 
 // Operand tiles of the final merge are 16-bit, 128-byte-swizzled rows (see
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kWyThreads, kWyCtasPerSm)
 gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
   using P = WyPlan;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(16) float s_gc[kChunk], s_beta[kChunk], s_E[kChunk], s_F[kChunk];
+  __shared__ __align__(16) float s_gc[kChunk], s_beta[kChunk], s_E[kChunk], s_F[kChunk], s_rk[kChunk];
   __shared__ __align__(16) float s_gstage[2][2 * kChunk];  // g, beta of an item, by parity
   __shared__ int s_fast;
   __shared__ __align__(8) uint64_t s_mb[3];
@@ -230,6 +231,23 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     }
     tc::fence_after_sync();
 
+    // ---- fused prologue: 1 / |k_t| of every key row (thread pair per row), folded into
+    //      the factor F_t of the decays as well ---------------------------------------------
+    if (p.qk_l2norm) {
+      const int t = tid >> 1, kb = tid & 1;
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        ss += sumsq_bf16x8(*reinterpret_cast<const uint4*>(sm + k_off + kb * 8192 + tc::sw128(t, j * 16)));
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      if (kb == 0) {
+        const float r = 1.f / sqrtf(ss + kL2Eps);
+        s_rk[t] = r;
+        s_F[t] *= r;
+      }
+      __syncthreads();
+    }
+
     // ---- L (fp32): row t = 16 warp + l sits in lane 32 warp + l (M = 64 layout) --------
     {
       uint32_t d[2][32];
@@ -240,7 +258,9 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
         const int t = 16 * warp + lane;
         const bool live = t < clen;
         const bool fast = s_fast != 0;
-        const float bt = live ? s_beta[t] : 0.f, be = bt * s_E[t], gt = s_gc[t];
+        const bool norm = p.qk_l2norm != 0;
+        const float rt = norm ? s_rk[t] : 1.f;
+        const float bt = live ? s_beta[t] * rt : 0.f, be = bt * s_E[t], gt = s_gc[t];
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           float l[32];
@@ -259,7 +279,7 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
               const int j = hf * 32 + e;
-              l[e] = j < t ? bt * __expf(gt - s_gc[j]) * __uint_as_float(d[hf][e]) : 0.f;
+              l[e] = j < t ? bt * (norm ? s_rk[j] : 1.f) * __expf(gt - s_gc[j]) * __uint_as_float(d[hf][e]) : 0.f;
             }
           }
 #pragma unroll

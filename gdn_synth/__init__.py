@@ -102,6 +102,15 @@ def _normalised_rows(rng, rows, heads, d):
     return (x / np.maximum(n, np.float32(1e-30))).astype(np.float32)
 
 
+def _raw_rows(rng, rscale, rows, heads, d):
+    # un-normalised rows for the fused-prologue path: N(0,1) entries times a
+    # per-row power of two in [2^-3, 2^3] (exact in bf16), so row norms spread
+    # over about 1.4 .. 91
+    x = rng.standard_normal((rows, heads, d), dtype=np.float32)
+    e = rscale.integers(-3, 4, size=(rows, heads, 1))
+    return (x * np.exp2(e).astype(np.float32)).astype(np.float32)
+
+
 def make_problem(
     *,
     seed: int,
@@ -120,6 +129,7 @@ def make_problem(
     pad_qk: int = 0,
     pad_v: int = 0,
     gb_stride: int | None = None,
+    qk_raw: bool = False,
     name: str = "",
 ) -> Problem:
     """Draw one problem.
@@ -129,7 +139,9 @@ def make_problem(
     from them). ``h0_mask[s]`` selects which sequences get a N(0, h0_std)
     state (others start at zero). ``pad_qk``/``pad_v`` widen the row strides of
     q/k and v beyond the packed minimum; ``gb_stride`` sets the row stride of
-    g and beta (the packed conv layout uses 2*nv).
+    g and beta (the packed conv layout uses 2*nv). ``qk_raw`` leaves the q and k
+    head rows un-normalised (the input of the fused L2-norm prologue), with a
+    per-row power-of-two scale drawn from an eighth child stream.
     """
     ss = np.random.SeedSequence(seed)
     rq, rk, rv, rg, rb, rh, rl = [np.random.Generator(np.random.PCG64(c)) for c in ss.spawn(7)]
@@ -153,8 +165,15 @@ def make_problem(
     q = np.zeros((rows, qs), dtype=np.uint16)
     k = np.zeros((rows, qs), dtype=np.uint16)
     v = np.zeros((rows, vs), dtype=np.uint16)
-    q[:, : nk * dk] = f32_to_bf16_bits(_normalised_rows(rq, rows, nk, dk).reshape(rows, nk * dk))
-    k[:, : nk * dk] = f32_to_bf16_bits(_normalised_rows(rk, rows, nk, dk).reshape(rows, nk * dk))
+    if qk_raw:
+        rs = np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed).spawn(8)[7]))
+        qf = _raw_rows(rq, rs, rows, nk, dk)
+        kf = _raw_rows(rk, rs, rows, nk, dk)
+    else:
+        qf = _normalised_rows(rq, rows, nk, dk)
+        kf = _normalised_rows(rk, rows, nk, dk)
+    q[:, : nk * dk] = f32_to_bf16_bits(qf.reshape(rows, nk * dk))
+    k[:, : nk * dk] = f32_to_bf16_bits(kf.reshape(rows, nk * dk))
     v[:, : nv * dv] = f32_to_bf16_bits(rv.standard_normal((rows, nv * dv), dtype=np.float32))
 
     g = np.zeros((rows, gs), dtype=np.float32)
@@ -173,7 +192,7 @@ def make_problem(
         mask = np.ones(B, dtype=bool) if h0_mask is None else np.asarray(h0_mask, dtype=bool)
         h0[mask] = draw[mask]
     return Problem(B=B, T=T, nk=nk, nv=nv, dk=dk, dv=dv, q=q, k=k, v=v, g=g, beta=beta,
-                   h0=h0, cu_seqlens=cu, name=name)
+                   h0=h0, cu_seqlens=cu, name=name, meta={"qk_raw": qk_raw})
 
 
 def draw_lengths(seed: int, n: int, lo: int, hi: int, avoid_multiple: int = 64):

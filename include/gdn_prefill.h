@@ -46,7 +46,8 @@ enum {
 /*
  * Row strides, in elements, between consecutive token rows of each tensor
  * (the op's qk_stride / v_stride / gb_stride arguments; the packed conv layout
- * uses qk_stride = v_stride = conv width and a g/beta stride of 2*nv).
+ * uses qk_stride = v_stride = conv width and a g/beta stride of 2*nv), and
+ * the prologue option.
  *   q, k : bf16 elements; multiple of 8 (16-byte rows for TMA); >= nk*dk
  *   v    : bf16 elements; multiple of 8; >= nv*dv
  *   g, beta : fp32 elements; >= nv
@@ -54,14 +55,21 @@ enum {
  *   state_is_table : 0 -> h_state_inout is float[B][nv][dk][dv];
  *                    1 -> h_state_inout is a device array of B device
  *                         pointers, each to one float[nv][dk][dv]
+ *   qk_l2norm : 0 -> q and k rows are used as given (already L2-normalised
+ *                    by the caller);
+ *               1 -> fused prologue: every head row of q and of k is
+ *                    normalised inside the kernels, x / sqrt(sum(x^2) + 1e-6)
+ *                    in fp32, before any use (the input tensors are not
+ *                    modified)
  * Passing NULL for the struct means packed rows (q = k = nk*dk, v = out =
- * nv*dv, g = beta = nv) and a contiguous state.
+ * nv*dv, g = beta = nv), a contiguous state and no prologue.
  */
 typedef struct {
   int64_t q, k, v;
   int64_t g, beta;
   int64_t out;
   int32_t state_is_table;
+  int32_t qk_l2norm;
 } gdn_strides_t;
 
 /*

@@ -108,8 +108,44 @@ def token_loop_raw(q, k, v, g, beta, h0, *, B, T, nk, nv, dk, dv,
     return out, hT
 
 
-def token_loop(p: Problem, heads=None, threads=0):
-    """Oracle evaluation of a ``gdn_synth.Problem`` (see ``token_loop_raw``)."""
-    return token_loop_raw(p.q, p.k, p.v, p.g, p.beta, p.h0, B=p.B, T=p.T, nk=p.nk, nv=p.nv,
+L2_EPS = 1e-6
+
+
+def bf16_to_f64(a: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to fp64; other dtypes are cast."""
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def l2norm_heads(x: np.ndarray, heads: int, d: int, eps: float = L2_EPS) -> np.ndarray:
+    """The fused prologue's q/k normalisation, in fp64.
+
+    x: [rows, >= heads*d] (bf16 bits or float). Every head row x_h = x[:, h*d:(h+1)*d]
+    becomes x_h / sqrt(sum(x_h^2) + eps). Returns fp64 [rows, heads*d].
+
+    The GDN prefill op takes q and k from the packed conv layout (ssm_gdn_a3.rs,
+    doc comment of `gdn_prefill_fla`: strides of the packed conv tensor); the
+    normalisation of each head row is the step between that layout and the
+    recurrence. The pages print no formula for it: this is the usual L2 norm
+    with eps added to the sum of squares.
+    """
+    xf = bf16_to_f64(np.ascontiguousarray(x)[:, : heads * d]).reshape(x.shape[0], heads, d)
+    n = np.sqrt(np.sum(xf * xf, axis=-1, keepdims=True) + eps)
+    return (xf / n).reshape(x.shape[0], heads * d)
+
+
+def token_loop(p: Problem, heads=None, threads=0, qk_l2norm=False):
+    """Oracle evaluation of a ``gdn_synth.Problem`` (see ``token_loop_raw``).
+
+    With ``qk_l2norm`` the q and k head rows first go through ``l2norm_heads``
+    and the recurrence runs on fp64 q, k, v.
+    """
+    q, k, v = p.q, p.k, p.v
+    if qk_l2norm:
+        q = l2norm_heads(q, p.nk, p.dk)
+        k = l2norm_heads(k, p.nk, p.dk)
+        v = bf16_to_f64(v)
+    return token_loop_raw(q, k, v, p.g, p.beta, p.h0, B=p.B, T=p.T, nk=p.nk, nv=p.nv,
                           dk=p.dk, dv=p.dv, cu_seqlens=p.cu_seqlens, heads=heads,
                           threads=threads)

@@ -25,7 +25,7 @@ def to_torch_bf16(bits, device):
 class DeviceProblem:
     """Device copies of a ``gdn_synth.Problem`` plus output/state buffers."""
 
-    def __init__(self, p: gdn_synth.Problem, device="cuda", state_table=None, out_pad=0):
+    def __init__(self, p: gdn_synth.Problem, device="cuda", state_table=None, out_pad=0, qk_l2norm=None):
         import torch
 
         self.p = p
@@ -37,6 +37,7 @@ class DeviceProblem:
         self.beta = torch.from_numpy(p.beta).to(device)
         self.cu = None if p.cu_seqlens is None else torch.from_numpy(p.cu_seqlens).to(device)
         self.table = p.meta.get("state_table", False) if state_table is None else state_table
+        self.qk_l2norm = p.meta.get("qk_raw", False) if qk_l2norm is None else qk_l2norm
         self.out = torch.empty((p.rows, p.nv * p.dv + out_pad), dtype=torch.bfloat16, device=device)
         self.reset()
 
@@ -58,7 +59,7 @@ class DeviceProblem:
         p = self.p
         gdn.prefill(self.q, self.k, self.v, self.g, self.beta, self.state, self.out, nk=p.nk, nv=p.nv,
                     B=p.B, T=p.T, cu_seqlens=self.cu, state_is_table=self.table, workspace=workspace,
-                    stream=stream)
+                    stream=stream, qk_l2norm=self.qk_l2norm)
 
     def out_np(self):
         import torch
