@@ -232,19 +232,22 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       // ---- V -> fp16 in place (rows t; tail rows zeroed), lane quarters 0, 1 -----------
       ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_v1 : x.mb_v0, use, kWaitLimitNs);
       if (ok) {
-        uint4 raw[8];
+#pragma unroll 1
+        for (int r0 = 0; r0 < 8; r0 += 4) {
+          uint4 raw[4];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int it = hq + r * 128, t = it & 63, cc = it >> 6;
-          raw[r] = *reinterpret_cast<const uint4*>(sm + v_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16));
-        }
+          for (int r = 0; r < 4; ++r) {
+            const int it = hq + (r0 + r) * 128, t = it & 63, cc = it >> 6;
+            raw[r] = *reinterpret_cast<const uint4*>(sm + v_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16));
+          }
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int it = hq + r * 128, t = it & 63, cc = it >> 6;
-          float f[8];
-          unpack_bf16x8(raw[r], f);
-          *reinterpret_cast<uint4*>(sm + v_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
-              t < clen ? pack_half8(f, 1.f) : make_uint4(0, 0, 0, 0);
+          for (int r = 0; r < 4; ++r) {
+            const int it = hq + (r0 + r) * 128, t = it & 63, cc = it >> 6;
+            float f[8];
+            unpack_bf16x8(raw[r], f);
+            *reinterpret_cast<uint4*>(sm + v_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
+                t < clen ? pack_half8(f, 1.f) : make_uint4(0, 0, 0, 0);
+          }
         }
       }
       signal(x.mb_vrdy);  // V is fp16: the U MMAs may go
@@ -280,35 +283,37 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         tc::named_barrier(kBarNorm, kProducerThreads);
       }
       if (ok) {
-        uint32_t d[32];
-        tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + half * 32, d);
-        tc::tmem_ld_wait();
         const int i = (quad - 2) * 32 + lane;  // A_ij = e^{gc_i - gc_j} q_i.k_j / sqrt(dk), j <= i
-        float a[32];
-        if (x.s_fast[b] != 0) {
-          const float ei = x.s_E[gs + i] * kInvSqrtD;
+        const bool fast = x.s_fast[b] != 0;
+        const float ei = x.s_E[gs + i] * kInvSqrtD;
+#pragma unroll 1
+        for (int j8 = 0; j8 < 4; ++j8) {  // 8 columns at a time
+          const int j0 = half * 32 + j8 * 8;
+          uint32_t d[8];
+          tc::tmem_ld8(x.tmem + ((quad * 32u) << 16) + P::COL_GW + j0, d);
+          tc::tmem_ld_wait();
+          float a[8];
+          if (fast) {
+            const float4 f0 = *reinterpret_cast<const float4*>(x.s_F + gs + j0);
+            const float4 f1 = *reinterpret_cast<const float4*>(x.s_F + gs + j0 + 4);
+            const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = half * 32 + e;
-            a[e] = (j <= i) ? ei * x.s_F[gs + j] * __uint_as_float(d[e]) : 0.f;
+            for (int e = 0; e < 8; ++e) a[e] = (j0 + e <= i) ? ei * f[e] * __uint_as_float(d[e]) : 0.f;
+          } else {
+            const bool norm = p.qk_l2norm != 0;
+            const float ri = (norm ? x.s_rq[i] : 1.f) * kInvSqrtD;
+            const float gi = x.s_gc[gs + i];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int j = j0 + e;
+              a[e] = (j <= i) ? __expf(gi - x.s_gc[gs + j]) * ri * (norm ? x.s_rk[j] : 1.f) * __uint_as_float(d[e])
+                              : 0.f;
+            }
           }
-        } else {
-          const bool norm = p.qk_l2norm != 0;
-          const float ri = (norm ? x.s_rq[i] : 1.f) * kInvSqrtD;
-          const float gi = x.s_gc[gs + i];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = half * 32 + e;
-            a[e] = (j <= i) ? __expf(gi - x.s_gc[gs + j]) * ri * (norm ? x.s_rk[j] : 1.f) * __uint_as_float(d[e])
-                            : 0.f;
-          }
-        }
-#pragma unroll
-        for (int j8 = 0; j8 < 4; ++j8) {
           uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) split_half2(a[j8 * 8 + 2 * e], a[j8 * 8 + 2 * e + 1], hi[e], lo[e]);
-          const uint32_t o = tc::sw128(i, (half * 32 + j8 * 8) * 2);
+          for (int e = 0; e < 4; ++e) split_half2(a[2 * e], a[2 * e + 1], hi[e], lo[e]);
+          const uint32_t o = tc::sw128(i, j0 * 2);
           *reinterpret_cast<uint4*>(sm + a_off + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(sm + a_off + 8192 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
@@ -319,15 +324,17 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     //      Kd = e^{gc_last-gc} K (KD[b]); tail rows zeroed
     ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
     if (ok) {
-      uint4 rk[4];
+#pragma unroll 1
+      for (int r0 = 0; r0 < 4; r0 += 2) {
+      uint4 rk[2];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
+      for (int r = 0; r < 2; ++r) {
+        const int it = ptid + (r0 + r) * kProducerThreads, t = it & 63, cc = it >> 6;
         rk[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16));
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
+      for (int r = 0; r < 2; ++r) {
+        const int it = ptid + (r0 + r) * kProducerThreads, t = it & 63, cc = it >> 6;
         const bool live = t < clen;
         float f[8];
         unpack_bf16x8(rk[r], f);
@@ -336,6 +343,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         *reinterpret_cast<uint4*>(sm + kd_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
             live ? pack_half8(f, x.s_edec[gs + t]) : make_uint4(0, 0, 0, 0);
       }
+      }
     }
     signal(x.mb_krdy);  // e^gc K is converted and Q K^T has been read: the W MMAs may go
 
@@ -343,19 +351,22 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     //      the spine of chunk c-1 has read Q~ (and -W^T) ------------------------------------
     if (c > 0) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
     if (ok) {
-      uint4 rq[4];
+#pragma unroll 1
+      for (int r0 = 0; r0 < 4; r0 += 2) {
+        uint4 rq[2];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
-        rq[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + 8192 + tc::sw128(t, (cc & 7) * 16));
-      }
+        for (int r = 0; r < 2; ++r) {
+          const int it = ptid + (r0 + r) * kProducerThreads, t = it & 63, cc = it >> 6;
+          rq[r] = *reinterpret_cast<const uint4*>(sm + kq_off + (cc >> 3) * 16384 + 8192 + tc::sw128(t, (cc & 7) * 16));
+        }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int it = ptid + r * kProducerThreads, t = it & 63, cc = it >> 6;
-        float f[8];
-        unpack_bf16x8(rq[r], f);
-        *reinterpret_cast<uint4*>(sm + P::QT + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
-            t < clen ? pack_half8(f, x.s_egq[gs + t]) : make_uint4(0, 0, 0, 0);
+        for (int r = 0; r < 2; ++r) {
+          const int it = ptid + (r0 + r) * kProducerThreads, t = it & 63, cc = it >> 6;
+          float f[8];
+          unpack_bf16x8(rq[r], f);
+          *reinterpret_cast<uint4*>(sm + P::QT + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
+              t < clen ? pack_half8(f, x.s_egq[gs + t]) : make_uint4(0, 0, 0, 0);
+        }
       }
     }
     signal(x.mb_qrdy);  // the raw K/Q tile is consumed: it may be refilled
@@ -445,7 +456,7 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     // fp16 copy, which the MMAs read, is separate)
     {
       const float el = x.s_elast[c % 3];
-#pragma unroll
+#pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t s[32];
         tc::tmem_ld32(lanes + P::COL_S + q4 * 32, s);
@@ -460,7 +471,7 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
 
     // ---- u^T as an fp16 hi + lo pair in tensor memory (the A operand of the next MMAs) ---
     {
-#pragma unroll
+#pragma unroll 1
       for (int h2 = 0; h2 < 2; ++h2) {
         uint32_t u[32], hi[16], lo[16];
         tc::tmem_ld32(lanes + col_u + h2 * 32, u);
@@ -484,7 +495,7 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
 
     // ---- next chunk's fp16 S^T operand, and this chunk's output rows -------------------
     {
-#pragma unroll
+#pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t s[32], st[16];
         tc::tmem_ld32(lanes + P::COL_S + q4 * 32, s);
@@ -499,15 +510,20 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
                             static_cast<int64_t>(x.h) * kDim + v;
       const int64_t ostride = p.out_stride;
 #pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t o[32];
-        tc::tmem_ld32(lanes + P::COL_O + h2 * 32, o);
+      for (int g = 0; g < 4; ++g) {
+        uint32_t o[8];
+        tc::tmem_ld8(lanes + P::COL_O + g * 8, o);
+        uint32_t o2[8];
+        tc::tmem_ld8(lanes + P::COL_O + 32 + g * 8, o2);
         tc::tmem_ld_wait();
-        const int n_rows = clen - h2 * 32;  // rows of this half inside the sequence
+        const int n_rows = clen - g * 8;  // rows of this group inside the sequence
+        __nv_bfloat16* op2 = optr + 32 * ostride;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < 8; ++e) {
           if (e < n_rows) *optr = __float2bfloat16_rn(__uint_as_float(o[e]));
+          if (e + 32 < n_rows) *op2 = __float2bfloat16_rn(__uint_as_float(o2[e]));
           optr += ostride;
+          op2 += ostride;
         }
       }
       tc::tmem_st_wait();
@@ -576,7 +592,7 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
   auto gram = [&](int c) {
     constexpr uint32_t idesc = tc::idesc_f16(128, 64, tc::kBF16, false, false);
     const uint32_t kq = x.sbase + ((c & 1) ? P::KQ1 : P::KQ0);
-#pragma unroll
+#pragma unroll 1
     for (int st = 0; st < 8; ++st) {
       const uint32_t a = kq + (st >> 2) * 16384 + (st & 3) * 32;
       tc::mma_f16(x.tmem + P::COL_GW, tc::desc_sw128(a, 16, 1024), tc::desc_sw128(a, 16, 1024), idesc, st > 0);
@@ -591,9 +607,9 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
     const uint32_t d_col = is_u ? P::COL_U + 64 * b : P::COL_GW;
     const uint32_t a_base = x.sbase + (is_u ? (b ? P::V1 : P::V0) : (b ? P::KQ1 : P::KQ0));
     const uint32_t a_lbo = is_u ? 8192 : 16384;
-#pragma unroll
+#pragma unroll 1
     for (int part = 0; part < 2; ++part) {
-#pragma unroll
+#pragma unroll 2
       for (int st = 0; st < 4; ++st)
         tc::mma_f16(x.tmem + d_col, tc::desc_sw128(a_base + st * 2048, a_lbo, 1024),
                     tc::desc_sw128(x.sbase + P::TB + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
@@ -604,7 +620,7 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
     constexpr uint32_t id_u = tc::idesc_f16(128, 64, tc::kF16, false, true);
     constexpr uint32_t id_o = tc::idesc_f16(128, 64, tc::kF16, false, false);
     const uint32_t col_u = P::COL_U + 64 * (c & 1);
-#pragma unroll
+#pragma unroll 1
     for (int st = 0; st < 8; ++st) {
       const uint32_t a = x.tmem + P::COL_ST + st * 8;
       tc::mma_f16_ts(x.tmem + col_u, a, tc::desc_sw128(x.sbase + P::W16 + st * 2048, 16384, 1024), id_u, 1);
@@ -619,7 +635,7 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
     constexpr uint32_t id_o = tc::idesc_f16(128, 64, tc::kF16, false, false);
     const int b = c & 1;
     const uint32_t kd_off = b ? P::KD1 : P::KD0, a_off = b ? P::A1 : P::A0;
-#pragma unroll
+#pragma unroll 1
     for (int st = 0; st < 4; ++st) {
       const uint32_t u_hi = x.tmem + P::COL_UT + st * 8, u_lo = x.tmem + P::COL_UT + 32 + st * 8;
       const uint64_t a_hi = tc::desc_sw128(x.sbase + a_off + st * 32, 16, 1024);
