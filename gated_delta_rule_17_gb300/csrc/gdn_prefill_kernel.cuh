@@ -592,7 +592,7 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
   auto gram = [&](int c) {
     constexpr uint32_t idesc = tc::idesc_f16(128, 64, tc::kBF16, false, false);
     const uint32_t kq = x.sbase + ((c & 1) ? P::KQ1 : P::KQ0);
-#pragma unroll 1
+#pragma unroll
     for (int st = 0; st < 8; ++st) {
       const uint32_t a = kq + (st >> 2) * 16384 + (st & 3) * 32;
       tc::mma_f16(x.tmem + P::COL_GW, tc::desc_sw128(a, 16, 1024), tc::desc_sw128(a, 16, 1024), idesc, st > 0);
@@ -607,9 +607,9 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
     const uint32_t d_col = is_u ? P::COL_U + 64 * b : P::COL_GW;
     const uint32_t a_base = x.sbase + (is_u ? (b ? P::V1 : P::V0) : (b ? P::KQ1 : P::KQ0));
     const uint32_t a_lbo = is_u ? 8192 : 16384;
-#pragma unroll 1
+#pragma unroll
     for (int part = 0; part < 2; ++part) {
-#pragma unroll 2
+#pragma unroll
       for (int st = 0; st < 4; ++st)
         tc::mma_f16(x.tmem + d_col, tc::desc_sw128(a_base + st * 2048, a_lbo, 1024),
                     tc::desc_sw128(x.sbase + P::TB + part * 8192 + st * 32, 16, 1024), id, part + st > 0);
