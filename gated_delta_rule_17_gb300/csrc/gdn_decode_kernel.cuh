@@ -48,6 +48,10 @@ gdn_decode_kernel(const DecodeParams p) {
   float* base = p.state_is_table ? reinterpret_cast<float* const*>(p.state)[b]
                                  : reinterpret_cast<float*>(p.state) + static_cast<int64_t>(b) * p.nv * kDim * kDim;
   float* S = base + static_cast<int64_t>(h) * kDim * kDim;
+  // the state block first, so that its HBM latency overlaps the token's loads
+  float4 s[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) s[i] = *reinterpret_cast<const float4*>(S + (16 * kg + i) * kDim + 4 * vg);
   if (tid < kDim) {
     s_k[tid] = __bfloat162float(p.k[b * p.k_stride + kh * kDim + tid]);
     s_q[tid] = __bfloat162float(p.q[b * p.q_stride + kh * kDim + tid]);
@@ -78,9 +82,6 @@ gdn_decode_kernel(const DecodeParams p) {
   const float bt = p.beta[b * p.beta_stride + h];
 
   // decayed state block and its partial k^T S'
-  float4 s[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) s[i] = *reinterpret_cast<const float4*>(S + (16 * kg + i) * kDim + 4 * vg);
   __syncthreads();
   float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll

@@ -254,13 +254,14 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       if (p.qk_l2norm) tc::named_barrier(kBarNorm, kProducerThreads);
     } else {
       // ---- A (fp16 hi + lo) from Q K^T, lanes 64-127 ------------------------------------
-      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
-      tc::fence_after_sync();
       if (p.qk_l2norm) {
-        // fused prologue: one raw row per thread, K rows 0-63 then Q rows 0-63, read
-        // before any thread converts the tile in place. The inverse norms are folded
-        // into this chunk's per-token factors (K: e^gc, e^{gc_last-gc}, F; Q: e^gc/sqrt(dk),
-        // E) and kept apart for the direct-decay path
+        // fused prologue, while the Gram MMA runs: one raw row per thread, K rows 0-63
+        // then Q rows 0-63, read once the tile has landed and before any thread converts
+        // it in place. The inverse norms are folded into this chunk's per-token factors
+        // (K: e^gc, e^{gc_last-gc}, F; Q: e^gc/sqrt(dk), E) and kept apart for the
+        // direct-decay path
+        ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_kq1 : x.mb_kq0, use, kWaitLimitNs);
+        tc::fence_after_sync();
         const int row = half * 64 + (quad - 2) * 32 + lane, t = row & 63;
         const uint32_t base = kq_off + (row >> 6) * 8192;
         float ss = 0.f;
@@ -282,6 +283,8 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         }
         tc::named_barrier(kBarNorm, kProducerThreads);
       }
+      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
+      tc::fence_after_sync();
       if (ok) {
         const int i = (quad - 2) * 32 + lane;  // A_ij = e^{gc_i - gc_j} q_i.k_j / sqrt(dk), j <= i
         const bool fast = x.s_fast[b] != 0;

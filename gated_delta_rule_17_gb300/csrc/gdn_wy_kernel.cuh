@@ -224,29 +224,30 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
       failed = true;
       break;
     }
-    ok = tc::mbar_wait_timed(mb_g, gph++ & 1, kWaitLimitNs);
+    // ---- fused prologue, while the MMA runs: 1 / |k_t| of every key row (thread pair
+    //      per row), folded into the factor F_t of the decays as well ---------------------
+    if (p.qk_l2norm) {
+      // the tile's arrival is observed by each thread (the phase is already complete)
+      ok = tc::mbar_wait_timed(tc::smem_u32(&s_mb[kb]), kuse, kWaitLimitNs);
+      tc::fence_after_sync();
+      const int t = tid >> 1, part = tid & 1;
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        ss += sumsq_bf16x8(*reinterpret_cast<const uint4*>(sm + k_off + part * 8192 + tc::sw128(t, j * 16)));
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      if (part == 0) {
+        const float r = 1.f / sqrtf(ss + kL2Eps);
+        s_rk[t] = r;
+        s_F[t] *= r;
+      }
+    }
+    ok = ok && tc::mbar_wait_timed(mb_g, gph++ & 1, kWaitLimitNs);
     if (!__syncthreads_and(ok)) {
       failed = true;
       break;
     }
     tc::fence_after_sync();
-
-    // ---- fused prologue: 1 / |k_t| of every key row (thread pair per row), folded into
-    //      the factor F_t of the decays as well ---------------------------------------------
-    if (p.qk_l2norm) {
-      const int t = tid >> 1, kb = tid & 1;
-      float ss = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        ss += sumsq_bf16x8(*reinterpret_cast<const uint4*>(sm + k_off + kb * 8192 + tc::sw128(t, j * 16)));
-      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-      if (kb == 0) {
-        const float r = 1.f / sqrtf(ss + kL2Eps);
-        s_rk[t] = r;
-        s_F[t] *= r;
-      }
-      __syncthreads();
-    }
 
     // ---- L (fp32): row t = 16 warp + l sits in lane 32 warp + l (M = 64 layout) --------
     {
