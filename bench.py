@@ -246,8 +246,12 @@ def run_gpu(args, world, rank, local):
     dp = DeviceProblem(p, device=dev)
     stream = torch.cuda.current_stream(dev)
     ws = None
-    if p.varlen:
-        ws = torch.empty(max(gdn.workspace_bytes(p.B, p.T, p.nv, True), 256), dtype=torch.uint8, device=dev)
+    ws_bytes = gdn.workspace_bytes(p.B, p.T, p.nv, p.varlen)
+    if args.no_segments and not p.varlen:
+        ws = torch.empty(0, dtype=torch.uint8, device=dev)  # declines the segment schedule
+        workload += ", serial spine (no segment workspace)"
+    elif ws_bytes:  # varlen schedule, or the segment schedule of a long dense batch
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
     def step():
         dp.run(workspace=ws)
@@ -432,6 +436,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", default="prefill", choices=["prefill", "decode"],
                     help="prefill (the headline) or the single-token decode step")
+    ap.add_argument("--no-segments", action="store_true",
+                    help="dense batches: run the serial spine even where the segment schedule applies")
     ap.add_argument("--qk-l2norm", action="store_true",
                     help="un-normalised q/k inputs, normalised by the fused prologue")
     ap.add_argument("--decode-batch", type=int, default=256, help="sequences per decode step")

@@ -111,6 +111,198 @@ __global__ void gdn_schedule_kernel(const int32_t* cu, int B, int T, int32_t* or
   if (s == 0) cu_chunks[0] = 0;
 }
 
+// ---- segment-parallel schedule ---------------------------------------------------
+// A dense batch with few (sequence, head) chains and long sequences leaves most SMs
+// idle in the serial spine. The state map of a run of chunks is affine,
+// S_end = M S_start + N (the spine recurrence of ssm_gdn_a3.rs, `gdn_prefill_fla`
+// doc comment, stage 2, is linear in S), so each sequence is cut into G segments
+// of L chunks:
+//   phase 1: segment 0 runs from the carried-in state (with its output rows), and
+//            for each middle segment g = 1 .. G-2 the spine runs twice without output
+//            rows: from S = I with v = 0 (giving M_g) and from S = 0 (giving N_g);
+//   combine: X_{g+1} = M_g X_g + N_g in fp32, g = 1 .. G-2 (X_1 = segment 0's end
+//            state, X_{G-1} lands in the caller's state);
+//   phase 2: segments 1 .. G-1 run from X_g with their output rows.
+// Phase 1 takes chains * (2G - 3) CTAs, so G is the largest count with that within
+// the SM count, at least kSegMinChunks chunks per segment and at most kSegMaxCount.
+constexpr int kSegMinChunks = 8;
+constexpr int kSegMaxCount = 8;
+constexpr int64_t kStateFloats = static_cast<int64_t>(gdn::kDim) * gdn::kDim;
+
+struct SegPlan {
+  int G = 0, L = 0;  // G >= 3 segments of L chunks (the last may be shorter); G = 0: serial
+};
+
+SegPlan seg_plan(int B, int T, int nv, int sms) {
+  SegPlan sp;
+  const int64_t chains = static_cast<int64_t>(B) * nv;
+  const int nchunks = static_cast<int>((static_cast<int64_t>(T) + gdn::kChunk - 1) / gdn::kChunk);
+  if (chains <= 0 || chains * 3 > sms) return sp;
+  int G = static_cast<int>((sms / chains + 3) / 2);
+  if (G > nchunks / kSegMinChunks) G = nchunks / kSegMinChunks;
+  if (G > kSegMaxCount) G = kSegMaxCount;
+  if (G < 3) return sp;
+  const int L = (nchunks + G - 1) / G;
+  G = (nchunks + L - 1) / L;
+  if (G < 3) return sp;
+  sp.G = G;
+  sp.L = L;
+  return sp;
+}
+
+// Workspace of the segment schedule: two segment tables (4 int32 per entry), two
+// state-pointer tables, then the X_1..X_{G-2}, M_1..M_{G-2} and N_1..N_{G-2} states.
+struct SegLayout {
+  size_t tab1 = 0, tab2 = 0, ptr1 = 0, ptr2 = 0, bufs = 0, total = 0;
+  int n1 = 0, n2 = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+SegLayout seg_layout(const SegPlan& sp, int B, int nv) {
+  SegLayout l;
+  if (sp.G < 3) return l;
+  l.n1 = B * (2 * sp.G - 3);
+  l.n2 = B * (sp.G - 1);
+  l.tab1 = 0;
+  l.tab2 = align256(l.tab1 + 16 * static_cast<size_t>(l.n1));
+  l.ptr1 = align256(l.tab2 + 16 * static_cast<size_t>(l.n2));
+  l.ptr2 = align256(l.ptr1 + 8 * static_cast<size_t>(l.n1));
+  l.bufs = align256(l.ptr2 + 8 * static_cast<size_t>(l.n2));
+  l.total = l.bufs + 3 * static_cast<size_t>(sp.G - 2) * B * nv * kStateFloats * sizeof(float);
+  return l;
+}
+
+// SM count for the plan: the current device's, or GB300's 152 where no device is
+// visible (the workspace query works on a host without a GPU).
+int plan_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+    return sms;
+  cudaGetLastError();
+  return 152;
+}
+
+struct SegArgs {
+  int B, T, nv, G, L;
+  int32_t* tab1;
+  int32_t* tab2;
+  float** ptr1;
+  float** ptr2;
+  float* X;  // [G-2][B][nv][128][128]: the states entering segments 1 .. G-2
+  float* M;  // [G-2][B][nv][128][128]
+  float* N;  // [G-2][B][nv][128][128]
+  void* state;  // the caller's state (contiguous, or a table of B pointers)
+  int state_is_table;
+};
+
+__device__ __forceinline__ float* user_state(const SegArgs& a, int b) {
+  return a.state_is_table ? reinterpret_cast<float* const*>(a.state)[b]
+                          : reinterpret_cast<float*>(a.state) + static_cast<int64_t>(b) * a.nv * kStateFloats;
+}
+
+// Builds both segment tables and pointer tables, sets M = I and N = 0, and copies the
+// carried-in state into X_1. Grid-stride over the state buffers.
+__global__ void gdn_segment_setup_kernel(const SegArgs a) {
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int per1 = 2 * a.G - 3, per2 = a.G - 1;
+  const int64_t seg_rows = static_cast<int64_t>(a.L) * gdn::kChunk;
+  const int64_t head = static_cast<int64_t>(a.nv) * kStateFloats;  // floats per (b) state
+  auto seg_len = [&](int g) -> int {
+    const int64_t r = static_cast<int64_t>(a.T) - g * seg_rows;
+    return static_cast<int>(r < seg_rows ? r : seg_rows);
+  };
+  auto buf = [&](float* base, int g, int b) { return base + (static_cast<int64_t>(g - 1) * a.B + b) * head; };
+  if (tid < static_cast<int64_t>(a.B) * per1) {
+    const int b = static_cast<int>(tid / per1), j = static_cast<int>(tid % per1);
+    int g = 0, mode = 0;
+    float* st = nullptr;
+    if (j == 0) {
+      st = buf(a.X, 1, b);
+    } else {
+      g = 1 + (j - 1) / 2;
+      const bool is_m = ((j - 1) & 1) == 0;
+      mode = gdn::kSegNoOutput | (is_m ? gdn::kSegZeroValues : 0);
+      st = buf(is_m ? a.M : a.N, g, b);
+    }
+    int32_t* e = a.tab1 + 4 * tid;
+    e[0] = static_cast<int32_t>(static_cast<int64_t>(b) * a.T + g * seg_rows);
+    e[1] = seg_len(g);
+    e[2] = mode;
+    e[3] = 0;
+    a.ptr1[tid] = st;
+  }
+  if (tid < static_cast<int64_t>(a.B) * per2) {
+    const int b = static_cast<int>(tid / per2), g = 1 + static_cast<int>(tid % per2);
+    int32_t* e = a.tab2 + 4 * tid;
+    e[0] = static_cast<int32_t>(static_cast<int64_t>(b) * a.T + g * seg_rows);
+    e[1] = seg_len(g);
+    e[2] = 0;
+    e[3] = 0;
+    a.ptr2[tid] = g < a.G - 1 ? buf(a.X, g, b) : user_state(a, b);
+  }
+  const int64_t nbuf = static_cast<int64_t>(a.G - 2) * a.B * head;
+  for (int64_t i = tid; i < nbuf; i += nthreads) {
+    const int64_t w = i % kStateFloats;
+    a.M[i] = (w / gdn::kDim == w % gdn::kDim) ? 1.f : 0.f;
+    a.N[i] = 0.f;
+  }
+  for (int64_t i = tid; i < static_cast<int64_t>(a.B) * head; i += nthreads) {
+    const int b = static_cast<int>(i / head);
+    a.X[i] = user_state(a, b)[i % head];  // X_1 is the first block of X
+  }
+}
+
+// X_out = M X_in + N for every (sequence, head) of one segment step, fp32 on the CUDA
+// cores (128 x 128 x 128 per head). CTA = one 64 x 64 output tile; thread = 4 x 4.
+constexpr int kCombineThreads = 256;
+__global__ void __launch_bounds__(kCombineThreads) gdn_segment_combine_kernel(const SegArgs a, int g) {
+  __shared__ float sa[64][17];
+  __shared__ __align__(16) float sb[16][64];
+  const int tile = blockIdx.x & 3, bh = blockIdx.x >> 2;
+  const int b = bh / a.nv, h = bh % a.nv;
+  const int r0 = (tile >> 1) * 64, c0 = (tile & 1) * 64;
+  const int64_t head = static_cast<int64_t>(a.nv) * kStateFloats;
+  const int64_t off = (static_cast<int64_t>(g - 1) * a.B + b) * head + static_cast<int64_t>(h) * kStateFloats;
+  const float* Mh = a.M + off;
+  const float* Nh = a.N + off;
+  const float* Xin = a.X + off;
+  float* Xout = g + 1 < a.G - 1 ? a.X + off + static_cast<int64_t>(a.B) * head
+                                : user_state(a, b) + static_cast<int64_t>(h) * kStateFloats;
+  const int tid = threadIdx.x, tr = (tid >> 4) * 4, tc = (tid & 15) * 4;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < gdn::kDim; k0 += 16) {
+    for (int i = tid; i < 64 * 16; i += kCombineThreads) {
+      const int r = i >> 4, c = i & 15;
+      sa[r][c] = Mh[(r0 + r) * gdn::kDim + k0 + c];
+      sb[i >> 6][i & 63] = Xin[(k0 + (i >> 6)) * gdn::kDim + c0 + (i & 63)];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const float4 bv = *reinterpret_cast<const float4*>(&sb[kk][tc]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float av = sa[tr + i][kk];
+        acc[i][0] = fmaf(av, bv.x, acc[i][0]);
+        acc[i][1] = fmaf(av, bv.y, acc[i][1]);
+        acc[i][2] = fmaf(av, bv.z, acc[i][2]);
+        acc[i][3] = fmaf(av, bv.w, acc[i][3]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t o = static_cast<int64_t>(r0 + tr + i) * gdn::kDim + c0 + tc + j;
+      Xout[o] = acc[i][j] + Nh[o];
+    }
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int make_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows, int64_t stride_elems, const char* name) {
@@ -164,7 +356,8 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
 }
 
 int launch(const void* q, const void* k, const void* v, const float* g, const float* beta, void* state, void* out,
-           int B, int T, int nk, int nv, const Resolved& r, const int32_t* cu, int32_t* sched, cudaStream_t stream) {
+           int B, int T, int nk, int nv, const Resolved& r, const int32_t* cu, int32_t* sched, cudaStream_t stream,
+           void* seg_ws = nullptr, size_t seg_ws_bytes = 0) {
   DeviceInfo* d = nullptr;
   if (int rc = device_info(&d)) return rc;
   const int64_t rows = cu ? static_cast<int64_t>(T) : static_cast<int64_t>(B) * T;
@@ -220,6 +413,7 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   p.nv = nv;
   p.state_is_table = r.table;
   p.qk_l2norm = r.l2norm;
+  p.seg = nullptr;
   int launches = 0;
   if (cu) {
     gdn_schedule_kernel<<<(B + 255) / 256, 256, 0, stream>>>(cu, B, T, order, cu_chunks, d->status);
@@ -231,11 +425,57 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   if (g_timing[1]) cudaEventRecord(g_timing[1], stream);
   // one CTA per (sequence, v-head); CTAs of the same sequence and GQA group are
   // adjacent so their shared q/k tiles meet in L2
-  const int64_t grid = static_cast<int64_t>(B) * nv;
-  if (grid > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "grid of %lld CTAs too large", (long long)grid);
-  gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt,
-                                                                                                      p);
-  ++launches;
+  const SegPlan sp = cu ? SegPlan() : seg_plan(B, T, nv, d->sms);
+  const SegLayout sl = seg_layout(sp, B, nv);
+  if (sp.G >= 3 && seg_ws && seg_ws_bytes >= sl.total) {
+    // segment-parallel schedule (see seg_plan): setup, phase 1, the combine steps, phase 2
+    char* w8 = static_cast<char*>(seg_ws);
+    SegArgs a;
+    a.B = B;
+    a.T = T;
+    a.nv = nv;
+    a.G = sp.G;
+    a.L = sp.L;
+    a.tab1 = reinterpret_cast<int32_t*>(w8 + sl.tab1);
+    a.tab2 = reinterpret_cast<int32_t*>(w8 + sl.tab2);
+    a.ptr1 = reinterpret_cast<float**>(w8 + sl.ptr1);
+    a.ptr2 = reinterpret_cast<float**>(w8 + sl.ptr2);
+    const size_t blk = static_cast<size_t>(sp.G - 2) * B * nv * kStateFloats;
+    a.X = reinterpret_cast<float*>(w8 + sl.bufs);
+    a.M = a.X + blk;
+    a.N = a.M + blk;
+    a.state = state;
+    a.state_is_table = r.table;
+    gdn_segment_setup_kernel<<<d->sms * 4, 256, 0, stream>>>(a);
+    ++launches;
+    gdn::ChunkParams ps = p;
+    ps.cu_seqlens = nullptr;
+    ps.order = nullptr;
+    ps.state_is_table = 1;
+    ps.T = static_cast<int>(rows);
+    ps.seg = a.tab1;
+    ps.state = a.ptr1;
+    ps.B = sl.n1;
+    gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(static_cast<int64_t>(sl.n1) * nv), gdn::kThreads,
+                                gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt, ps);
+    ++launches;
+    for (int gs = 1; gs <= sp.G - 2; ++gs) {
+      gdn_segment_combine_kernel<<<static_cast<unsigned>(B * nv * 4), kCombineThreads, 0, stream>>>(a, gs);
+      ++launches;
+    }
+    ps.seg = a.tab2;
+    ps.state = a.ptr2;
+    ps.B = sl.n2;
+    gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(static_cast<int64_t>(sl.n2) * nv), gdn::kThreads,
+                                gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt, ps);
+    ++launches;
+  } else {
+    const int64_t grid = static_cast<int64_t>(B) * nv;
+    if (grid > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "grid of %lld CTAs too large", (long long)grid);
+    gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan::DYN_SMEM, stream>>>(
+        mq, mk, mv, mt, p);
+    ++launches;
+  }
   if (g_timing[2]) cudaEventRecord(g_timing[2], stream);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
@@ -243,9 +483,12 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   return GDN_OK;
 }
 
-// varlen: the sequence order (B int32) followed by the chunk prefix (B + 1 int32)
-size_t workspace_bytes(int B, int varlen) {
-  if (!varlen || B <= 0) return 0;
+// varlen: the sequence order (B int32) followed by the chunk prefix (B + 1 int32);
+// dense: the segment schedule's tables and states when seg_plan cuts the sequences
+// (0 when it does not)
+size_t workspace_bytes(int B, int T, int nv, int varlen) {
+  if (B <= 0) return 0;
+  if (!varlen) return seg_layout(seg_plan(B, T, nv, plan_sms()), B, nv).total;
   return ((2 * static_cast<size_t>(B) + 1) * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
 }
 
@@ -282,11 +525,10 @@ int noalloc_scratch(int32_t** out) {
 extern "C" {
 
 size_t gdn_prefill_workspace_bytes(int B, int T, int nv, int dk, int dv, int varlen) {
-  (void)T;
-  (void)nv;
   (void)dk;
   (void)dv;
-  return workspace_bytes(B, varlen);
+  if (T < 0 || nv <= 0) return 0;
+  return workspace_bytes(B, T, nv, varlen);
 }
 
 int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -298,13 +540,18 @@ int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
   Resolved r;
   if (int rc = validate(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, dk, dv, strides, &r)) return rc;
   if (B == 0 || (T == 0 && !cu_seqlens)) return GDN_OK;
-  const size_t need = workspace_bytes(B, cu_seqlens != nullptr);
-  if (workspace_bytes_ < need) return fail(GDN_ERR_ARG, "workspace of %zu bytes is smaller than the %zu required", workspace_bytes_, need);
-  if (need && !workspace) return fail(GDN_ERR_ARG, "workspace is NULL but %zu bytes are required", need);
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return fail(GDN_ERR_ARG, "workspace must be 256-byte aligned");
-  if (T == 0) return GDN_OK;  // varlen with no rows: every sequence is empty
-  return launch(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, r, cu_seqlens, static_cast<int32_t*>(workspace),
-                static_cast<cudaStream_t>(stream));
+  if (cu_seqlens) {
+    const size_t need = workspace_bytes(B, T, nv, 1);
+    if (workspace_bytes_ < need) return fail(GDN_ERR_ARG, "workspace of %zu bytes is smaller than the %zu required", workspace_bytes_, need);
+    if (need && !workspace) return fail(GDN_ERR_ARG, "workspace is NULL but %zu bytes are required", need);
+    if (T == 0) return GDN_OK;  // varlen with no rows: every sequence is empty
+    return launch(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, r, cu_seqlens, static_cast<int32_t*>(workspace),
+                  static_cast<cudaStream_t>(stream));
+  }
+  // dense: the workspace is optional; with enough of it long sequences run segment-parallel
+  return launch(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, r, nullptr, nullptr,
+                static_cast<cudaStream_t>(stream), workspace, workspace ? workspace_bytes_ : 0);
 }
 
 int gdn_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta, void* h_state_inout,
@@ -315,14 +562,15 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
   Resolved r;
   if (int rc = validate(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, dk, dv, strides, &r)) return rc;
   if (B == 0 || T == 0) return GDN_OK;
-  const size_t need = workspace_bytes(B, cu_seqlens != nullptr);
+  const size_t need = workspace_bytes(B, T, nv, cu_seqlens != nullptr);
   void* ws = nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (need) {
     cudaError_t e = cudaMallocAsync(&ws, need, s);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaMallocAsync(%zu): %s", need, cudaGetErrorString(e));
   }
-  int rc = launch(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, r, cu_seqlens, static_cast<int32_t*>(ws), s);
+  int rc = cu_seqlens ? launch(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, r, cu_seqlens, static_cast<int32_t*>(ws), s)
+                      : launch(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, r, nullptr, nullptr, s, ws, need);
   if (ws) {
     cudaError_t e = cudaFreeAsync(ws, s);
     if (e != cudaSuccess && rc == GDN_OK) rc = fail(GDN_ERR_CUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));

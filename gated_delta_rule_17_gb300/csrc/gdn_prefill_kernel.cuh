@@ -64,7 +64,14 @@ struct ChunkParams {
   int B, T, nk, nv;
   int state_is_table;
   int qk_l2norm;              // fused prologue: normalise every q and k row first
+  // Segment table (null: none). Entry s = {first row, length, mode, 0} of the row range
+  // CTA slot s runs, for the segment-parallel schedule of long sequences; mode bit 0
+  // skips the output rows (the range's T diag(beta) rows stay in place for a later run),
+  // bit 1 runs it with v = 0 (the state map's linear part).
+  const int32_t* seg;
 };
+constexpr int kSegNoOutput = 1;
+constexpr int kSegZeroValues = 2;
 
 // Shared-memory plan (bytes from a 1024-aligned base). Operand tiles are
 // row-major 16-bit tiles stored as 64-column blocks of 128-byte swizzled rows
@@ -103,6 +110,7 @@ struct Ctx {
   uint32_t tmem;     // tensor-memory base address
   int64_t row0, len; // first packed row and length of the sequence
   int nchunks, h, kh;
+  int store_out, zero_v;  // segment modes (1, 0 outside segment runs)
   float* state;      // this (sequence, head)'s fp32 [128][128] state, k-major
   // producer-side per-token scales, two gate sets by chunk parity ([2][64] each)
   float *s_gc, *s_eg, *s_egq, *s_edec;  // gc, e^gc, e^gc / sqrt(dk), e^{gc_last - gc}
@@ -246,7 +254,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
             float f[8];
             unpack_bf16x8(raw[r], f);
             *reinterpret_cast<uint4*>(sm + v_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
-                t < clen ? pack_half8(f, 1.f) : make_uint4(0, 0, 0, 0);
+                t < clen && !x.zero_v ? pack_half8(f, 1.f) : make_uint4(0, 0, 0, 0);
           }
         }
       }
@@ -447,6 +455,27 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
   }
   signal(x.mb_strdy);  // S^T of the first chunk is ready
 
+  // S^T <- e^{gc_last} S^T, the decay half of the state update of chunk `cn` (its fp16
+  // copy, which the MMAs read, is separate): two 64-column halves, both loads in flight
+  auto decay_state = [&](int cn) {
+    const float el = x.s_elast[cn % 3];
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      uint32_t s0[32], s1[32];
+      tc::tmem_ld32(lanes + P::COL_S + h * 64, s0);
+      tc::tmem_ld32(lanes + P::COL_S + h * 64 + 32, s1);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        s0[e] = __float_as_uint(el * __uint_as_float(s0[e]));
+        s1[e] = __float_as_uint(el * __uint_as_float(s1[e]));
+      }
+      tc::tmem_st32(lanes + P::COL_S + h * 64, s0);
+      tc::tmem_st32(lanes + P::COL_S + h * 64 + 32, s1);
+    }
+    tc::tmem_st_wait();
+  };
+
   for (int c = 0; c < x.nchunks; ++c) {
     const int b = c & 1;
     const int64_t rem = x.len - static_cast<int64_t>(c) * kChunk;
@@ -454,22 +483,9 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     const uint32_t col_u = P::COL_U + 64 * b;
 
     if (!group_wait(x, p, x.mb_hand, b, kBarConsumer, kConsumerThreads, leader)) break;
-    // (the issuer runs u^T = U^T - S^T W^T onto U^T and O^T = S^T Q~^T)
-    // meanwhile: S^T <- e^{gc_last} S^T, the decay half of the state update (its
-    // fp16 copy, which the MMAs read, is separate)
-    {
-      const float el = x.s_elast[c % 3];
-#pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t s[32];
-        tc::tmem_ld32(lanes + P::COL_S + q4 * 32, s);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s[e] = __float_as_uint(el * __uint_as_float(s[e]));
-        tc::tmem_st32(lanes + P::COL_S + q4 * 32, s);
-      }
-      tc::tmem_st_wait();
-    }
+    // (the issuer runs u^T = U^T - S^T W^T onto U^T and O^T = S^T Q~^T.) The decay of
+    // chunk c > 0 was applied at the end of the previous iteration, while these ran.
+    if (c == 0) decay_state(0);
     if (!group_wait(x, p, x.mb_c1, b, kBarConsumer, kConsumerThreads, leader)) break;
 
     // ---- u^T as an fp16 hi + lo pair in tensor memory (the A operand of the next MMAs) ---
@@ -496,7 +512,8 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     signal(b ? x.mb_cu1 : x.mb_cu0);     // the U columns of this chunk parity are free again
     if (!group_wait(x, p, b ? x.mb_c21 : x.mb_c20, (c >> 1) & 1, kBarConsumer, kConsumerThreads, leader)) break;
 
-    // ---- next chunk's fp16 S^T operand, and this chunk's output rows -------------------
+    // ---- next chunk's fp16 S^T operand; this chunk's O^T into registers ---------------
+    uint32_t o[64];
     {
 #pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
@@ -507,31 +524,30 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
         for (int e = 0; e < 16; ++e) st[e] = pack_half2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]));
         tc::tmem_st16u(lanes + P::COL_ST + q4 * 16, st);
       }
+      uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(o);
+      uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(o + 32);
+      tc::tmem_ld32(lanes + P::COL_O, o0);
+      tc::tmem_ld32(lanes + P::COL_O + 32, o1);
+      tc::tmem_ld_wait();
+      tc::tmem_st_wait();
+    }
+    signal(x.mb_strdy);  // S^T of the next chunk is ready and O^T has been read
+
+    // ---- meanwhile (the next chunk's first MMAs run): this chunk's output rows, then
+    //      the decay of the next chunk --------------------------------------------------
+    if (x.store_out) {
       // O^T holds one value column per thread: for each row t, the 32 lanes of a warp
       // store 32 consecutive bf16 values, one 64-byte segment (no shared-memory staging)
       __nv_bfloat16* optr = p.out + (x.row0 + static_cast<int64_t>(c) * kChunk) * p.out_stride +
                             static_cast<int64_t>(x.h) * kDim + v;
       const int64_t ostride = p.out_stride;
-#pragma unroll 1
-      for (int g = 0; g < 4; ++g) {
-        uint32_t o[8];
-        tc::tmem_ld8(lanes + P::COL_O + g * 8, o);
-        uint32_t o2[8];
-        tc::tmem_ld8(lanes + P::COL_O + 32 + g * 8, o2);
-        tc::tmem_ld_wait();
-        const int n_rows = clen - g * 8;  // rows of this group inside the sequence
-        __nv_bfloat16* op2 = optr + 32 * ostride;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          if (e < n_rows) *optr = __float2bfloat16_rn(__uint_as_float(o[e]));
-          if (e + 32 < n_rows) *op2 = __float2bfloat16_rn(__uint_as_float(o2[e]));
-          optr += ostride;
-          op2 += ostride;
-        }
+      for (int e = 0; e < 64; ++e) {
+        if (e < clen) *optr = __float2bfloat16_rn(__uint_as_float(o[e]));
+        optr += ostride;
       }
-      tc::tmem_st_wait();
     }
-    signal(x.mb_strdy);  // S^T of the next chunk is ready and O^T has been read
+    if (c + 1 < x.nchunks) decay_state(c + 1);
   }
 
   if (*x.s_abort == 0) {  // carried-out state S_T, k-major
@@ -716,7 +732,14 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   const int slot = blockIdx.x / p.nv;
   const int s = p.order ? p.order[slot] : slot;
   x.kh = x.h / (p.nv / p.nk);
-  if (p.cu_seqlens) {
+  x.store_out = 1;
+  x.zero_v = 0;
+  if (p.seg) {  // host-built segment table: trusted ranges inside the packed rows
+    x.row0 = p.seg[4 * s];
+    x.len = p.seg[4 * s + 1];
+    x.store_out = (p.seg[4 * s + 2] & kSegNoOutput) == 0;
+    x.zero_v = (p.seg[4 * s + 2] & kSegZeroValues) != 0;
+  } else if (p.cu_seqlens) {
     if (s < 0 || s >= p.B) {
       if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
       return;

@@ -173,6 +173,7 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
   bool ok = true, failed = false;
   uint32_t gph = 0;  // completed phases of the MMA barrier
 
+  prefetch(cur, 0);  // the first item's tiles; each later item's are fetched during the one before
   int n = 0;
   for (int it = static_cast<int>(blockIdx.x); it < items; it += static_cast<int>(gridDim.x), ++n) {
     const int kb = 0;
@@ -184,9 +185,8 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     const uint32_t al = sbase + k_off + P::S_AL - 4096;
     const int clen = cur.clen;
 
-    // ---- this item's tiles ----------------------------------------------------------
-    prefetch(cur, 0);
     const int nx = it + static_cast<int>(gridDim.x);
+    WyItem nxt = cur;
 
     // ---- gates (warp 1; padding tokens: g = 0, beta = 0) -------------------------------
     if (warp == 1) {
@@ -432,6 +432,13 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
       break;
     }
     tc::fence_after_sync();
+    // The K region is dead for this item (its last reader, the MMA above, has completed,
+    // and every thread fenced its generic accesses before that MMA was issued): the next
+    // item's tile and gates are fetched now, behind the rest of this solve and its store.
+    if (nx < items) {
+      nxt = wy_locate(p, nx);
+      prefetch(nxt, 0);
+    }
     // X (accumulator rows 32-63: warps 2, 3, lanes 0-15) as the bf16 B tile of the
     // second product, over the consumed T[0:32, 0:32] tile
     if (warp >= 2) {
@@ -502,11 +509,10 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
         }
       }
     }
-    // this item's K buffer (now scratch) is refilled by TMA two items on
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
-    if (nx < items) cur = wy_locate(p, nx);
+    cur = nxt;
   }
 
   if (failed) {

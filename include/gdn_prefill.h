@@ -115,15 +115,28 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
                 void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
                 const gdn_strides_t* strides, const int32_t* cu_seqlens, void* stream);
 
-/* Bytes of device scratch gdn_prefill_ex needs for these sizes (0 for dense
- * batches; for varlen ones a schedule of 2B + 1 int32: the sequence order
- * and the chunk prefix over the sequences, rounded up to 256 bytes). */
+/* Bytes of device scratch gdn_prefill_ex needs for these sizes. Varlen
+ * batches: a schedule of 2B + 1 int32 (the sequence order and the chunk
+ * prefix over the sequences), rounded up to 256 bytes. Dense batches: 0, or,
+ * when the batch has few (sequence, head) chains for the device's SM count and
+ * long sequences (at least 3 segments of 8 chunks; B * nv * 3 <= SMs), the
+ * segment-parallel schedule's scratch: two segment tables and pointer tables
+ * (under 4 KB for small B) plus 3 (G - 2) fp32 states of nv x 128 x 128 per
+ * sequence, G being the segment count. The state map of a run of chunks is
+ * affine in the entry state (the spine stage of ssm_gdn_a3.rs
+ * `gdn_prefill_fla`), so the library computes the middle segments' maps in
+ * parallel with the first segment, chains the segment entry states, and runs
+ * the remaining segments in parallel. The SM count is the current device's,
+ * or 152 when no device is visible. */
 size_t gdn_prefill_workspace_bytes(int B, int T, int nv, int dk, int dv, int varlen);
 
 /* gdn_prefill with caller-provided scratch: `workspace` is a device buffer
  * of at least gdn_prefill_workspace_bytes(...) bytes (may be NULL when that
  * is 0), 256-byte aligned, not used by other work until the stream passes
- * this call. Allocates nothing. */
+ * this call. Allocates nothing. Varlen batches require the full size (else
+ * GDN_ERR_ARG). For dense batches the workspace is optional: with at least
+ * the queried size the segment-parallel schedule runs, with less (or NULL)
+ * the serial one; both meet the same tolerances. */
 int gdn_prefill_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,
                    void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
                    const gdn_strides_t* strides, const int32_t* cu_seqlens, void* workspace,
