@@ -34,7 +34,7 @@
 namespace gdn {
 
 constexpr int kWyThreads = 128;
-constexpr int kWyCtasPerSm = 4;
+constexpr int kWyCtasPerSm = 5;
 
 struct WyParams {
   const float* g;
@@ -58,16 +58,18 @@ struct WyPlan {
   static constexpr int K0 = 0;              // raw bf16 K tile (2 blocks x 64 rows); once its Gram
                                             //   MMA is done it holds the item's scratch
   static constexpr int LF = 16384;          // fp32 64 x 64 L, overwritten by T
-  static constexpr int BT = LF + 16384;     // bf16 hi, lo of T[0:32, 0:32] (B, rows m), later of X
-  static constexpr int AT = BT + 8192;      // bf16 hi, lo of T[32:64, 32:64]: A rows 32-63 of tiles
-                                            //   based 4 KB earlier (hi) and here (lo)
-  static constexpr int BYTES = AT + 8192;
+  static constexpr int BYTES = LF + 16384;
   static constexpr int DYN_SMEM = BYTES + 1024;  // slack for 1024-byte alignment
-  // scratch inside the item's own (consumed) K tile
+  // Scratch inside the item's own (consumed) K tile. The merge operands are 64-row
+  // tiles at base 0 (hi) and 8 KB (lo): rows 0-31 of a tile are its B part, rows 32-63
+  // its A part (an MMA of M = 64 reads rows 0-31 of its A tile too; those rows only
+  // feed accumulator rows it ignores).
   static constexpr int S_LT = 0;       // fp32 4 x 16 x 16 diagonal blocks of L, transposed
-  static constexpr int S_AL = 4096;    // bf16 hi of L[32:64, 0:32] (A rows 32-63 of a tile based at 0),
-                                       //   lo 8 KB on (tile based at 8 KB)
+  static constexpr int S_AL = 4096;    // bf16 hi of L[32:64, 0:32] (A rows 32-63 of the tile at 0),
+                                       //   lo 8 KB on (the tile at 8 KB); later T[32:64, 32:64]
   static constexpr int S_X16 = 8192;   // fp32 2 x 16 x 16 partial products
+  static constexpr int BT_HI = 0;      // bf16 hi of T[0:32, 0:32] (B rows m), later of X (over S_LT)
+  static constexpr int BT_LO = 8192;   // ... lo (over S_X16)
   static constexpr uint32_t TMEM_COLS = 64;  // K K^T (M = 64), then X and T22 X (32 columns each)
 };
 
@@ -251,64 +253,62 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
 
     // ---- L (fp32): row t = 16 warp + l sits in lane 32 warp + l (M = 64 layout) --------
     {
-      uint32_t d[2][32];
-      tc::tmem_ld32(tmem + ((warp * 32u) << 16), d[0]);
-      tc::tmem_ld32(tmem + ((warp * 32u) << 16) + 32, d[1]);
-      tc::tmem_ld_wait();
-      if (lane < 16) {
-        const int t = 16 * warp + lane;
-        const bool live = t < clen;
-        const bool fast = s_fast != 0;
-        const bool norm = p.qk_l2norm != 0;
-        const float rt = norm ? s_rk[t] : 1.f;
-        const float bt = live ? s_beta[t] * rt : 0.f, be = bt * s_E[t], gt = s_gc[t];
+      const int t = 16 * warp + (lane & 15);  // lanes 16-31 hold no row of the M = 64 layout
+      const bool live = t < clen;
+      const bool fast = s_fast != 0;
+      const bool norm = p.qk_l2norm != 0;
+      const float rt = norm ? s_rk[t] : 1.f;
+      const float bt = live ? s_beta[t] * rt : 0.f, be = bt * s_E[t], gt = s_gc[t];
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {  // 32 columns at a time
+        uint32_t d[32];
+        tc::tmem_ld32(tmem + ((warp * 32u) << 16) + hf * 32, d);
+        tc::tmem_ld_wait();
+        if (lane >= 16) continue;
+        float l[32];
+        if (fast) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float l[32];
-          if (fast) {
-#pragma unroll
-            for (int e4 = 0; e4 < 8; ++e4) {
-              const float4 f4 = *reinterpret_cast<const float4*>(s_F + hf * 32 + 4 * e4);
-              const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int e = 4 * e4 + q, j = hf * 32 + e;
-                l[e] = j < t ? be * fv[q] * __uint_as_float(d[hf][e]) : 0.f;
-              }
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int j = hf * 32 + e;
-              l[e] = j < t ? bt * (norm ? s_rk[j] : 1.f) * __expf(gt - s_gc[j]) * __uint_as_float(d[hf][e]) : 0.f;
-            }
-          }
-#pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4)
-            *reinterpret_cast<float4*>(lf + lf_idx(t, hf * 32 + j4 * 4)) =
-                make_float4(l[4 * j4], l[4 * j4 + 1], l[4 * j4 + 2], l[4 * j4 + 3]);
-          // rows 32-63, columns 0-31: the A tile of the final merge (bf16 hi, lo)
-          if (hf == 0 && t >= 32) {
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 f4 = *reinterpret_cast<const float4*>(s_F + hf * 32 + 4 * e4);
+            const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              uint32_t hi[4], lo[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) split_bf162(l[8 * q + 2 * e], l[8 * q + 2 * e + 1], hi[e], lo[e]);
-              const uint32_t o = tc::sw128(t, q * 16);
-              *reinterpret_cast<uint4*>(sm + k_off + P::S_AL - 4096 + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-              *reinterpret_cast<uint4*>(sm + k_off + P::S_AL + 4096 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+              const int e = 4 * e4 + q, j = hf * 32 + e;
+              l[e] = j < t ? be * fv[q] * __uint_as_float(d[e]) : 0.f;
             }
           }
-          // this row's part of its diagonal 16 x 16 block (block `warp`), transposed
-          if ((warp >> 1) == hf) {
-            float* dst = lt + warp * 256 + lane;
-            if (warp & 1) {
+        } else {
 #pragma unroll
-              for (int m = 0; m < 16; ++m) dst[m * 16] = l[16 + m];
-            } else {
+          for (int e = 0; e < 32; ++e) {
+            const int j = hf * 32 + e;
+            l[e] = j < t ? bt * (norm ? s_rk[j] : 1.f) * __expf(gt - s_gc[j]) * __uint_as_float(d[e]) : 0.f;
+          }
+        }
 #pragma unroll
-              for (int m = 0; m < 16; ++m) dst[m * 16] = l[m];
-            }
+        for (int j4 = 0; j4 < 8; ++j4)
+          *reinterpret_cast<float4*>(lf + lf_idx(t, hf * 32 + j4 * 4)) =
+              make_float4(l[4 * j4], l[4 * j4 + 1], l[4 * j4 + 2], l[4 * j4 + 3]);
+        // rows 32-63, columns 0-31: the A tile of the final merge (bf16 hi, lo)
+        if (hf == 0 && t >= 32) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_bf162(l[8 * q + 2 * e], l[8 * q + 2 * e + 1], hi[e], lo[e]);
+            const uint32_t o = tc::sw128(t, q * 16);
+            *reinterpret_cast<uint4*>(sm + k_off + P::S_AL - 4096 + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(sm + k_off + P::S_AL + 4096 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        // this row's part of its diagonal 16 x 16 block (block `warp`), transposed
+        if ((warp >> 1) == hf) {
+          float* dst = lt + warp * 256 + lane;
+          if (warp & 1) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) dst[m * 16] = l[16 + m];
+          } else {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) dst[m * 16] = l[m];
           }
         }
       }
@@ -386,28 +386,19 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
       *reinterpret_cast<float4*>(lf + lf_idx(rr, cb - 16 + c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
-    // (c) the last merge on the tensor cores. Operands as bf16 hi + lo: T[0:32, 0:32]
-    //     (B tile, rows m) and T[32:64, 32:64] (A tile, rows 32-63); each thread
-    //     converts 8 values of one row of each.
+    // (c) the last merge on the tensor cores, with bf16 hi + lo operands. First
+    //     T[0:32, 0:32] (the B tile, rows m): each thread converts 8 values of one row.
     {
       const int r = tid >> 2, q = tid & 3;  // row 0-31, 8-column group
       const float4 a0 = *reinterpret_cast<const float4*>(lf + lf_idx(r, 8 * q));
       const float4 a1 = *reinterpret_cast<const float4*>(lf + lf_idx(r, 8 * q + 4));
-      const float4 b0 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 32 + 8 * q));
-      const float4 b1 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 36 + 8 * q));
       uint32_t hi[4], lo[4];
       split_bf162(a0.x, a0.y, hi[0], lo[0]);
       split_bf162(a0.z, a0.w, hi[1], lo[1]);
       split_bf162(a1.x, a1.y, hi[2], lo[2]);
       split_bf162(a1.z, a1.w, hi[3], lo[3]);
-      *reinterpret_cast<uint4*>(sm + P::BT + tc::sw128(r, q * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(sm + P::BT + 4096 + tc::sw128(r, q * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      split_bf162(b0.x, b0.y, hi[0], lo[0]);
-      split_bf162(b0.z, b0.w, hi[1], lo[1]);
-      split_bf162(b1.x, b1.y, hi[2], lo[2]);
-      split_bf162(b1.z, b1.w, hi[3], lo[3]);
-      *reinterpret_cast<uint4*>(sm + P::AT - 4096 + tc::sw128(32 + r, q * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(sm + P::AT + tc::sw128(32 + r, q * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(sm + k_off + P::BT_HI + tc::sw128(r, q * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(sm + k_off + P::BT_LO + tc::sw128(r, q * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
@@ -425,22 +416,30 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
                       tc::desc_sw128(bs[pr] + st * 2048, 64, 1024), id, pr + st > 0);
       tc::mma_commit(mb_g);
     };
-    if (tid == 0) merge_mma(0, al, al + 8192, sbase + P::BT, sbase + P::BT + 4096);
+    const uint32_t bt_hi = sbase + k_off + P::BT_HI, bt_lo = sbase + k_off + P::BT_LO;
+    if (tid == 0) merge_mma(0, al, al + 8192, bt_hi, bt_lo);
     ok = tc::mbar_wait_timed(mb_g, gph++ & 1, kWaitLimitNs);
     if (!__syncthreads_and(ok)) {
       failed = true;
       break;
     }
     tc::fence_after_sync();
-    // The K region is dead for this item (its last reader, the MMA above, has completed,
-    // and every thread fenced its generic accesses before that MMA was issued): the next
-    // item's tile and gates are fetched now, behind the rest of this solve and its store.
-    if (nx < items) {
-      nxt = wy_locate(p, nx);
-      prefetch(nxt, 0);
+    // L[32:64, 0:32] is consumed: T[32:64, 32:64] takes its place as the A rows 32-63 of
+    // the same two tiles (each thread converts 8 values of one row) ...
+    {
+      const int r = tid >> 2, q = tid & 3;
+      const float4 b0 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 32 + 8 * q));
+      const float4 b1 = *reinterpret_cast<const float4*>(lf + lf_idx(32 + r, 36 + 8 * q));
+      uint32_t hi[4], lo[4];
+      split_bf162(b0.x, b0.y, hi[0], lo[0]);
+      split_bf162(b0.z, b0.w, hi[1], lo[1]);
+      split_bf162(b1.x, b1.y, hi[2], lo[2]);
+      split_bf162(b1.z, b1.w, hi[3], lo[3]);
+      *reinterpret_cast<uint4*>(sm + k_off + P::S_AL - 4096 + tc::sw128(32 + r, q * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(sm + k_off + P::S_AL + 4096 + tc::sw128(32 + r, q * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    // X (accumulator rows 32-63: warps 2, 3, lanes 0-15) as the bf16 B tile of the
-    // second product, over the consumed T[0:32, 0:32] tile
+    // ... and X (accumulator rows 32-63: warps 2, 3, lanes 0-15) becomes the bf16 B tile
+    // of the second product, over the consumed T[0:32, 0:32] tile
     if (warp >= 2) {
       uint32_t d[32];
       tc::tmem_ld32(tmem + ((warp * 32u) << 16), d);
@@ -453,8 +452,8 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             split_bf162(__uint_as_float(d[8 * q + 2 * e]), __uint_as_float(d[8 * q + 2 * e + 1]), hi[e], lo[e]);
-          *reinterpret_cast<uint4*>(sm + P::BT + tc::sw128(m, q * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(sm + P::BT + 4096 + tc::sw128(m, q * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(sm + k_off + P::BT_HI + tc::sw128(m, q * 16)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm + k_off + P::BT_LO + tc::sw128(m, q * 16)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
     }
@@ -462,13 +461,20 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     tc::fence_before_sync();
     __syncthreads();
     // T22 X (M = 64, N = 32, K = 32) into accumulator columns 32-63
-    if (tid == 0) merge_mma(32, sbase + P::AT - 4096, sbase + P::AT, sbase + P::BT, sbase + P::BT + 4096);
+    if (tid == 0) merge_mma(32, al, al + 8192, bt_hi, bt_lo);
     ok = tc::mbar_wait_timed(mb_g, gph++ & 1, kWaitLimitNs);
     if (!__syncthreads_and(ok)) {
       failed = true;
       break;
     }
     tc::fence_after_sync();
+    // The K region is dead for this item (its last reader, the MMA above, has completed,
+    // and every thread fenced its generic accesses before that MMA was issued): the next
+    // item's tile and gates are fetched now, behind the rest of this item and its store.
+    if (nx < items) {
+      nxt = wy_locate(p, nx);
+      prefetch(nxt, 0);
+    }
     // T[32:64, 0:32] = -T22 X
     if (warp >= 2) {
       uint32_t d[32];
