@@ -252,64 +252,69 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     tc::fence_after_sync();
 
     // ---- L (fp32): row t = 16 warp + l sits in lane 32 warp + l (M = 64 layout) --------
+    // Lanes 16-31 of a warp hold no row, so each row is split between lane l (columns
+    // 0-31) and lane l + 16 (columns 32-63, passed over by shuffles), 16 columns at a time.
     {
-      const int t = 16 * warp + (lane & 15);  // lanes 16-31 hold no row of the M = 64 layout
+      const int hf = lane >> 4;                 // which 32-column half this lane takes
+      const int t = 16 * warp + (lane & 15);    // its row
       const bool live = t < clen;
       const bool fast = s_fast != 0;
       const bool norm = p.qk_l2norm != 0;
       const float rt = norm ? s_rk[t] : 1.f;
       const float bt = live ? s_beta[t] * rt : 0.f, be = bt * s_E[t], gt = s_gc[t];
 #pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {  // 32 columns at a time
-        uint32_t d[32];
-        tc::tmem_ld32(tmem + ((warp * 32u) << 16) + hf * 32, d);
+      for (int cc = 0; cc < 2; ++cc) {
+        float da[16], db[16];
+        tc::tmem_ld16(tmem + ((warp * 32u) << 16) + cc * 16, da);
+        tc::tmem_ld16(tmem + ((warp * 32u) << 16) + 32 + cc * 16, db);
         tc::tmem_ld_wait();
-        if (lane >= 16) continue;
-        float l[32];
+        const int j0 = hf * 32 + cc * 16;
+        float l[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float x = __shfl_sync(0xffffffffu, db[e], lane & 15);
+          l[e] = hf ? x : da[e];
+        }
         if (fast) {
 #pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 f4 = *reinterpret_cast<const float4*>(s_F + hf * 32 + 4 * e4);
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const float4 f4 = *reinterpret_cast<const float4*>(s_F + j0 + 4 * e4);
             const float fv[4] = {f4.x, f4.y, f4.z, f4.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const int e = 4 * e4 + q, j = hf * 32 + e;
-              l[e] = j < t ? be * fv[q] * __uint_as_float(d[e]) : 0.f;
+              const int e = 4 * e4 + q;
+              l[e] = j0 + e < t ? be * fv[q] * l[e] : 0.f;
             }
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = hf * 32 + e;
-            l[e] = j < t ? bt * (norm ? s_rk[j] : 1.f) * __expf(gt - s_gc[j]) * __uint_as_float(d[e]) : 0.f;
+          for (int e = 0; e < 16; ++e) {
+            const int j = j0 + e;
+            l[e] = j < t ? bt * (norm ? s_rk[j] : 1.f) * __expf(gt - s_gc[j]) * l[e] : 0.f;
           }
         }
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4)
-          *reinterpret_cast<float4*>(lf + lf_idx(t, hf * 32 + j4 * 4)) =
+        for (int j4 = 0; j4 < 4; ++j4)
+          *reinterpret_cast<float4*>(lf + lf_idx(t, j0 + j4 * 4)) =
               make_float4(l[4 * j4], l[4 * j4 + 1], l[4 * j4 + 2], l[4 * j4 + 3]);
         // rows 32-63, columns 0-31: the A tile of the final merge (bf16 hi, lo)
         if (hf == 0 && t >= 32) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q2 = 0; q2 < 2; ++q2) {
             uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) split_bf162(l[8 * q + 2 * e], l[8 * q + 2 * e + 1], hi[e], lo[e]);
-            const uint32_t o = tc::sw128(t, q * 16);
+            for (int e = 0; e < 4; ++e) split_bf162(l[8 * q2 + 2 * e], l[8 * q2 + 2 * e + 1], hi[e], lo[e]);
+            const uint32_t o = tc::sw128(t, (2 * cc + q2) * 16);
             *reinterpret_cast<uint4*>(sm + k_off + P::S_AL - 4096 + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
             *reinterpret_cast<uint4*>(sm + k_off + P::S_AL + 4096 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
         }
-        // this row's part of its diagonal 16 x 16 block (block `warp`), transposed
-        if ((warp >> 1) == hf) {
-          float* dst = lt + warp * 256 + lane;
-          if (warp & 1) {
+        // this row's part of its diagonal 16 x 16 block (block `warp`, columns 16 warp ..),
+        // transposed
+        if (j0 == 16 * warp) {
+          float* dst = lt + warp * 256 + (lane & 15);
 #pragma unroll
-            for (int m = 0; m < 16; ++m) dst[m * 16] = l[16 + m];
-          } else {
-#pragma unroll
-            for (int m = 0; m < 16; ++m) dst[m * 16] = l[m];
-          }
+          for (int m = 0; m < 16; ++m) dst[m * 16] = l[m];
         }
       }
     }
@@ -317,15 +322,16 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     __syncthreads();
 
     // ---- T = (I + L)^{-1} in fp32, in place over L ---------------------------------------
-    // (a) the four diagonal 16 x 16 blocks: one column per thread (lanes 0-15 of
-    //     warp w invert block w), right-looking substitution; column m of a block
-    //     comes from its transposed copy as broadcast loads.
-    if (lane < 16) {
-      const int r0 = 16 * warp;
-      const float* ltb = lt + warp * 256;
+    // (a) the four diagonal 16 x 16 blocks: one column per thread (half-warp h of
+    //     warp w < 2 inverts block w + 2h), right-looking substitution; column m of a
+    //     block comes from its transposed copy as broadcast loads.
+    if (warp < 2) {
+      const int blk = warp + 2 * (lane >> 4), col = lane & 15;
+      const int r0 = 16 * blk;
+      const float* ltb = lt + blk * 256;
       float xv[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) xv[i] = (i == lane) ? 1.f : 0.f;
+      for (int i = 0; i < 16; ++i) xv[i] = (i == col) ? 1.f : 0.f;
 #pragma unroll
       for (int m = 0; m < 15; ++m) {
         float lc[16];
@@ -342,7 +348,7 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
         for (int i = m + 1; i < 16; ++i) xv[i] = fmaf(-lc[i], xm, xv[i]);
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) lf[lf_idx(r0 + i, r0 + lane)] = xv[i];
+      for (int i = 0; i < 16; ++i) lf[lf_idx(r0 + i, r0 + col)] = xv[i];
     }
     __syncthreads();
     // (b) the 16 x 16 blocks (1,0) and (3,2) of T: X = L_{i,i-1} T_{i-1,i-1}, then
