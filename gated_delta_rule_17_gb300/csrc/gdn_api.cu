@@ -76,7 +76,10 @@ int device_info(DeviceInfo** out) {
     if (major != 10 || minor != 3)
       return fail(GDN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    e = cudaFuncSetAttribute(gdn::gdn_prefill_kernel<>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gdn::gdn_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gdn::Plan::DYN_SMEM);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    e = cudaFuncSetAttribute(gdn::gdn_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gdn::Plan::DYN_SMEM);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     e = cudaFuncSetAttribute(gdn::gdn_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gdn::WyPlan::DYN_SMEM);
@@ -117,41 +120,40 @@ __global__ void gdn_schedule_kernel(const int32_t* cu, int B, int T, int32_t* or
 // S_end = M S_start + N (the spine recurrence of ssm_gdn_a3.rs, `gdn_prefill_fla`
 // doc comment, stage 2, is linear in S), so each sequence is cut into G segments
 // of L chunks:
-//   phase 1: segment 0 runs from the carried-in state (with its output rows), and
-//            for each middle segment g = 1 .. G-2 the spine runs twice without output
-//            rows: from S = I with v = 0 (giving M_g) and from S = 0 (giving N_g);
-//   combine: X_{g+1} = M_g X_g + N_g in fp32, g = 1 .. G-2 (X_1 = segment 0's end
+//   phase 1: for every segment g = 0 .. G-2 the output-free spine kernel runs twice,
+//            from S = I with v = 0 (giving M_g) and from S = 0 (giving N_g);
+//   combine: X_{g+1} = M_g X_g + N_g in fp32, g = 0 .. G-2 (X_0 = the carried-in
 //            state, X_{G-1} lands in the caller's state);
-//   phase 2: segments 1 .. G-1 run from X_g with their output rows.
-// Phase 1 takes chains * (2G - 3) CTAs, so G is the largest count with that within
+//   phase 2: every segment runs from X_g with its output rows.
+// Phase 1 takes chains * 2 (G - 1) CTAs, so G is the largest count with that within
 // the SM count, at least kSegMinChunks chunks per segment and at most kSegMaxCount.
 constexpr int kSegMinChunks = 8;
 constexpr int kSegMaxCount = 8;
 constexpr int64_t kStateFloats = static_cast<int64_t>(gdn::kDim) * gdn::kDim;
 
 struct SegPlan {
-  int G = 0, L = 0;  // G >= 3 segments of L chunks (the last may be shorter); G = 0: serial
+  int G = 0, L = 0;  // G >= 2 segments of L chunks (the last may be shorter); G = 0: serial
 };
 
 SegPlan seg_plan(int B, int T, int nv, int sms) {
   SegPlan sp;
   const int64_t chains = static_cast<int64_t>(B) * nv;
   const int nchunks = static_cast<int>((static_cast<int64_t>(T) + gdn::kChunk - 1) / gdn::kChunk);
-  if (chains <= 0 || chains * 3 > sms) return sp;
-  int G = static_cast<int>((sms / chains + 3) / 2);
+  if (chains <= 0 || chains * 2 > sms) return sp;
+  int G = static_cast<int>(sms / (2 * chains) + 1);
   if (G > nchunks / kSegMinChunks) G = nchunks / kSegMinChunks;
   if (G > kSegMaxCount) G = kSegMaxCount;
-  if (G < 3) return sp;
+  if (G < 2) return sp;
   const int L = (nchunks + G - 1) / G;
   G = (nchunks + L - 1) / L;
-  if (G < 3) return sp;
+  if (G < 2) return sp;
   sp.G = G;
   sp.L = L;
   return sp;
 }
 
 // Workspace of the segment schedule: two segment tables (4 int32 per entry), two
-// state-pointer tables, then the X_1..X_{G-2}, M_1..M_{G-2} and N_1..N_{G-2} states.
+// state-pointer tables, then the X_0..X_{G-2}, M_0..M_{G-2} and N_0..N_{G-2} states.
 struct SegLayout {
   size_t tab1 = 0, tab2 = 0, ptr1 = 0, ptr2 = 0, bufs = 0, total = 0;
   int n1 = 0, n2 = 0;
@@ -161,15 +163,15 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 SegLayout seg_layout(const SegPlan& sp, int B, int nv) {
   SegLayout l;
-  if (sp.G < 3) return l;
-  l.n1 = B * (2 * sp.G - 3);
-  l.n2 = B * (sp.G - 1);
+  if (sp.G < 2) return l;
+  l.n1 = B * 2 * (sp.G - 1);
+  l.n2 = B * sp.G;
   l.tab1 = 0;
   l.tab2 = align256(l.tab1 + 16 * static_cast<size_t>(l.n1));
   l.ptr1 = align256(l.tab2 + 16 * static_cast<size_t>(l.n2));
   l.ptr2 = align256(l.ptr1 + 8 * static_cast<size_t>(l.n1));
   l.bufs = align256(l.ptr2 + 8 * static_cast<size_t>(l.n2));
-  l.total = l.bufs + 3 * static_cast<size_t>(sp.G - 2) * B * nv * kStateFloats * sizeof(float);
+  l.total = l.bufs + 3 * static_cast<size_t>(sp.G - 1) * B * nv * kStateFloats * sizeof(float);
   return l;
 }
 
@@ -190,9 +192,9 @@ struct SegArgs {
   int32_t* tab2;
   float** ptr1;
   float** ptr2;
-  float* X;  // [G-2][B][nv][128][128]: the states entering segments 1 .. G-2
-  float* M;  // [G-2][B][nv][128][128]
-  float* N;  // [G-2][B][nv][128][128]
+  float* X;  // [G-1][B][nv][128][128]: the states entering segments 0 .. G-2
+  float* M;  // [G-1][B][nv][128][128]
+  float* N;  // [G-1][B][nv][128][128]
   void* state;  // the caller's state (contiguous, or a table of B pointers)
   int state_is_table;
 };
@@ -203,39 +205,31 @@ __device__ __forceinline__ float* user_state(const SegArgs& a, int b) {
 }
 
 // Builds both segment tables and pointer tables, sets M = I and N = 0, and copies the
-// carried-in state into X_1. Grid-stride over the state buffers.
+// carried-in state into X_0. Grid-stride over the state buffers.
 __global__ void gdn_segment_setup_kernel(const SegArgs a) {
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  const int per1 = 2 * a.G - 3, per2 = a.G - 1;
+  const int per1 = 2 * (a.G - 1), per2 = a.G;
   const int64_t seg_rows = static_cast<int64_t>(a.L) * gdn::kChunk;
   const int64_t head = static_cast<int64_t>(a.nv) * kStateFloats;  // floats per (b) state
   auto seg_len = [&](int g) -> int {
     const int64_t r = static_cast<int64_t>(a.T) - g * seg_rows;
     return static_cast<int>(r < seg_rows ? r : seg_rows);
   };
-  auto buf = [&](float* base, int g, int b) { return base + (static_cast<int64_t>(g - 1) * a.B + b) * head; };
+  auto buf = [&](float* base, int g, int b) { return base + (static_cast<int64_t>(g) * a.B + b) * head; };
   if (tid < static_cast<int64_t>(a.B) * per1) {
     const int b = static_cast<int>(tid / per1), j = static_cast<int>(tid % per1);
-    int g = 0, mode = 0;
-    float* st = nullptr;
-    if (j == 0) {
-      st = buf(a.X, 1, b);
-    } else {
-      g = 1 + (j - 1) / 2;
-      const bool is_m = ((j - 1) & 1) == 0;
-      mode = gdn::kSegNoOutput | (is_m ? gdn::kSegZeroValues : 0);
-      st = buf(is_m ? a.M : a.N, g, b);
-    }
+    const int g = j >> 1;
+    const bool is_m = (j & 1) == 0;
     int32_t* e = a.tab1 + 4 * tid;
     e[0] = static_cast<int32_t>(static_cast<int64_t>(b) * a.T + g * seg_rows);
     e[1] = seg_len(g);
-    e[2] = mode;
+    e[2] = gdn::kSegNoOutput | (is_m ? gdn::kSegZeroValues : 0);
     e[3] = 0;
-    a.ptr1[tid] = st;
+    a.ptr1[tid] = buf(is_m ? a.M : a.N, g, b);
   }
   if (tid < static_cast<int64_t>(a.B) * per2) {
-    const int b = static_cast<int>(tid / per2), g = 1 + static_cast<int>(tid % per2);
+    const int b = static_cast<int>(tid / per2), g = static_cast<int>(tid % per2);
     int32_t* e = a.tab2 + 4 * tid;
     e[0] = static_cast<int32_t>(static_cast<int64_t>(b) * a.T + g * seg_rows);
     e[1] = seg_len(g);
@@ -243,7 +237,7 @@ __global__ void gdn_segment_setup_kernel(const SegArgs a) {
     e[3] = 0;
     a.ptr2[tid] = g < a.G - 1 ? buf(a.X, g, b) : user_state(a, b);
   }
-  const int64_t nbuf = static_cast<int64_t>(a.G - 2) * a.B * head;
+  const int64_t nbuf = static_cast<int64_t>(a.G - 1) * a.B * head;
   for (int64_t i = tid; i < nbuf; i += nthreads) {
     const int64_t w = i % kStateFloats;
     a.M[i] = (w / gdn::kDim == w % gdn::kDim) ? 1.f : 0.f;
@@ -251,12 +245,12 @@ __global__ void gdn_segment_setup_kernel(const SegArgs a) {
   }
   for (int64_t i = tid; i < static_cast<int64_t>(a.B) * head; i += nthreads) {
     const int b = static_cast<int>(i / head);
-    a.X[i] = user_state(a, b)[i % head];  // X_1 is the first block of X
+    a.X[i] = user_state(a, b)[i % head];  // X_0 is the first block of X
   }
 }
 
-// X_out = M X_in + N for every (sequence, head) of one segment step, fp32 on the CUDA
-// cores (128 x 128 x 128 per head). CTA = one 64 x 64 output tile; thread = 4 x 4.
+// X_{g+1} = M_g X_g + N_g for every (sequence, head), fp32 on the CUDA cores
+// (128 x 128 x 128 per head). CTA = one 64 x 64 output tile; thread = 4 x 4.
 constexpr int kCombineThreads = 256;
 __global__ void __launch_bounds__(kCombineThreads) gdn_segment_combine_kernel(const SegArgs a, int g) {
   __shared__ float sa[64][17];
@@ -265,7 +259,7 @@ __global__ void __launch_bounds__(kCombineThreads) gdn_segment_combine_kernel(co
   const int b = bh / a.nv, h = bh % a.nv;
   const int r0 = (tile >> 1) * 64, c0 = (tile & 1) * 64;
   const int64_t head = static_cast<int64_t>(a.nv) * kStateFloats;
-  const int64_t off = (static_cast<int64_t>(g - 1) * a.B + b) * head + static_cast<int64_t>(h) * kStateFloats;
+  const int64_t off = (static_cast<int64_t>(g) * a.B + b) * head + static_cast<int64_t>(h) * kStateFloats;
   const float* Mh = a.M + off;
   const float* Nh = a.N + off;
   const float* Xin = a.X + off;
@@ -427,7 +421,7 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   // adjacent so their shared q/k tiles meet in L2
   const SegPlan sp = cu ? SegPlan() : seg_plan(B, T, nv, d->sms);
   const SegLayout sl = seg_layout(sp, B, nv);
-  if (sp.G >= 3 && seg_ws && seg_ws_bytes >= sl.total) {
+  if (sp.G >= 2 && seg_ws && seg_ws_bytes >= sl.total) {
     // segment-parallel schedule (see seg_plan): setup, phase 1, the combine steps, phase 2
     char* w8 = static_cast<char*>(seg_ws);
     SegArgs a;
@@ -440,7 +434,7 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
     a.tab2 = reinterpret_cast<int32_t*>(w8 + sl.tab2);
     a.ptr1 = reinterpret_cast<float**>(w8 + sl.ptr1);
     a.ptr2 = reinterpret_cast<float**>(w8 + sl.ptr2);
-    const size_t blk = static_cast<size_t>(sp.G - 2) * B * nv * kStateFloats;
+    const size_t blk = static_cast<size_t>(sp.G - 1) * B * nv * kStateFloats;
     a.X = reinterpret_cast<float*>(w8 + sl.bufs);
     a.M = a.X + blk;
     a.N = a.M + blk;
@@ -456,23 +450,23 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
     ps.seg = a.tab1;
     ps.state = a.ptr1;
     ps.B = sl.n1;
-    gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(static_cast<int64_t>(sl.n1) * nv), gdn::kThreads,
-                                gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt, ps);
+    gdn::gdn_prefill_kernel<false><<<static_cast<unsigned>(static_cast<int64_t>(sl.n1) * nv), gdn::kThreads,
+                                     gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt, ps);
     ++launches;
-    for (int gs = 1; gs <= sp.G - 2; ++gs) {
+    for (int gs = 0; gs <= sp.G - 2; ++gs) {
       gdn_segment_combine_kernel<<<static_cast<unsigned>(B * nv * 4), kCombineThreads, 0, stream>>>(a, gs);
       ++launches;
     }
     ps.seg = a.tab2;
     ps.state = a.ptr2;
     ps.B = sl.n2;
-    gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(static_cast<int64_t>(sl.n2) * nv), gdn::kThreads,
-                                gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt, ps);
+    gdn::gdn_prefill_kernel<true><<<static_cast<unsigned>(static_cast<int64_t>(sl.n2) * nv), gdn::kThreads,
+                                    gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt, ps);
     ++launches;
   } else {
     const int64_t grid = static_cast<int64_t>(B) * nv;
     if (grid > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "grid of %lld CTAs too large", (long long)grid);
-    gdn::gdn_prefill_kernel<><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan::DYN_SMEM, stream>>>(
+    gdn::gdn_prefill_kernel<true><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan::DYN_SMEM, stream>>>(
         mq, mk, mv, mt, p);
     ++launches;
   }

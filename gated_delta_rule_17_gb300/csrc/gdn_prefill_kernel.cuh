@@ -148,6 +148,7 @@ __device__ __forceinline__ bool group_wait(const Ctx& x, const ChunkParams& p, u
 // (the issuer runs its MMAs). Warp 4 also scans the gates of the chunk after,
 // so every chunk starts with its gate set ready.
 // ---------------------------------------------------------------------------------
+template <bool kOut>
 __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p, int ptid) {
   using P = Plan;
   const int pw = ptid >> 5, lane = ptid & 31;
@@ -291,9 +292,9 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         }
         tc::named_barrier(kBarNorm, kProducerThreads);
       }
-      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
+      if constexpr (kOut) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
       tc::fence_after_sync();
-      if (ok) {
+      if (kOut && ok) {
         const int i = (quad - 2) * 32 + lane;  // A_ij = e^{gc_i - gc_j} q_i.k_j / sqrt(dk), j <= i
         const bool fast = x.s_fast[b] != 0;
         const float ei = x.s_E[gs + i] * kInvSqrtD;
@@ -333,7 +334,12 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 
     // ---- once the Gram MMA has read K: K -> e^gc K (fp16, in place, rows t) and --------
     //      Kd = e^{gc_last-gc} K (KD[b]); tail rows zeroed
-    ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
+    // (without outputs there is no Gram MMA: the tile only has to have landed)
+    if constexpr (kOut)
+      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
+    else
+      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_kq1 : x.mb_kq0, use, kWaitLimitNs);
+    tc::fence_after_sync();
     if (ok) {
 #pragma unroll 1
       for (int r0 = 0; r0 < 4; r0 += 2) {
@@ -360,8 +366,8 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 
     // ---- meanwhile: Q -> Q~ = e^gc Q / sqrt(dk) (fp16, rows t, tail rows zeroed), once
     //      the spine of chunk c-1 has read Q~ (and -W^T) ------------------------------------
-    if (c > 0) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
-    if (ok) {
+    if (kOut && c > 0) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
+    if (kOut && ok) {
 #pragma unroll 1
       for (int r0 = 0; r0 < 4; r0 += 2) {
         uint4 rq[2];
@@ -423,6 +429,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 // Consumer: the state spine and the output of each chunk. Thread v owns value
 // column v: tensor-memory lane v holds S^T[v][:], u^T[v][:] and O^T[v][:].
 // ---------------------------------------------------------------------------------
+template <bool kOut>
 __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p, int ctid) {
   using P = Plan;
   const int quad = ctid >> 5;
@@ -524,18 +531,20 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
         for (int e = 0; e < 16; ++e) st[e] = pack_half2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]));
         tc::tmem_st16u(lanes + P::COL_ST + q4 * 16, st);
       }
-      uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(o);
-      uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(o + 32);
-      tc::tmem_ld32(lanes + P::COL_O, o0);
-      tc::tmem_ld32(lanes + P::COL_O + 32, o1);
-      tc::tmem_ld_wait();
+      if constexpr (kOut) {
+        uint32_t (&o0)[32] = *reinterpret_cast<uint32_t(*)[32]>(o);
+        uint32_t (&o1)[32] = *reinterpret_cast<uint32_t(*)[32]>(o + 32);
+        tc::tmem_ld32(lanes + P::COL_O, o0);
+        tc::tmem_ld32(lanes + P::COL_O + 32, o1);
+        tc::tmem_ld_wait();
+      }
       tc::tmem_st_wait();
     }
     signal(x.mb_strdy);  // S^T of the next chunk is ready and O^T has been read
 
     // ---- meanwhile (the next chunk's first MMAs run): this chunk's output rows, then
     //      the decay of the next chunk --------------------------------------------------
-    if (x.store_out) {
+    if (kOut && x.store_out) {
       // O^T holds one value column per thread: for each row t, the 32 lanes of a warp
       // store 32 consecutive bf16 values, one 64-byte segment (no shared-memory staging)
       __nv_bfloat16* optr = p.out + (x.row0 + static_cast<int64_t>(c) * kChunk) * p.out_stride +
@@ -569,6 +578,7 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
 // consumer warps only convert operands and signal readiness, so no warp that
 // converts waits for an instruction queue.
 // ---------------------------------------------------------------------------------
+template <bool kOut>
 __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, const CUtensorMap* tmap_q,
                                             const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                                             const CUtensorMap* tmap_t, bool spine_side) {
@@ -643,8 +653,9 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
     for (int st = 0; st < 8; ++st) {
       const uint32_t a = x.tmem + P::COL_ST + st * 8;
       tc::mma_f16_ts(x.tmem + col_u, a, tc::desc_sw128(x.sbase + P::W16 + st * 2048, 16384, 1024), id_u, 1);
-      tc::mma_f16_ts(x.tmem + P::COL_O, a, tc::desc_sw128(x.sbase + P::QT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024),
-                     id_o, st > 0);
+      if constexpr (kOut)
+        tc::mma_f16_ts(x.tmem + P::COL_O, a,
+                       tc::desc_sw128(x.sbase + P::QT + (st >> 2) * 8192 + (st & 3) * 32, 16, 1024), id_o, st > 0);
     }
     tc::mma_commit(x.mb_c1);
   };
@@ -660,9 +671,11 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
       const uint64_t a_hi = tc::desc_sw128(x.sbase + a_off + st * 32, 16, 1024);
       const uint64_t a_lo = tc::desc_sw128(x.sbase + a_off + 8192 + st * 32, 16, 1024);
       tc::mma_f16_ts(x.tmem + P::COL_S, u_hi, tc::desc_sw128(x.sbase + kd_off + st * 2048, 8192, 1024), id_s, 1);
-      tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_hi, id_o, 1);
-      tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_lo, id_o, 1);
-      tc::mma_f16_ts(x.tmem + P::COL_O, u_lo, a_hi, id_o, 1);
+      if constexpr (kOut) {
+        tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_hi, id_o, 1);
+        tc::mma_f16_ts(x.tmem + P::COL_O, u_hi, a_lo, id_o, 1);
+        tc::mma_f16_ts(x.tmem + P::COL_O, u_lo, a_hi, id_o, 1);
+      }
     }
     tc::mma_commit(b ? x.mb_c21 : x.mb_c20);
   };
@@ -689,8 +702,11 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
   for (int c = 0; c < n; ++c) {
     const int b = c & 1;
     // Gram of c: its K/Q tile has landed and the W MMAs of c-1 have been read out
-    if ((c > 0 && !wait(x.mb_wrd, (c - 1) & 1)) || !wait(b ? x.mb_kq1 : x.mb_kq0, (c >> 1) & 1)) break;
-    gram(c);
+    // (runs without outputs need no Gram)
+    if constexpr (kOut) {
+      if ((c > 0 && !wait(x.mb_wrd, (c - 1) & 1)) || !wait(b ? x.mb_kq1 : x.mb_kq0, (c >> 1) & 1)) break;
+      gram(c);
+    }
     // U of c: V is fp16, T diag(beta) has landed, and u of c-2 has been read
     if (!wait(x.mb_vrdy, c & 1) || !wait(x.mb_t, c & 1) ||
         (c >= 2 && !wait(b ? x.mb_cu1 : x.mb_cu0, ((c - 2) >> 1) & 1)))
@@ -698,6 +714,9 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
     wy(c, true);
     // W of c: e^gc K is converted and the Gram columns have been read
     if (!wait(x.mb_krdy, c & 1)) break;
+    if constexpr (!kOut) {  // no Gram ordered this after the W epilogue of c-1
+      if (c > 0 && !wait(x.mb_wrd, (c - 1) & 1)) break;
+    }
     wy(c, false);
     tc::mma_commit(x.mb_uw);
     // refill what chunk c has consumed
@@ -710,7 +729,9 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
   }
 }
 
-template <int kUnused = 0>
+// kOut = false: runs that only carry the state (the segment schedule's state maps):
+// no Gram, A, Q~, output MMAs or output rows.
+template <bool kOut = true>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_t,
@@ -809,11 +830,11 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.tmem = s_tmem;
 
   if (warp < kConsumerWarps)
-    consumer_role(x, p, tid);
+    consumer_role<kOut>(x, p, tid);
   else if (warp < kConsumerWarps + kProducerWarps)
-    producer_role(x, p, tid - kConsumerThreads);
+    producer_role<kOut>(x, p, tid - kConsumerThreads);
   else if ((tid & 31) == 0)
-    issuer_role(x, p, &tmap_q, &tmap_k, &tmap_v, &tmap_t, warp == kConsumerWarps + kProducerWarps + 1);
+    issuer_role<kOut>(x, p, &tmap_q, &tmap_k, &tmap_v, &tmap_t, warp == kConsumerWarps + kProducerWarps + 1);
 
   tc::fence_before_sync();
   __syncthreads();

@@ -119,14 +119,14 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
  * batches: a schedule of 2B + 1 int32 (the sequence order and the chunk
  * prefix over the sequences), rounded up to 256 bytes. Dense batches: 0, or,
  * when the batch has few (sequence, head) chains for the device's SM count and
- * long sequences (at least 3 segments of 8 chunks; B * nv * 3 <= SMs), the
+ * long sequences (at least 2 segments of 8 chunks; B * nv * 2 <= SMs), the
  * segment-parallel schedule's scratch: two segment tables and pointer tables
- * (under 4 KB for small B) plus 3 (G - 2) fp32 states of nv x 128 x 128 per
+ * (under 4 KB for small B) plus 3 (G - 1) fp32 states of nv x 128 x 128 per
  * sequence, G being the segment count. The state map of a run of chunks is
  * affine in the entry state (the spine stage of ssm_gdn_a3.rs
- * `gdn_prefill_fla`), so the library computes the middle segments' maps in
- * parallel with the first segment, chains the segment entry states, and runs
- * the remaining segments in parallel. The SM count is the current device's,
+ * `gdn_prefill_fla`), so the library computes the segments' maps in
+ * parallel, chains the segment entry states, and then runs every segment in
+ * parallel. The SM count is the current device's,
  * or 152 when no device is visible. */
 size_t gdn_prefill_workspace_bytes(int B, int T, int nv, int dk, int dv, int varlen);
 

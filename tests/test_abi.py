@@ -113,12 +113,14 @@ def test_workspace_sizes(lib):
     assert lib.gdn_prefill_workspace_bytes(8, 64000, 48, 128, 128, 1) == 256
     assert lib.gdn_prefill_workspace_bytes(100, 64000, 48, 128, 128, 1) == 1024
     # dense batches with few chains and long sequences: the segment schedule's tables
-    # (4 x 256-byte-aligned regions) and 3 (G-2) per-sequence states, here G = 3 on the
+    # (4 x 256-byte-aligned regions) and 3 (G-1) per-sequence states, here G = 3 on the
     # 152 SMs assumed without a visible GPU
-    assert lib.gdn_prefill_workspace_bytes(1, 65536, 32, 128, 128, 0) == 1024 + 3 * 32 * 128 * 128 * 4
-    # too many chains, or too few chunks, for 3 segments: none
-    assert lib.gdn_prefill_workspace_bytes(2, 65536, 32, 128, 128, 0) == 0
-    assert lib.gdn_prefill_workspace_bytes(1, 64 * 23, 4, 128, 128, 0) == 0
+    assert lib.gdn_prefill_workspace_bytes(1, 65536, 32, 128, 128, 0) == 1024 + 3 * 2 * 32 * 128 * 128 * 4
+    # G = 2 (B * nv = 64 chains): 3 states per sequence
+    assert lib.gdn_prefill_workspace_bytes(2, 65536, 32, 128, 128, 0) == 1024 + 3 * 2 * 32 * 128 * 128 * 4
+    # too many chains, or too few chunks, for 2 segments: none
+    assert lib.gdn_prefill_workspace_bytes(3, 65536, 32, 128, 128, 0) == 0
+    assert lib.gdn_prefill_workspace_bytes(1, 64 * 15, 4, 128, 128, 0) == 0
 
 
 def test_ex_rejects_small_workspace(lib):
