@@ -247,7 +247,9 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     ws = None
     ws_bytes = gdn.workspace_bytes(p.B, p.T, p.nv, p.varlen)
-    if args.no_segments and not p.varlen:
+    # the profiling case mirrors the B=4 workload's single spine launch at half the
+    # sequences, so it keeps the serial schedule
+    if (args.no_segments or args.profile_case) and not p.varlen:
         ws = torch.empty(0, dtype=torch.uint8, device=dev)  # declines the segment schedule
         workload += ", serial spine (no segment workspace)"
     elif ws_bytes:  # varlen schedule, or the segment schedule of a long dense batch

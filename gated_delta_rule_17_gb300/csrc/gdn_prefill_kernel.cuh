@@ -781,7 +781,9 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   float* state = p.state_is_table ? reinterpret_cast<float* const*>(p.state)[s]
                                   : reinterpret_cast<float*>(p.state) + static_cast<int64_t>(s) * p.nv * kDim * kDim;
   x.state = state + static_cast<int64_t>(x.h) * kDim * kDim;
-  x.sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned, by pointer arithmetic on the shared array so that accesses
+  // through it stay shared-space (not generic) loads and stores
+  x.sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   x.sbase = tc::smem_u32(x.sm);
   x.s_gc = s_gc;
   x.s_eg = s_eg;

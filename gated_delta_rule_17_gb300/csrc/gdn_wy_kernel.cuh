@@ -129,7 +129,9 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
   }
   if (static_cast<int>(blockIdx.x) >= items) return;
 
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned, by pointer arithmetic on the shared array so that accesses
+  // through it stay shared-space (not generic) loads and stores
+  uint8_t* sm = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = tc::smem_u32(sm);
   float* lf = reinterpret_cast<float*>(sm + P::LF);
   const uint32_t mb_g = tc::smem_u32(&s_mb[2]);
