@@ -6,6 +6,9 @@ token-by-token fp64 recurrence lives in ``gdn_token_loop.c`` (compiled here
 with gcc + OpenMP), and an independent chunked-WY evaluation in numpy lives in
 ``chunked_wy.py``.
 
+The backward (``token_loop_backward``) is the same recurrence differentiated
+by hand, token by token in reverse, in the same C file.
+
 Parity pins: every function here is checked by ``tests/test_oracle.py``
 against closed forms (pure decay, exact overwrite with orthonormal keys,
 strong decay), exact rational brute force, dense transition-matrix products
@@ -51,6 +54,7 @@ def _lib():
             lib = ctypes.CDLL(build())
             lib.gdn_oracle_run.restype = ctypes.c_int
             lib.gdn_oracle_max_threads.restype = ctypes.c_int
+            lib.gdn_oracle_backward.restype = ctypes.c_int
             _handle = lib
     return _handle
 
@@ -106,6 +110,44 @@ def token_loop_raw(q, k, v, g, beta, h0, *, B, T, nk, nv, dk, dv,
     if rc != 0:
         raise RuntimeError("oracle rejected its arguments")
     return out, hT
+
+
+def token_loop_backward(p: Problem, dout, dST=None, threads=0):
+    """Backward of the token recurrence in fp64 (the training pass).
+
+    dout: [rows, nv, dv] (dL/do); dST: [B, nv, dk, dv] (dL/dS_T) or None.
+    Returns a dict with dq, dk [rows, nk, dk], dv [rows, nv, dv], dg, dbeta
+    [rows, nv] and dh0 [B, nv, dk, dv], all fp64 (rows outside every sequence
+    are zero).
+    """
+    rows = p.rows
+    dout = np.ascontiguousarray(dout, dtype=np.float64).reshape(rows, p.nv, p.dv)
+    dst = None if dST is None else np.ascontiguousarray(dST, dtype=np.float64)
+    q = np.ascontiguousarray(p.q)
+    k = np.ascontiguousarray(p.k)
+    v = np.ascontiguousarray(p.v)
+    g = np.ascontiguousarray(p.g)
+    beta = np.ascontiguousarray(p.beta)
+    assert q.dtype == k.dtype == v.dtype and g.dtype == beta.dtype
+    res = {"dq": np.zeros((rows, p.nk, p.dk)), "dk": np.zeros((rows, p.nk, p.dk)),
+           "dv": np.zeros((rows, p.nv, p.dv)), "dg": np.zeros((rows, p.nv)),
+           "dbeta": np.zeros((rows, p.nv)), "dh0": np.zeros((p.B, p.nv, p.dk, p.dv))}
+    h0 = None if p.h0 is None else np.ascontiguousarray(p.h0)
+    cu = None if p.cu_seqlens is None else np.ascontiguousarray(p.cu_seqlens, dtype=np.int32)
+    rc = _lib().gdn_oracle_backward(
+        _ptr(q), _ptr(k), _ptr(v), ctypes.c_int(_dtype_code(q)),
+        _ptr(g), _ptr(beta), ctypes.c_int(_dtype_code(g)),
+        _ptr(h0), ctypes.c_int(_dtype_code(h0) if h0 is not None else DT_F32),
+        _ptr(dout), _ptr(dst),
+        _ptr(res["dq"]), _ptr(res["dk"]), _ptr(res["dv"]), _ptr(res["dg"]), _ptr(res["dbeta"]), _ptr(res["dh0"]),
+        ctypes.c_int(p.B), ctypes.c_int(p.T), ctypes.c_int(p.nk), ctypes.c_int(p.nv),
+        ctypes.c_int(p.dk), ctypes.c_int(p.dv),
+        ctypes.c_int64(q.shape[1]), ctypes.c_int64(k.shape[1]), ctypes.c_int64(v.shape[1]),
+        ctypes.c_int64(g.shape[1]), ctypes.c_int64(beta.shape[1]),
+        _ptr(cu), ctypes.c_int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle rejected its arguments")
+    return res
 
 
 L2_EPS = 1e-6
