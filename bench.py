@@ -427,6 +427,75 @@ def run_decode(args, world, rank, local):
             "gpu_launches": args.steps, "clocks": clk.summary()}), flush=True)
 
 
+def run_backward(args, world, rank, local):
+    """The backward of the prefill (dL/dq, dk, dv, dg, dbeta, dS_0 from dL/do and
+    dL/dS_T) on a workload of --config, inputs resident in HBM."""
+    import torch
+
+    import gated_delta_rule_17_gb300 as gdn
+    from gated_delta_rule_17_gb300 import build as gbuild
+
+    gbuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    p = gdn_synth.config_problem(args.config)
+    from tests.gpu_helpers import DeviceProblem
+
+    dp = DeviceProblem(p, device=dev)
+    rng = torch.Generator(device=dev).manual_seed(7)
+    rows = p.rows
+    f32 = dict(dtype=torch.float32, device=dev)
+    dout = torch.randn((rows, p.nv * p.dv), generator=rng, **f32)
+    dst = torch.randn((p.B, p.nv, p.dk, p.dv), generator=rng, **f32)
+    dq = torch.empty((rows, p.nk * p.dk), **f32)
+    dk = torch.empty_like(dq)
+    dv = torch.empty((rows, p.nv * p.dv), **f32)
+    dg = torch.empty((rows, p.nv), **f32)
+    dbeta = torch.empty_like(dg)
+    dh0 = torch.empty((p.B, p.nv, p.dk, p.dv), **f32)
+    ws = torch.empty(gdn.backward_workspace_bytes(p.B, p.T, p.nv, p.varlen), dtype=torch.uint8, device=dev)
+    h0 = dp.state  # the initial state (no forward runs here)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gdn.backward(dp.q, dp.k, dp.v, dp.g, dp.beta, h0, dout, dq, dk, dv, dg, dbeta, nk=p.nk, nv=p.nv,
+                     B=p.B, T=p.T, cu_seqlens=dp.cu, dST=dst, dh0=dh0, state_is_table=dp.table, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    gdn.check()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    gdn.check()
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    hbm_peak, _, peak_src = measured_peaks()
+    tokens = p.tokens
+    # each input read once and each gradient written once, the states in and out
+    io = tokens * (2 * p.nk * p.dk * 2 + p.nv * p.dv * 2 + p.nv * 8 + p.nv * p.dv * 4
+                   + 2 * p.nk * p.dk * 4 + p.nv * p.dv * 4 + p.nv * 8) + 3 * p.B * p.nv * p.dk * p.dv * 4
+    achieved = io / (ms / 1e3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "GDN prefill backward tokens/s (dq, dk, dv, dg, dbeta, dS_0), 1xGB300",
+            "value": world * tokens / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 inputs, fp32 gradients, state and arithmetic", "data": "synthetic",
+            "config": {"workload": gdn_synth.CONFIG_NAMES[args.config], "parallelism": "1 GPU",
+                       "l2": "no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "kernel": "gdn_backward_kernel",
+                         "algorithmic_bytes": io, "peak_source": peak_src},
+            "gpu_launches": 2 * args.steps, "clocks": clk.summary()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -436,7 +505,7 @@ def main():
     ap.add_argument("--config", type=int, default=2, help="workload index (2 = B=4 T=8192 nv=32)")
     ap.add_argument("--ref-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="prefill", choices=["prefill", "decode"],
+    ap.add_argument("--op", default="prefill", choices=["prefill", "decode", "backward"],
                     help="prefill (the headline) or the single-token decode step")
     ap.add_argument("--no-segments", action="store_true",
                     help="dense batches: run the serial spine even where the segment schedule applies")
@@ -453,6 +522,8 @@ def main():
         run_reference(args, world, rank)
     elif args.op == "decode":
         run_decode(args, world, rank, local)
+    elif args.op == "backward":
+        run_backward(args, world, rank, local)
     else:
         run_gpu(args, world, rank, local)
     if world > 1:

@@ -12,6 +12,7 @@ import os
 import threading
 
 __all__ = ["prefill", "prefill_noalloc", "NOALLOC_MAX_SEQS", "workspace_bytes", "check", "last_launch_count",
+           "backward", "backward_workspace_bytes",
            "set_timing_events", "decode", "lib_path", "load", "GdnError",
            "Strides", "GDN_OK", "GDN_ERR_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
            "GDN_ERR_DEVICE_STATUS", "GDN_ERR_TIMEOUT"]
@@ -68,6 +69,10 @@ def load():
             lib.gdn_prefill_noalloc.restype = i
             lib.gdn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(Strides), vp]
             lib.gdn_decode.restype = i
+            lib.gdn_prefill_backward_workspace_bytes.argtypes = [i, i, i, i, i, i]
+            lib.gdn_prefill_backward_workspace_bytes.restype = sz
+            lib.gdn_prefill_backward.argtypes = [vp] * 14 + [i] * 6 + [ctypes.POINTER(Strides), vp, vp, sz, vp]
+            lib.gdn_prefill_backward.restype = i
             lib.gdn_set_timing_events.argtypes = [vp, vp, vp]
             lib.gdn_set_timing_events.restype = None
             del i64
@@ -212,6 +217,59 @@ def decode(q, k, v, g, beta, state, out, *, nk: int, nv: int, state_is_table: bo
         stream = stream.cuda_stream
     rc = lib.gdn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(), state.data_ptr(),
                         out.data_ptr(), q.shape[0], nk, nv, dk, dv, ctypes.byref(st), stream)
+    if rc != GDN_OK:
+        _raise(rc)
+
+
+def backward_workspace_bytes(B, T, nv, varlen, dk=128, dv=128) -> int:
+    return int(load().gdn_prefill_backward_workspace_bytes(B, T, nv, dk, dv, 1 if varlen else 0))
+
+
+def backward(q, k, v, g, beta, h0, dout, dq, dk, dv, dg, dbeta, *, nk: int, nv: int, dST=None, dh0=None,
+             B: int | None = None, T: int | None = None, cu_seqlens=None, state_is_table: bool = False,
+             workspace=None, stream=None, dk_dim: int = 128, dv_dim: int = 128) -> None:
+    """Enqueue the backward of ``prefill`` (``gdn_prefill_backward``).
+
+    q, k, v, g, beta, cu_seqlens, state_is_table: as ``prefill``; ``h0`` is the initial
+    state the forward started from. ``dout`` fp32 [rows, nv*dv] (dL/do), ``dST`` fp32
+    [B, nv, dk, dv] or None. Outputs (fp32): dq, dk [rows, nk*dk], dv [rows, nv*dv],
+    dg, dbeta [rows, nv], dh0 [B, nv, dk, dv] or None.
+    """
+    import torch
+
+    lib = load()
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("g", g, torch.float32), ("beta", beta, torch.float32), ("dout", dout, torch.float32)):
+        if t.dtype != dt:
+            raise GdnError(GDN_ERR_ARG, f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_cuda:
+            raise GdnError(GDN_ERR_ARG, f"{name} must be a CUDA tensor")
+    for name, t in (("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg), ("dbeta", dbeta),
+                    ("dST", dST), ("dh0", dh0)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda):
+            raise GdnError(GDN_ERR_ARG, f"{name} must be a contiguous fp32 CUDA tensor")
+    rows = q.shape[0]
+    if cu_seqlens is not None:
+        B = cu_seqlens.numel() - 1
+        T = rows
+    elif B is None or T is None:
+        raise GdnError(GDN_ERR_ARG, "dense batches need B and T")
+    st = Strides(_row_stride(q, "q", nk * dk_dim), _row_stride(k, "k", nk * dk_dim), _row_stride(v, "v", nv * dv_dim),
+                 _row_stride(g, "g", nv), _row_stride(beta, "beta", nv), nv * dv_dim,
+                 1 if state_is_table else 0, 0)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+
+    def ptr(t):
+        return None if t is None else t.data_ptr()
+
+    ws_ptr, ws_size = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    rc = lib.gdn_prefill_backward(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(), h0.data_ptr(),
+                                  dout.data_ptr(), ptr(dST), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dg.data_ptr(),
+                                  dbeta.data_ptr(), ptr(dh0), B, T, nk, nv, dk_dim, dv_dim, ctypes.byref(st),
+                                  ptr(cu_seqlens), ws_ptr, ws_size, stream)
     if rc != GDN_OK:
         _raise(rc)
 

@@ -20,6 +20,7 @@
 #include "gdn_prefill_kernel.cuh"
 #include "gdn_wy_kernel.cuh"
 #include "gdn_decode_kernel.cuh"
+#include "gdn_backward_kernel.cuh"
 
 namespace {
 
@@ -514,6 +515,28 @@ int noalloc_scratch(int32_t** out) {
   return GDN_OK;
 }
 
+// ---- backward -------------------------------------------------------------------
+// Scratch of gdn_prefill_backward: the per-v-head dq and dk (2 x rows x nv x 128
+// fp32), the states at 64-token boundaries ((rows/64 + B + 1) x nv states) and one
+// 65-state block buffer per persistent CTA.
+struct BwdLayout {
+  size_t part = 0, ckpt = 0, blocks = 0, total = 0;
+  int grid = 0;
+};
+
+BwdLayout bwd_layout(int B, int T, int nv, int varlen, int sms) {
+  BwdLayout l;
+  const int64_t rows = varlen ? static_cast<int64_t>(T) : static_cast<int64_t>(B) * T;
+  const int64_t items = static_cast<int64_t>(B) * nv;
+  l.grid = static_cast<int>(items < sms ? items : sms);
+  const size_t state = static_cast<size_t>(kStateFloats) * sizeof(float);
+  l.part = 0;
+  l.ckpt = align256(2 * static_cast<size_t>(rows) * nv * gdn::kDim * sizeof(float));
+  l.blocks = align256(l.ckpt + (static_cast<size_t>(rows) / gdn::kBwdBlock + B + 1) * nv * state);
+  l.total = l.blocks + static_cast<size_t>(l.grid) * (gdn::kBwdBlock + 1) * state;
+  return l;
+}
+
 }  // namespace
 
 extern "C" {
@@ -647,6 +670,97 @@ int gdn_decode(const void* q, const void* k, const void* v, const float* g, cons
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
   g_launches = 1;
   return GDN_OK;
+}
+
+size_t gdn_prefill_backward_workspace_bytes(int B, int T, int nv, int dk, int dv, int varlen) {
+  (void)dk;
+  (void)dv;
+  if (B <= 0 || T <= 0 || nv <= 0) return 0;
+  return bwd_layout(B, T, nv, varlen, plan_sms()).total;
+}
+
+int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const void* h0, const float* dout, const float* dST, float* dq, float* dk, float* dv,
+                         float* dg, float* dbeta, float* dh0, int B, int T, int nk, int nv, int dk_dim, int dv_dim,
+                         const gdn_strides_t* strides, const int32_t* cu_seqlens, void* workspace,
+                         size_t workspace_bytes_, void* stream) {
+  g_err[0] = 0;
+  g_launches = 0;
+  Resolved r;
+  // dout stands in for `out` in the shared checks (contiguous [rows][nv][128] rows)
+  gdn_strides_t st{};
+  if (strides) st = *strides;
+  else {
+    st.q = static_cast<int64_t>(nk) * dk_dim;
+    st.k = st.q;
+    st.v = static_cast<int64_t>(nv) * dv_dim;
+    st.g = nv;
+    st.beta = nv;
+  }
+  st.out = static_cast<int64_t>(nv) * dv_dim;
+  if (int rc = validate(q, k, v, g, beta, const_cast<void*>(h0), const_cast<float*>(dout), B, T, nk, nv, dk_dim, dv_dim, &st, &r))
+    return rc;
+  if (r.l2norm) return fail(GDN_ERR_UNSUPPORTED, "the backward takes already normalised q and k (qk_l2norm = 0)");
+  if (B == 0 || T == 0) return GDN_OK;
+  if (!dq || !dk || !dv || !dg || !dbeta) return fail(GDN_ERR_ARG, "a gradient output pointer is NULL");
+  if (!aligned16(dv) || (dST && !aligned16(dST)) || (dh0 && !aligned16(dh0)))
+    return fail(GDN_ERR_ARG, "dv, dS_T and dh0 must be 16-byte aligned");
+  DeviceInfo* d = nullptr;
+  if (int rc = device_info(&d)) return rc;
+  const int64_t rows = cu_seqlens ? static_cast<int64_t>(T) : static_cast<int64_t>(B) * T;
+  const BwdLayout l = bwd_layout(B, T, nv, cu_seqlens != nullptr, d->sms);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  if (ws) {
+    if (workspace_bytes_ < l.total)
+      return fail(GDN_ERR_ARG, "workspace of %zu bytes is smaller than the %zu required", workspace_bytes_, l.total);
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(GDN_ERR_ARG, "workspace must be 256-byte aligned");
+  } else {
+    cudaError_t e = cudaMallocAsync(&ws, l.total, s);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaMallocAsync(%zu): %s", l.total, cudaGetErrorString(e));
+  }
+  char* w8 = static_cast<char*>(ws);
+  gdn::BwdParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.g = g;
+  p.beta = beta;
+  p.h0 = h0;
+  p.dout = dout;
+  p.dst = dST;
+  p.dq_part = reinterpret_cast<float*>(w8 + l.part);
+  p.dk_part = p.dq_part + rows * nv * gdn::kDim;
+  p.dv = dv;
+  p.dg = dg;
+  p.dbeta = dbeta;
+  p.dh0 = dh0;
+  p.ckpt = reinterpret_cast<float*>(w8 + l.ckpt);
+  p.blocks = reinterpret_cast<float*>(w8 + l.blocks);
+  p.cu_seqlens = cu_seqlens;
+  p.status = d->status;
+  p.q_stride = r.q;
+  p.k_stride = r.k;
+  p.v_stride = r.v;
+  p.g_stride = r.g;
+  p.beta_stride = r.beta;
+  p.B = B;
+  p.T = T;
+  p.nk = nk;
+  p.nv = nv;
+  p.state_is_table = r.table;
+  gdn::gdn_backward_kernel<<<static_cast<unsigned>(l.grid), gdn::kBwdThreads, 0, s>>>(p);
+  gdn::gdn_backward_reduce_kernel<<<static_cast<unsigned>(d->sms * 4), 256, 0, s>>>(p.dq_part, p.dk_part, dq, dk,
+                                                                                    rows, nk, nv);
+  int rc = GDN_OK;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) rc = fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  if (!workspace) {
+    e = cudaFreeAsync(ws, s);
+    if (e != cudaSuccess && rc == GDN_OK) rc = fail(GDN_ERR_CUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
+  }
+  if (rc == GDN_OK) g_launches = 2;
+  return rc;
 }
 
 const char* gdn_last_error(void) { return g_err; }

@@ -182,6 +182,33 @@ int gdn_decode(const void* q, const void* k, const void* v, const float* g, cons
  * switches the hook off. The events must outlive the calls that record them. */
 void gdn_set_timing_events(void* before_wy, void* before_spine, void* after_spine);
 
+/* Backward of the prefill (the training pass): gradients of a loss L with
+ * respect to every input of the recurrence S_t = e^{g_t}(I - beta_t k_t k_t^T)
+ * S_{t-1} + beta_t k_t v_t^T, o_t = S_t^T q_t / sqrt(dk) (the forward of
+ * ssm_gdn_a3.rs `gdn_prefill_fla`), given dL/do and dL/dS_T. Computed token by
+ * token in reverse in fp32 on the CUDA cores; the states are recomputed from the
+ * inputs and h0 (stored every 64 tokens), so the forward's outputs are not needed.
+ *   q, k, v, g, beta, strides, cu_seqlens, B, T, nk, nv, dk, dv: as gdn_prefill
+ *             (qk_l2norm must be 0: pass the normalised q and k).
+ *   h0     : the INITIAL state (gdn_prefill updates its state in place, so keep a
+ *            copy), fp32 [B][nv][128][128] or a table of B pointers (state_is_table).
+ *   dout   : fp32 [rows][nv][128], dL/do.
+ *   dST    : fp32 [B][nv][128][128] (dL/dS_T) or NULL for zero.
+ *   dq, dk : fp32 [rows][nk][128] (summed over the value heads of each key head).
+ *   dv     : fp32 [rows][nv][128].      dg, dbeta : fp32 [rows][nv].
+ *   dh0    : fp32 [B][nv][128][128] (dL/dS_0) or NULL.
+ *   (A well-formed cu_seqlens covers every row; with a malformed one the rows
+ *   of the rejected sequences hold unspecified values and the status word says so.)
+ *   workspace : device scratch of gdn_prefill_backward_workspace_bytes(...) bytes,
+ *            256-byte aligned, or NULL to allocate it stream-ordered.
+ * dv, dST and dh0 must be 16-byte aligned. Returns GDN_OK or an error code. */
+size_t gdn_prefill_backward_workspace_bytes(int B, int T, int nv, int dk, int dv, int varlen);
+int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const void* h0, const float* dout, const float* dST, float* dq, float* dk, float* dv,
+                         float* dg, float* dbeta, float* dh0, int B, int T, int nk, int nv, int dk_dim, int dv_dim,
+                         const gdn_strides_t* strides, const int32_t* cu_seqlens, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream`, then read and clear the current device's status word
  * that kernels set on malformed cu_seqlens (GDN_ERR_DEVICE_STATUS) or on an
  * expired bounded wait (GDN_ERR_TIMEOUT). The word is shared by all calls on
