@@ -30,7 +30,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("gdn_prefill", "gdn_prefill_ex", "gdn_prefill_workspace_bytes", "gdn_prefill_check",
-              "gdn_last_error", "gdn_last_launch_count", "gdn_prefill_noalloc", "gdn_set_timing_events"):
+              "gdn_last_error", "gdn_last_launch_count", "gdn_prefill_noalloc", "gdn_set_timing_events",
+              "gdn_decode", "gdn_prefill_backward", "gdn_prefill_backward_workspace_bytes"):
         assert n in names
 
 
@@ -42,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_no_cpu_fallback_symbols(lib):
     # the library is CUDA-only: its product path links nothing from oracle/
     data = open(lib._name, "rb").read()
-    assert b"gdn_oracle_run" not in data
+    assert b"gdn_oracle_run" not in data and b"gdn_oracle_backward" not in data
 
 
 def _call(lib, B=1, T=64, nk=1, nv=1, dk=128, dv=128, strides=None, ptr=16, cu=None):
@@ -139,3 +140,15 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gdn, "_lib", None)
     with pytest.raises(gdn.GdnError):
         gdn.load()
+
+
+def test_backward_workspace_sizes(lib):
+    # per-v-head dq/dk (2 x rows x nv x 128 fp32), a state per 64 rows per head (plus
+    # B + 1), and a 65-state slot per persistent CTA (min(B * nv, SMs); 152 SMs without
+    # a visible GPU)
+    state = 128 * 128 * 4
+    B, T, nv = 1, 4096, 32
+    part = 2 * B * T * nv * 128 * 4
+    ckpt = (B * T // 64 + B + 1) * nv * state
+    assert lib.gdn_prefill_backward_workspace_bytes(B, T, nv, 128, 128, 0) == part + ckpt + 32 * 65 * state
+    assert lib.gdn_prefill_backward_workspace_bytes(0, T, nv, 128, 128, 0) == 0
