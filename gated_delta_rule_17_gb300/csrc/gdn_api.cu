@@ -516,24 +516,40 @@ int noalloc_scratch(int32_t** out) {
 }
 
 // ---- backward -------------------------------------------------------------------
-// Scratch of gdn_prefill_backward: the per-v-head dq and dk (2 x rows x nv x 128
-// fp32), the states at 64-token boundaries ((rows/64 + B + 1) x nv states) and one
-// 65-state block buffer per persistent CTA.
+// Column split of the backward: each (sequence, v-head) item runs on nsplit CTAs of
+// 128 / nsplit columns, the most that the SMs hold at once (4, then 2, then 1).
+// Scratch: the split parts of dq, dk (2 x rows x nv x nsplit x 128 fp32) and of dg,
+// dbeta (2 x rows x nv x nsplit), the states at 64-token boundaries ((rows/64 + B + 1)
+// x nv states) and one 65-block slot of 128 x 128/nsplit floats per persistent CTA.
 struct BwdLayout {
-  size_t part = 0, ckpt = 0, blocks = 0, total = 0;
-  int grid = 0;
+  size_t dq = 0, dk = 0, dg = 0, dbeta = 0, ckpt = 0, blocks = 0, total = 0;
+  int grid = 0, cols = 0;  // cols: columns per thread (kC)
 };
 
 BwdLayout bwd_layout(int B, int T, int nv, int varlen, int sms) {
   BwdLayout l;
   const int64_t rows = varlen ? static_cast<int64_t>(T) : static_cast<int64_t>(B) * T;
-  const int64_t items = static_cast<int64_t>(B) * nv;
-  l.grid = static_cast<int>(items < sms ? items : sms);
-  const size_t state = static_cast<size_t>(kStateFloats) * sizeof(float);
-  l.part = 0;
-  l.ckpt = align256(2 * static_cast<size_t>(rows) * nv * gdn::kDim * sizeof(float));
-  l.blocks = align256(l.ckpt + (static_cast<size_t>(rows) / gdn::kBwdBlock + B + 1) * nv * state);
-  l.total = l.blocks + static_cast<size_t>(l.grid) * (gdn::kBwdBlock + 1) * state;
+  const int64_t chains = static_cast<int64_t>(B) * nv;
+  l.cols = 4;
+  for (int c = 1; c <= 2; c *= 2)
+    if (chains * (4 / c) <= static_cast<int64_t>(sms) * gdn::bwd_ctas_per_sm(c)) {
+      l.cols = c;
+      break;
+    }
+  const int nsplit = 4 / l.cols;
+  const int64_t items = chains * nsplit;
+  const int64_t slots = static_cast<int64_t>(sms) * gdn::bwd_ctas_per_sm(l.cols);
+  l.grid = static_cast<int>(items < slots ? items : slots);
+  const size_t part = static_cast<size_t>(rows) * nv * nsplit;
+  l.dq = 0;
+  l.dk = align256(l.dq + part * gdn::kDim * sizeof(float));
+  l.dg = align256(l.dk + part * gdn::kDim * sizeof(float));
+  l.dbeta = align256(l.dg + part * sizeof(float));
+  l.ckpt = align256(l.dbeta + part * sizeof(float));
+  l.blocks = align256(l.ckpt + (static_cast<size_t>(rows) / gdn::kBwdBlock + B + 1) * nv *
+                                   static_cast<size_t>(kStateFloats) * sizeof(float));
+  l.total = l.blocks + static_cast<size_t>(l.grid) * (gdn::kBwdBlock + 1) * gdn::kDim * (gdn::kDim / nsplit) *
+                           sizeof(float);
   return l;
 }
 
@@ -729,11 +745,13 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   p.h0 = h0;
   p.dout = dout;
   p.dst = dST;
-  p.dq_part = reinterpret_cast<float*>(w8 + l.part);
-  p.dk_part = p.dq_part + rows * nv * gdn::kDim;
+  p.dq_part = reinterpret_cast<float*>(w8 + l.dq);
+  p.dk_part = reinterpret_cast<float*>(w8 + l.dk);
+  p.dg_part = reinterpret_cast<float*>(w8 + l.dg);
+  p.dbeta_part = reinterpret_cast<float*>(w8 + l.dbeta);
   p.dv = dv;
-  p.dg = dg;
-  p.dbeta = dbeta;
+  p.dg_out = dg;
+  p.dbeta_out = dbeta;
   p.dh0 = dh0;
   p.ckpt = reinterpret_cast<float*>(w8 + l.ckpt);
   p.blocks = reinterpret_cast<float*>(w8 + l.blocks);
@@ -749,9 +767,14 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   p.nk = nk;
   p.nv = nv;
   p.state_is_table = r.table;
-  gdn::gdn_backward_kernel<<<static_cast<unsigned>(l.grid), gdn::kBwdThreads, 0, s>>>(p);
-  gdn::gdn_backward_reduce_kernel<<<static_cast<unsigned>(d->sms * 4), 256, 0, s>>>(p.dq_part, p.dk_part, dq, dk,
-                                                                                    rows, nk, nv);
+  p.nsplit = 4 / l.cols;
+  if (l.cols == 1)
+    gdn::gdn_backward_kernel<1><<<static_cast<unsigned>(l.grid), gdn::kBwdThreads, 0, s>>>(p);
+  else if (l.cols == 2)
+    gdn::gdn_backward_kernel<2><<<static_cast<unsigned>(l.grid), gdn::kBwdThreads, 0, s>>>(p);
+  else
+    gdn::gdn_backward_kernel<4><<<static_cast<unsigned>(l.grid), gdn::kBwdThreads, 0, s>>>(p);
+  gdn::gdn_backward_reduce_kernel<<<static_cast<unsigned>(d->sms * 4), 256, 0, s>>>(p, dq, dk, rows);
   int rc = GDN_OK;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) rc = fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));

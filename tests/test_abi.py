@@ -143,12 +143,20 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 
 def test_backward_workspace_sizes(lib):
-    # per-v-head dq/dk (2 x rows x nv x 128 fp32), a state per 64 rows per head (plus
-    # B + 1), and a 65-state slot per persistent CTA (min(B * nv, SMs); 152 SMs without
-    # a visible GPU)
+    # column-split parts of dq, dk (rows x nv x 4 x 128 fp32 each) and of dg, dbeta
+    # (rows x nv x 4), a state per 64 rows per head (plus B + 1), and a 65-block slot of
+    # 128 x 32 floats per persistent CTA (min(B * nv * 4, 3 * SMs); 152 SMs without a
+    # visible GPU)
+    def a256(x):
+        return (x + 255) // 256 * 256
+
     state = 128 * 128 * 4
     B, T, nv = 1, 4096, 32
-    part = 2 * B * T * nv * 128 * 4
-    ckpt = (B * T // 64 + B + 1) * nv * state
-    assert lib.gdn_prefill_backward_workspace_bytes(B, T, nv, 128, 128, 0) == part + ckpt + 32 * 65 * state
+    part = B * T * nv * 4
+    off = a256(part * 128 * 4)
+    off = a256(off + part * 128 * 4)
+    off = a256(off + part * 4)
+    off = a256(off + part * 4)
+    off = a256(off + (B * T // 64 + B + 1) * nv * state)
+    assert lib.gdn_prefill_backward_workspace_bytes(B, T, nv, 128, 128, 0) == off + 128 * 65 * 128 * 32 * 4
     assert lib.gdn_prefill_backward_workspace_bytes(0, T, nv, 128, 128, 0) == 0

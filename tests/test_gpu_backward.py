@@ -99,3 +99,17 @@ def test_backward_one_head_per_key():
     p = gdn_synth.make_problem(seed=8500, B=3, T=90, nk=3, nv=3, h0_std=0.02)
     got, ref = run_backward(p, 8500)
     assert_grads(got, ref, "nk = nv")
+
+
+@pytest.mark.parametrize("B,cols", [(4, 2), (5, 4)])
+def test_backward_wide_batches_use_wider_column_blocks(B, cols):
+    # 128 chains take 2 CTAs of 64 columns per (sequence, head), 160 chains one CTA of
+    # 128 columns (the kernel variants with 2 and 4 columns per thread); a ragged last
+    # recompute block
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    chains = B * 32
+    expect = 1 if chains * 4 <= 3 * sms else (2 if chains * 2 <= 2 * sms else 4)
+    assert expect == cols, "the case must select the intended variant on this device"
+    p = gdn_synth.make_problem(seed=8600 + B, B=B, T=70, nk=16, nv=32, h0_std=0.02)
+    got, ref = run_backward(p, 8600 + B)
+    assert_grads(got, ref, f"B={B} nv=32 ({cols} columns per thread)")
