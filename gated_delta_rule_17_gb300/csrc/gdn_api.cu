@@ -77,12 +77,13 @@ int device_info(DeviceInfo** out) {
     if (major != 10 || minor != 3)
       return fail(GDN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-    e = cudaFuncSetAttribute(gdn::gdn_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gdn::Plan::DYN_SMEM);
-    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    e = cudaFuncSetAttribute(gdn::gdn_prefill_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gdn::Plan::DYN_SMEM);
-    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    for (const void* f : {reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<true, false>),
+                          reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<true, true>),
+                          reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<false, false>),
+                          reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<false, true>)}) {
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, gdn::Plan::DYN_SMEM);
+      if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    }
     e = cudaFuncSetAttribute(gdn::gdn_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gdn::WyPlan::DYN_SMEM);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status);
@@ -350,6 +351,20 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
   return GDN_OK;
 }
 
+// One spine launch: the instantiation for output rows (or not) and the fused q/k norms (or not).
+void launch_spine(bool out_rows, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                  const CUtensorMap& mt, const gdn::ChunkParams& p, int64_t grid, cudaStream_t stream) {
+  const dim3 g(static_cast<unsigned>(grid)), blk(gdn::kThreads);
+  const size_t sm = gdn::Plan::DYN_SMEM;
+  if (out_rows) {
+    if (p.qk_l2norm) gdn::gdn_prefill_kernel<true, true><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
+    else gdn::gdn_prefill_kernel<true, false><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
+  } else {
+    if (p.qk_l2norm) gdn::gdn_prefill_kernel<false, true><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
+    else gdn::gdn_prefill_kernel<false, false><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
+  }
+}
+
 int launch(const void* q, const void* k, const void* v, const float* g, const float* beta, void* state, void* out,
            int B, int T, int nk, int nv, const Resolved& r, const int32_t* cu, int32_t* sched, cudaStream_t stream,
            void* seg_ws = nullptr, size_t seg_ws_bytes = 0) {
@@ -451,8 +466,7 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
     ps.seg = a.tab1;
     ps.state = a.ptr1;
     ps.B = sl.n1;
-    gdn::gdn_prefill_kernel<false><<<static_cast<unsigned>(static_cast<int64_t>(sl.n1) * nv), gdn::kThreads,
-                                     gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt, ps);
+    launch_spine(false, mq, mk, mv, mt, ps, static_cast<int64_t>(sl.n1) * nv, stream);
     ++launches;
     for (int gs = 0; gs <= sp.G - 2; ++gs) {
       gdn_segment_combine_kernel<<<static_cast<unsigned>(B * nv * 4), kCombineThreads, 0, stream>>>(a, gs);
@@ -461,14 +475,12 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
     ps.seg = a.tab2;
     ps.state = a.ptr2;
     ps.B = sl.n2;
-    gdn::gdn_prefill_kernel<true><<<static_cast<unsigned>(static_cast<int64_t>(sl.n2) * nv), gdn::kThreads,
-                                    gdn::Plan::DYN_SMEM, stream>>>(mq, mk, mv, mt, ps);
+    launch_spine(true, mq, mk, mv, mt, ps, static_cast<int64_t>(sl.n2) * nv, stream);
     ++launches;
   } else {
     const int64_t grid = static_cast<int64_t>(B) * nv;
     if (grid > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "grid of %lld CTAs too large", (long long)grid);
-    gdn::gdn_prefill_kernel<true><<<static_cast<unsigned>(grid), gdn::kThreads, gdn::Plan::DYN_SMEM, stream>>>(
-        mq, mk, mv, mt, p);
+    launch_spine(true, mq, mk, mv, mt, p, grid, stream);
     ++launches;
   }
   if (g_timing[2]) cudaEventRecord(g_timing[2], stream);

@@ -148,7 +148,7 @@ __device__ __forceinline__ bool group_wait(const Ctx& x, const ChunkParams& p, u
 // (the issuer runs its MMAs). Warp 4 also scans the gates of the chunk after,
 // so every chunk starts with its gate set ready.
 // ---------------------------------------------------------------------------------
-template <bool kOut>
+template <bool kOut, bool kNorm>
 __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p, int ptid) {
   using P = Plan;
   const int pw = ptid >> 5, lane = ptid & 31;
@@ -260,10 +260,10 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         }
       }
       signal(x.mb_vrdy);  // V is fp16: the U MMAs may go
-      if (p.qk_l2norm) tc::named_barrier(kBarNorm, kProducerThreads);
+      if constexpr (kNorm) tc::named_barrier(kBarNorm, kProducerThreads);
     } else {
       // ---- A (fp16 hi + lo) from Q K^T, lanes 64-127 ------------------------------------
-      if (p.qk_l2norm) {
+      if constexpr (kNorm) {
         // fused prologue, while the Gram MMA runs: one raw row per thread, K rows 0-63
         // then Q rows 0-63, read once the tile has landed and before any thread converts
         // it in place. The inverse norms are folded into this chunk's per-token factors
@@ -312,7 +312,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 #pragma unroll
             for (int e = 0; e < 8; ++e) a[e] = (j0 + e <= i) ? ei * f[e] * __uint_as_float(d[e]) : 0.f;
           } else {
-            const bool norm = p.qk_l2norm != 0;
+            constexpr bool norm = kNorm;
             const float ri = (norm ? x.s_rq[i] : 1.f) * kInvSqrtD;
             const float gi = x.s_gc[gs + i];
 #pragma unroll
@@ -730,8 +730,10 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
 }
 
 // kOut = false: runs that only carry the state (the segment schedule's state maps):
-// no Gram, A, Q~, output MMAs or output rows.
-template <bool kOut = true>
+// no Gram, A, Q~, output MMAs or output rows. kNorm: the fused q/k normalisation
+// (ChunkParams::qk_l2norm), a separate instantiation so that the common path carries
+// none of its code.
+template <bool kOut = true, bool kNorm = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_t,
@@ -834,7 +836,7 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   if (warp < kConsumerWarps)
     consumer_role<kOut>(x, p, tid);
   else if (warp < kConsumerWarps + kProducerWarps)
-    producer_role<kOut>(x, p, tid - kConsumerThreads);
+    producer_role<kOut, kNorm>(x, p, tid - kConsumerThreads);
   else if ((tid & 31) == 0)
     issuer_role<kOut>(x, p, &tmap_q, &tmap_k, &tmap_v, &tmap_t, warp == kConsumerWarps + kProducerWarps + 1);
 
