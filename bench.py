@@ -476,6 +476,7 @@ def run_backward(args, world, rank, local):
     barrier(world)
     gdn.check()
     ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+    launches = gdn.last_launch_count()
     hbm_peak, _, peak_src = measured_peaks()
     tokens = p.tokens
     # each input read once and each gradient written once, the states in and out
@@ -487,13 +488,15 @@ def run_backward(args, world, rank, local):
             "metric": "GDN prefill backward tokens/s (dq, dk, dv, dg, dbeta, dS_0), 1xGB300",
             "value": world * tokens / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16 inputs, fp32 gradients, state and arithmetic", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16 inputs, fp16 tensor-core operands, fp32 accumulate, states and gradients",
+            "data": "synthetic",
             "config": {"workload": gdn_synth.CONFIG_NAMES[args.config], "parallelism": "1 GPU",
                        "l2": "no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None, "kernel": "gdn_backward_kernel",
+                         "frac": achieved / hbm_peak, "traffic": None,
+                         "kernel": "whole backward (WY, two chains, per-chunk gradients, GQA reduce)",
                          "algorithmic_bytes": io, "peak_source": peak_src},
-            "gpu_launches": 2 * args.steps, "clocks": clk.summary()}), flush=True)
+            "gpu_launches": launches * args.steps, "clocks": clk.summary()}), flush=True)
 
 
 def main():

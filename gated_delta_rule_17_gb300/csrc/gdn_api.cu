@@ -15,12 +15,13 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "gdn_prefill.h"
 #include "gdn_prefill_kernel.cuh"
 #include "gdn_wy_kernel.cuh"
 #include "gdn_decode_kernel.cuh"
-#include "gdn_backward_kernel.cuh"
+#include "gdn_bwd_chunk_kernel.cuh"
 
 namespace {
 
@@ -86,6 +87,14 @@ int device_info(DeviceInfo** out) {
     }
     e = cudaFuncSetAttribute(gdn::gdn_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gdn::WyPlan::DYN_SMEM);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    const std::pair<const void*, int> bwd[] = {
+        {reinterpret_cast<const void*>(gdn::gdn_bwd_states_kernel), gdn::kStatesSmem},
+        {reinterpret_cast<const void*>(gdn::gdn_bwd_dstates_kernel), gdn::kDStatesSmem},
+        {reinterpret_cast<const void*>(gdn::gdn_bwd_grads_kernel), gdn::kGradsSmem}};
+    for (const auto& f : bwd) {
+      e = cudaFuncSetAttribute(f.first, cudaFuncAttributeMaxDynamicSharedMemorySize, f.second);
+      if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    }
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
     d.attrs = true;
@@ -351,6 +360,20 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
   return GDN_OK;
 }
 
+// WY launch geometry. Items: dense batches every (chunk, v-head); varlen an upper
+// bound on them (sum of ceil(len / 64) <= T / 64 + B), whose excess CTAs exit at
+// once. The kernel is persistent: a few CTAs per SM walk the items.
+int wy_geometry(const DeviceInfo& d, int B, int T, int nv, bool varlen, int* items, int64_t* grid) {
+  const int64_t chunks = varlen ? static_cast<int64_t>(T) / gdn::kChunk + B + 1
+                                : static_cast<int64_t>((T + gdn::kChunk - 1) / gdn::kChunk) * B;
+  if (chunks * nv + static_cast<int64_t>(d.sms) * gdn::kWyCtasPerSm > INT32_MAX)
+    return fail(GDN_ERR_UNSUPPORTED, "%lld (chunk, head) items exceed the 2^31 item range", (long long)(chunks * nv));
+  *items = static_cast<int>(chunks * nv);
+  const int64_t slots = static_cast<int64_t>(d.sms) * gdn::kWyCtasPerSm;
+  *grid = *items < slots ? *items : slots;
+  return GDN_OK;
+}
+
 // One spine launch: the instantiation for output rows (or not) and the fused q/k norms (or not).
 void launch_spine(bool out_rows, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                   const CUtensorMap& mt, const gdn::ChunkParams& p, int64_t grid, cudaStream_t stream) {
@@ -397,16 +420,9 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   w.nv = nv;
   w.chunks_per_seq = (T + gdn::kChunk - 1) / gdn::kChunk;
   w.qk_l2norm = r.l2norm;
-  // dense: every chunk of every sequence; varlen: an upper bound on the chunk
-  // count (sum of ceil(len / 64) <= T / 64 + B), the excess CTAs exit at once
-  const int64_t wy_chunks = cu ? static_cast<int64_t>(T) / gdn::kChunk + B + 1
-                               : static_cast<int64_t>(w.chunks_per_seq) * B;
-  if (wy_chunks * nv + static_cast<int64_t>(d->sms) * gdn::kWyCtasPerSm > INT32_MAX)
-    return fail(GDN_ERR_UNSUPPORTED, "%lld (chunk, head) items exceed the 2^31 item range", (long long)(wy_chunks * nv));
-  w.items = static_cast<int>(wy_chunks * nv);
-  // persistent: a few CTAs per SM walk the items
-  const int64_t wy_grid = w.items < static_cast<int64_t>(d->sms) * gdn::kWyCtasPerSm
-                              ? w.items : static_cast<int64_t>(d->sms) * gdn::kWyCtasPerSm;
+  w.t_only = 0;
+  int64_t wy_grid = 0;
+  if (int rc = wy_geometry(*d, B, T, nv, cu != nullptr, &w.items, &wy_grid)) return rc;
 
   gdn::ChunkParams p;
   p.g = g;
@@ -528,40 +544,29 @@ int noalloc_scratch(int32_t** out) {
 }
 
 // ---- backward -------------------------------------------------------------------
-// Column split of the backward: each (sequence, v-head) item runs on nsplit CTAs of
-// 128 / nsplit columns, the most that the SMs hold at once (4, then 2, then 1).
-// Scratch: the split parts of dq, dk (2 x rows x nv x nsplit x 128 fp32) and of dg,
-// dbeta (2 x rows x nv x nsplit), the states at 64-token boundaries ((rows/64 + B + 1)
-// x nv states) and one 65-block slot of 128 x 128/nsplit floats per persistent CTA.
+// Scratch of the chunked backward: the varlen schedule; T (16-bit, rows x nv x 128),
+// u and du' (fp16, same shape); each chunk's S0 and dS_end (fp16 128 x 128 per
+// (chunk slot, v-head), rows / 64 + B + 1 slots); the per-v-head dq and dk parts
+// (fp32, rows x nv x 128 each).
 struct BwdLayout {
-  size_t dq = 0, dk = 0, dg = 0, dbeta = 0, ckpt = 0, blocks = 0, total = 0;
-  int grid = 0, cols = 0;  // cols: columns per thread (kC)
+  size_t sched = 0, tm = 0, u = 0, du = 0, s0 = 0, ds = 0, dq = 0, dk = 0, total = 0;
 };
 
-BwdLayout bwd_layout(int B, int T, int nv, int varlen, int sms) {
+BwdLayout bwd_layout(int B, int T, int nv, int varlen) {
   BwdLayout l;
-  const int64_t rows = varlen ? static_cast<int64_t>(T) : static_cast<int64_t>(B) * T;
-  const int64_t chains = static_cast<int64_t>(B) * nv;
-  l.cols = 4;
-  for (int c = 1; c <= 2; c *= 2)
-    if (chains * (4 / c) <= static_cast<int64_t>(sms) * gdn::bwd_ctas_per_sm(c)) {
-      l.cols = c;
-      break;
-    }
-  const int nsplit = 4 / l.cols;
-  const int64_t items = chains * nsplit;
-  const int64_t slots = static_cast<int64_t>(sms) * gdn::bwd_ctas_per_sm(l.cols);
-  l.grid = static_cast<int>(items < slots ? items : slots);
-  const size_t part = static_cast<size_t>(rows) * nv * nsplit;
-  l.dq = 0;
-  l.dk = align256(l.dq + part * gdn::kDim * sizeof(float));
-  l.dg = align256(l.dk + part * gdn::kDim * sizeof(float));
-  l.dbeta = align256(l.dg + part * sizeof(float));
-  l.ckpt = align256(l.dbeta + part * sizeof(float));
-  l.blocks = align256(l.ckpt + (static_cast<size_t>(rows) / gdn::kBwdBlock + B + 1) * nv *
-                                   static_cast<size_t>(kStateFloats) * sizeof(float));
-  l.total = l.blocks + static_cast<size_t>(l.grid) * (gdn::kBwdBlock + 1) * gdn::kDim * (gdn::kDim / nsplit) *
-                           sizeof(float);
+  const size_t rows = varlen ? static_cast<size_t>(T) : static_cast<size_t>(B) * T;
+  const size_t slots = rows / gdn::kChunk + B + 1;
+  const size_t row16 = rows * nv * gdn::kDim * 2;
+  const size_t state16 = slots * nv * static_cast<size_t>(kStateFloats) * 2;
+  l.sched = 0;
+  l.tm = align256(varlen ? (2 * static_cast<size_t>(B) + 1) * sizeof(int32_t) : 0);
+  l.u = align256(l.tm + row16);
+  l.du = align256(l.u + row16);
+  l.s0 = align256(l.du + row16);
+  l.ds = align256(l.s0 + state16);
+  l.dq = align256(l.ds + state16);
+  l.dk = align256(l.dq + 2 * row16);
+  l.total = align256(l.dk + 2 * row16);
   return l;
 }
 
@@ -704,7 +709,7 @@ size_t gdn_prefill_backward_workspace_bytes(int B, int T, int nv, int dk, int dv
   (void)dk;
   (void)dv;
   if (B <= 0 || T <= 0 || nv <= 0) return 0;
-  return bwd_layout(B, T, nv, varlen, plan_sms()).total;
+  return bwd_layout(B, T, nv, varlen).total;
 }
 
 int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -731,13 +736,21 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   if (r.l2norm) return fail(GDN_ERR_UNSUPPORTED, "the backward takes already normalised q and k (qk_l2norm = 0)");
   if (B == 0 || T == 0) return GDN_OK;
   if (!dq || !dk || !dv || !dg || !dbeta) return fail(GDN_ERR_ARG, "a gradient output pointer is NULL");
-  if (!aligned16(dv) || (dST && !aligned16(dST)) || (dh0 && !aligned16(dh0)))
-    return fail(GDN_ERR_ARG, "dv, dS_T and dh0 must be 16-byte aligned");
+  if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv) || (dST && !aligned16(dST)) || (dh0 && !aligned16(dh0)))
+    return fail(GDN_ERR_ARG, "dq, dk, dv, dS_T and dh0 must be 16-byte aligned");
   DeviceInfo* d = nullptr;
   if (int rc = device_info(&d)) return rc;
   const int64_t rows = cu_seqlens ? static_cast<int64_t>(T) : static_cast<int64_t>(B) * T;
-  const BwdLayout l = bwd_layout(B, T, nv, cu_seqlens != nullptr, d->sms);
+  if (rows > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "%lld token rows exceed the 2^31 TMA coordinate range", (long long)rows);
+  const BwdLayout l = bwd_layout(B, T, nv, cu_seqlens != nullptr);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap mk;
+  if (int rc = make_map(&mk, k, static_cast<int64_t>(nk) * gdn::kDim, rows, r.k, "k")) return rc;
+  gdn::WyParams w;
+  int64_t wy_grid = 0;
+  if (int rc = wy_geometry(*d, B, T, nv, cu_seqlens != nullptr, &w.items, &wy_grid)) return rc;
+  const int64_t grad_items = static_cast<int64_t>(w.items);  // (chunk, v-head) items, same bound
+  if (static_cast<int64_t>(B) * nv > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "too many (sequence, head) chains");
   void* ws = workspace;
   if (ws) {
     if (workspace_bytes_ < l.total)
@@ -748,7 +761,28 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaMallocAsync(%zu): %s", l.total, cudaGetErrorString(e));
   }
   char* w8 = static_cast<char*>(ws);
-  gdn::BwdParams p;
+  int32_t* sched = cu_seqlens ? reinterpret_cast<int32_t*>(w8 + l.sched) : nullptr;
+  int32_t* order = sched;
+  int32_t* cu_chunks = sched ? sched + B : nullptr;
+
+  w.g = g;
+  w.beta = beta;
+  w.tb = reinterpret_cast<uint16_t*>(w8 + l.tm);
+  w.cu_seqlens = cu_seqlens;
+  w.cu_chunks = cu_chunks;
+  w.status = d->status;
+  w.g_stride = r.g;
+  w.beta_stride = r.beta;
+  w.out_stride = static_cast<int64_t>(nv) * gdn::kDim;
+  w.B = B;
+  w.T = T;
+  w.nk = nk;
+  w.nv = nv;
+  w.chunks_per_seq = (T + gdn::kChunk - 1) / gdn::kChunk;
+  w.qk_l2norm = 0;
+  w.t_only = 1;
+
+  gdn::BwdChunkParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
   p.v = static_cast<const __nv_bfloat16*>(v);
@@ -757,17 +791,20 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   p.h0 = h0;
   p.dout = dout;
   p.dst = dST;
+  p.tm = w.tb;
+  p.ubuf = reinterpret_cast<__half*>(w8 + l.u);
+  p.dubuf = reinterpret_cast<__half*>(w8 + l.du);
+  p.s0buf = reinterpret_cast<__half*>(w8 + l.s0);
+  p.dsbuf = reinterpret_cast<__half*>(w8 + l.ds);
   p.dq_part = reinterpret_cast<float*>(w8 + l.dq);
   p.dk_part = reinterpret_cast<float*>(w8 + l.dk);
-  p.dg_part = reinterpret_cast<float*>(w8 + l.dg);
-  p.dbeta_part = reinterpret_cast<float*>(w8 + l.dbeta);
   p.dv = dv;
-  p.dg_out = dg;
-  p.dbeta_out = dbeta;
+  p.dg = dg;
+  p.dbeta = dbeta;
   p.dh0 = dh0;
-  p.ckpt = reinterpret_cast<float*>(w8 + l.ckpt);
-  p.blocks = reinterpret_cast<float*>(w8 + l.blocks);
   p.cu_seqlens = cu_seqlens;
+  p.order = order;
+  p.cu_chunks = cu_chunks;
   p.status = d->status;
   p.q_stride = r.q;
   p.k_stride = r.k;
@@ -779,14 +816,20 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   p.nk = nk;
   p.nv = nv;
   p.state_is_table = r.table;
-  p.nsplit = 4 / l.cols;
-  if (l.cols == 1)
-    gdn::gdn_backward_kernel<1><<<static_cast<unsigned>(l.grid), gdn::kBwdThreads, 0, s>>>(p);
-  else if (l.cols == 2)
-    gdn::gdn_backward_kernel<2><<<static_cast<unsigned>(l.grid), gdn::kBwdThreads, 0, s>>>(p);
-  else
-    gdn::gdn_backward_kernel<4><<<static_cast<unsigned>(l.grid), gdn::kBwdThreads, 0, s>>>(p);
-  gdn::gdn_backward_reduce_kernel<<<static_cast<unsigned>(d->sms * 4), 256, 0, s>>>(p, dq, dk, rows);
+  p.items = static_cast<int>(grad_items);
+
+  int launches = 0;
+  if (cu_seqlens) {
+    gdn_schedule_kernel<<<(B + 255) / 256, 256, 0, s>>>(cu_seqlens, B, T, order, cu_chunks, d->status);
+    ++launches;
+  }
+  gdn::gdn_wy_kernel<<<static_cast<unsigned>(wy_grid), gdn::kWyThreads, gdn::WyPlan::DYN_SMEM, s>>>(mk, w);
+  const unsigned chains = static_cast<unsigned>(static_cast<int64_t>(B) * nv);
+  gdn::gdn_bwd_states_kernel<<<chains, gdn::kBcThreads, gdn::kStatesSmem, s>>>(p);
+  gdn::gdn_bwd_dstates_kernel<<<chains, gdn::kBcThreads, gdn::kDStatesSmem, s>>>(p);
+  gdn::gdn_bwd_grads_kernel<<<static_cast<unsigned>(grad_items), gdn::kBcThreads, gdn::kGradsSmem, s>>>(p);
+  gdn::gdn_bwd_reduce_kernel<<<static_cast<unsigned>(d->sms * 4), 256, 0, s>>>(p, dq, dk, rows);
+  launches += 5;
   int rc = GDN_OK;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) rc = fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
@@ -794,7 +837,7 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
     e = cudaFreeAsync(ws, s);
     if (e != cudaSuccess && rc == GDN_OK) rc = fail(GDN_ERR_CUDA, "cudaFreeAsync: %s", cudaGetErrorString(e));
   }
-  if (rc == GDN_OK) g_launches = 2;
+  if (rc == GDN_OK) g_launches = launches;
   return rc;
 }
 

@@ -1,0 +1,867 @@
+// Chunked backward of the gated delta rule (the training pass) for sm_103a.
+//
+// The forward (ssm_gdn_a3.rs, `gdn_prefill_fla` doc comment: the chunked WY form
+// of S_t = e^{g_t}(I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+// o_t = S_t^T q_t / sqrt(dk)) is, per chunk of 64 tokens with entry state S0,
+// in-chunk log-decay prefix b (Gamma = e^b, gamma = Gamma_last) and
+// M_tj = e^{b_t - b_j} (j <= t):
+//
+//     L = strict_lower(beta_t M_tj k_t.k_j),  T = (I + L)^{-1}
+//     X = V - Gamma K S0,                     u = T diag(beta) X
+//     O = Gamma Q S0 / sqrt(dk) + (Q K^T . M) u / sqrt(dk)
+//     S_end = gamma S0 + (gamma / Gamma) K^T u
+//
+// Its derivative, with dS_end the gradient of the chunk's end state (the pages
+// describe only the forward; this is the chain rule through the lines above):
+//
+//     du  = (Q K^T . M)^T dO / sqrt(dk) + (gamma / Gamma) K dS_end
+//     du' = T^T du,   r = beta du',   dV = r
+//     dS0 = gamma dS_end + Q^T (Gamma dO) / sqrt(dk) - K^T (Gamma r)
+//
+// and, per chunk and independent of the other chunks once S0 and dS_end are known,
+// with dA = lower(dO u^T) . M / sqrt(dk), F = -strict_lower(du' u^T) . M, E = beta F,
+// P = du' S0^T, G = K K^T:
+//
+//     dQ = Gamma dO S0^T / sqrt(dk) + dA K
+//     dK = E K + E^T K - Gamma beta P + dA^T Q + (gamma / Gamma) u dS_end^T
+//     dbeta_t = du'_t.v_t - Gamma_t k_t.P_t + sum_j F_tj G_tj
+//     d b_t   = Gamma_t q_t.(dO S0^T)_t / sqrt(dk) - Gamma_t beta_t k_t.P_t
+//               + rows - columns of (E . G) and of (dA . Q K^T)
+//               - w_t, w_t = (gamma / Gamma_t) k_t.(u dS_end^T)_t,
+//               plus gamma <dS_end, S0> + sum_t w_t on the last token
+//     dg_t = sum of d b over the chunk's tokens t .. 63
+//
+// Three kernels: gdn_bwd_states_kernel runs the forward chain once per (sequence,
+// v-head), storing every chunk's entry state S0 and u; gdn_bwd_dstates_kernel runs
+// the reverse chain, storing every chunk's dS_end and du' and writing dV;
+// gdn_bwd_grads_kernel takes one (chunk, v-head) each and writes dQ, dK (per
+// v-head, summed over each GQA group by gdn_bwd_reduce_kernel), dbeta and dg.
+// T comes from the forward's WY kernel (unscaled by beta). Every contraction is an
+// fp16 tensor-core product with fp32 accumulation (gdn_mma.cuh); the two chains
+// carry their state in fp32 registers and feed it to the tensor cores as an fp16
+// hi + lo pair, as do the operands that enter the chains (T, beta X, u, du, r).
+//
+// Padding tokens of a ragged last chunk are loaded as q = k = v = dO = 0,
+// g = beta = 0, and T's rows past the chunk's end as 0: every product then
+// reduces to the chunk's real tokens, and gamma = Gamma_63.
+#pragma once
+#include "gdn_common.cuh"
+#include "gdn_mma.cuh"
+
+namespace gdn {
+
+constexpr int kBcThreads = 256;
+constexpr int kLd = kDim + 8;     // halves per row of a 128-wide fp16 tile
+constexpr int kLd64 = kChunk + 8; // halves per row of a 64-wide fp16 tile
+constexpr int kTile128 = kChunk * kLd * 2;       // bytes of a 64 x 128 tile
+constexpr int kTile64 = kChunk * kLd64 * 2;      // bytes of a 64 x 64 tile
+constexpr int kTileState = kDim * kLd * 2;       // bytes of a 128 x 128 tile
+
+struct BwdChunkParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const float* g;
+  const float* beta;
+  const void* h0;      // float[B][nv][128][128], or float*[B] when state_is_table
+  const float* dout;   // [rows][nv][128]
+  const float* dst;    // [B][nv][128][128] or null (zero)
+  const uint16_t* tm;  // [rows][nv][128]: row t of the chunk's T, 64 fp16 hi then 64 lo
+  __half* ubuf;        // [rows][nv][128]: u
+  __half* dubuf;       // [rows][nv][128]: du' = T^T du
+  __half* s0buf;       // [slots][nv][128][128]: each chunk's entry state S0 ([k][v])
+  __half* dsbuf;       // [slots][nv][128][128]: each chunk's dS_end ([k][v])
+  float* dq_part;      // [rows][nv][128]
+  float* dk_part;      // [rows][nv][128]
+  float* dv;           // [rows][nv][128]
+  float* dg;           // [rows][nv]
+  float* dbeta;        // [rows][nv]
+  float* dh0;          // [B][nv][128][128] or null
+  const int32_t* cu_seqlens;
+  const int32_t* order;      // varlen: sequences by decreasing length
+  const int32_t* cu_chunks;  // varlen: chunk prefix over the sequences
+  unsigned* status;
+  int64_t q_stride, k_stride, v_stride, g_stride, beta_stride;
+  int B, T, nk, nv;
+  int state_is_table;
+  int items;  // gdn_bwd_grads_kernel: (chunk, v-head) items, an upper bound for varlen
+};
+
+// Rows of sequence s; false (and the status bit) for an invalid cu_seqlens entry.
+__device__ __forceinline__ bool bc_sequence(const BwdChunkParams& p, int s, int64_t& row0, int64_t& len) {
+  if (p.cu_seqlens) {
+    const int a = p.cu_seqlens[s], e = p.cu_seqlens[s + 1];
+    if (a < 0 || e < a || e > p.T) {
+      if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSeqlens);
+      return false;
+    }
+    row0 = a;
+    len = e - a;
+  } else {
+    row0 = static_cast<int64_t>(s) * p.T;
+    len = p.T;
+  }
+  return true;
+}
+
+// Slot of chunk c of the sequence starting at row0 (unique over the batch: the
+// chunks of sequence s occupy row0 / 64 + s + [0, chunks)).
+__device__ __forceinline__ int64_t bc_slot(int64_t row0, int s, int64_t c) { return row0 / kChunk + s + c; }
+
+// 64 x 128 bf16 rows (row stride in elements) -> fp16 tile; rows >= n are zero.
+__device__ __forceinline__ void bc_load_bf16(__half* dst, const __nv_bfloat16* src, int64_t stride, int n) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (row < n) {
+      float f[8];
+      unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(src + row * stride) + c8), f);
+      o = pack_half8(f, 1.f);
+    }
+    *reinterpret_cast<uint4*>(dst + row * kLd + 8 * c8) = o;
+  }
+}
+
+// 64 x 128 fp16 rows of a [rows][nv][128] buffer -> tile; rows >= n are zero.
+__device__ __forceinline__ void bc_load_half(__half* dst, const __half* src, int64_t stride, int n) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (row < n) o = __ldg(reinterpret_cast<const uint4*>(src + row * stride) + c8);
+    *reinterpret_cast<uint4*>(dst + row * kLd + 8 * c8) = o;
+  }
+}
+
+// 64 x 128 fp32 rows of dO -> fp16 tile scaled by scale[row] (or 1); rows >= n are zero.
+__device__ __forceinline__ void bc_load_f32(__half* dst, const float* src, int64_t stride, int n,
+                                            const float* scale) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 5, c4 = idx & 31;
+    uint2 o = make_uint2(0, 0);
+    if (row < n) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(src + row * stride) + c4);
+      const float s = scale ? scale[row] : 1.f;
+      o = make_uint2(pack_half2(x.x * s, x.y * s), pack_half2(x.z * s, x.w * s));
+    }
+    *reinterpret_cast<uint2*>(dst + row * kLd + 4 * c4) = o;
+  }
+}
+
+// The chunk's T rows (hi and lo 64 x 64 tiles); rows >= n are zero.
+__device__ __forceinline__ void bc_load_t(__half* th, __half* tl, const uint16_t* src, int64_t stride, int n) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (row < n) o = __ldg(reinterpret_cast<const uint4*>(src + row * stride) + c8);
+    __half* d = (c8 < 8 ? th : tl) + row * kLd64 + 8 * (c8 & 7);
+    *reinterpret_cast<uint4*>(d) = o;
+  }
+}
+
+// Gates of a chunk, by warp 0: b (in-chunk log-decay prefix) and beta per token,
+// zero past the chunk's end.
+__device__ __forceinline__ void bc_gates(const BwdChunkParams& p, int64_t r0, int n, int h, float* s_b,
+                                         float* s_beta) {
+  const int lane = threadIdx.x & 31;
+  const int t0 = 2 * lane, t1 = 2 * lane + 1;
+  const float g0 = t0 < n ? p.g[(r0 + t0) * p.g_stride + h] : 0.f;
+  const float g1 = t1 < n ? p.g[(r0 + t1) * p.g_stride + h] : 0.f;
+  const GatePrefix gp = gate_prefix(g0, g1);
+  s_b[t0] = gp.gca;
+  s_b[t1] = gp.gcb;
+  s_beta[t0] = t0 < n ? p.beta[(r0 + t0) * p.beta_stride + h] : 0.f;
+  s_beta[t1] = t1 < n ? p.beta[(r0 + t1) * p.beta_stride + h] : 0.f;
+}
+
+// fp32 accumulator fragment -> fp16 hi and lo tiles (row-major, leading dimension ld).
+template <int NT>
+__device__ __forceinline__ void bc_store_split(const float (&c)[NT][4], __half* hi, __half* lo, int ld, int m0,
+                                               int n0) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int row = m0 + gq + 8 * e, col = n0 + 8 * j + 2 * tq;
+      __half2 h, l;
+      mm::split2(c[j][2 * e], c[j][2 * e + 1], h, l);
+      *reinterpret_cast<__half2*>(hi + row * ld + col) = h;
+      *reinterpret_cast<__half2*>(lo + row * ld + col) = l;
+    }
+}
+
+// 128 x 128 fp16 tile (leading dimension kLd) -> global [128][128].
+__device__ __forceinline__ void bc_store_state(__half* dst, const __half* src) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+    reinterpret_cast<uint4*>(dst + row * kDim)[c8] = *reinterpret_cast<const uint4*>(src + row * kLd + 8 * c8);
+  }
+}
+
+// 64 x 128 bf16 rows -> bf16 tile (no conversion); rows >= n are zero.
+__device__ __forceinline__ void bc_load_raw(__nv_bfloat16* dst, const __nv_bfloat16* src, int64_t stride, int n) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (row < n) o = __ldg(reinterpret_cast<const uint4*>(src + row * stride) + c8);
+    *reinterpret_cast<uint4*>(dst + row * kLd + 8 * c8) = o;
+  }
+}
+
+__device__ __forceinline__ const float* bc_h0(const BwdChunkParams& p, int s, int h) {
+  const float* h0 = p.state_is_table ? reinterpret_cast<const float* const*>(p.h0)[s]
+                                     : reinterpret_cast<const float*>(p.h0) + static_cast<int64_t>(s) * p.nv * kDim * kDim;
+  return h0 + static_cast<int64_t>(h) * kDim * kDim;
+}
+
+// ---- forward chain: every chunk's entry state S0 and u ------------------------------
+// One CTA per (sequence, v-head). The state lives in fp32 registers: warp w holds
+// rows 16 w .. 16 w + 15 (k) and all 128 columns (v).
+constexpr int kStatesSmem = 2 * kTile128 + 2 * kTile64 + 2 * kTileState + 4 * kTile128;
+
+__global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const BwdChunkParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __half* sK = reinterpret_cast<__half*>(smem);
+  __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(smem + kTile128);
+  __half* sTh = reinterpret_cast<__half*>(smem + 2 * kTile128);
+  __half* sTl = sTh + kChunk * kLd64;
+  __half* sSh = reinterpret_cast<__half*>(smem + 2 * kTile128 + 2 * kTile64);
+  __half* sSl = sSh + kDim * kLd;
+  __half* sXh = sSl + kDim * kLd;
+  __half* sXl = sXh + kChunk * kLd;
+  __half* sUh = sXl + kChunk * kLd;
+  __half* sUl = sUh + kChunk * kLd;
+  __shared__ float s_b[kChunk], s_beta[kChunk];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  const int si = blockIdx.x / p.nv, h = blockIdx.x % p.nv, kh = h / (p.nv / p.nk);
+  const int s = p.order ? p.order[si] : si;
+  int64_t row0, len;
+  if (!bc_sequence(p, s, row0, len)) return;
+  const int64_t nch = (len + kChunk - 1) / kChunk;
+  if (nch == 0) return;
+  const int64_t hrow = static_cast<int64_t>(p.nv) * kDim;  // row stride of the [rows][nv][128] buffers
+  const int sm0 = 16 * warp;
+  const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);  // 64 x 128 products
+  const uint32_t aK = mm::saddr(sK), aTh = mm::saddr(sTh), aTl = mm::saddr(sTl), aSh = mm::saddr(sSh),
+                 aSl = mm::saddr(sSl), aXh = mm::saddr(sXh), aXl = mm::saddr(sXl), aUh = mm::saddr(sUh),
+                 aUl = mm::saddr(sUl);
+
+  float S[16][4];
+  {
+    const float* h0 = bc_h0(p, s, h);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float2 x = *reinterpret_cast<const float2*>(h0 + (sm0 + gq + 8 * e) * kDim + 8 * j + 2 * tq);
+        S[j][2 * e] = x.x;
+        S[j][2 * e + 1] = x.y;
+      }
+  }
+  bc_store_split<16>(S, sSh, sSl, kLd, sm0, 0);
+  __syncthreads();
+
+  for (int64_t c = 0; c < nch; ++c) {
+    const int64_t r0 = row0 + c * kChunk;
+    const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
+    bc_store_state(p.s0buf + (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim, sSh);
+    if (warp == 0) bc_gates(p, r0, n, h, s_b, s_beta);
+    bc_load_bf16(sK, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
+    bc_load_raw(sV, p.v + r0 * p.v_stride + h * kDim, p.v_stride, n);
+    bc_load_t(sTh, sTl, p.tm + r0 * hrow + h * kDim, hrow, n);
+    __syncthreads();
+
+    // K S0, then beta X = beta (V - Gamma K S0) as fp16 hi + lo
+    {
+      float acc[8][4];
+      mm::zero(acc);
+      mm::warp_mma<false, false, 8>(acc, aK, kLd, aSh, kLd, m0, n0, kDim);
+      mm::warp_mma<false, false, 8>(acc, aK, kLd, aSl, kLd, m0, n0, kDim);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = m0 + gq + 8 * e;
+        const float G = __expf(s_b[t]), bt = s_beta[t];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sV + t * kLd + n0 + 8 * j + 2 * tq));
+          acc[j][2 * e] = bt * (vv.x - G * acc[j][2 * e]);
+          acc[j][2 * e + 1] = bt * (vv.y - G * acc[j][2 * e + 1]);
+        }
+      }
+      bc_store_split<8>(acc, sXh, sXl, kLd, m0, n0);
+    }
+    __syncthreads();
+
+    // u = T (beta X): stored for the gradient kernel; (gamma / Gamma) u as fp16 hi + lo
+    {
+      float acc[8][4];
+      mm::zero(acc);
+      mm::warp_mma<false, false, 8>(acc, aTh, kLd64, aXh, kLd, m0, n0, kChunk);
+      mm::warp_mma<false, false, 8>(acc, aTh, kLd64, aXl, kLd, m0, n0, kChunk);
+      mm::warp_mma<false, false, 8>(acc, aTl, kLd64, aXh, kLd, m0, n0, kChunk);
+      const float blast = s_b[kChunk - 1];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = m0 + gq + 8 * e;
+        const float sc = __expf(blast - s_b[t]);
+        __half* urow = p.ubuf + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (t < n) *reinterpret_cast<__half2*>(urow + 8 * j) = __floats2half2_rn(acc[j][2 * e], acc[j][2 * e + 1]);
+          acc[j][2 * e] *= sc;
+          acc[j][2 * e + 1] *= sc;
+        }
+      }
+      bc_store_split<8>(acc, sUh, sUl, kLd, m0, n0);
+    }
+    __syncthreads();
+
+    // S = gamma S + K^T ((gamma / Gamma) u)
+    {
+      const float gam = __expf(s_b[kChunk - 1]);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) S[j][x] *= gam;
+      mm::warp_mma<true, false, 16>(S, aK, kLd, aUh, kLd, sm0, 0, kChunk);
+      mm::warp_mma<true, false, 16>(S, aK, kLd, aUl, kLd, sm0, 0, kChunk);
+      bc_store_split<16>(S, sSh, sSl, kLd, sm0, 0);
+    }
+    __syncthreads();
+  }
+}
+
+// ---- reverse chain: every chunk's dS_end and du', and dV ----------------------------
+// One CTA per (sequence, v-head), walking the chunks from the last; dS lives in fp32
+// registers like the forward chain's state. It needs no forward state.
+constexpr int kDStatesSmem = 4 * kTile128 + 3 * kTile64 + 2 * kTileState + 2 * kTile128;
+
+__global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const BwdChunkParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __half* sQ = reinterpret_cast<__half*>(smem);
+  __half* sK = sQ + kChunk * kLd;
+  __half* sDO = sK + kChunk * kLd;
+  __half* sDOs = sDO + kChunk * kLd;  // Gamma dO / sqrt(dk)
+  __half* sTh = sDOs + kChunk * kLd;
+  __half* sTl = sTh + kChunk * kLd64;
+  __half* sA = sTl + kChunk * kLd64;  // (Q K^T . M) / sqrt(dk)
+  __half* sDSh = sA + kChunk * kLd64;
+  __half* sDSl = sDSh + kDim * kLd;
+  __half* sDUh = sDSl + kDim * kLd;  // du, then -Gamma r
+  __half* sDUl = sDUh + kChunk * kLd;
+  __shared__ float s_b[kChunk], s_beta[kChunk], s_sc[kChunk];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  const int si = blockIdx.x / p.nv, h = blockIdx.x % p.nv, kh = h / (p.nv / p.nk);
+  const int s = p.order ? p.order[si] : si;
+  int64_t row0, len;
+  if (!bc_sequence(p, s, row0, len)) return;
+  const int64_t nch = (len + kChunk - 1) / kChunk;
+  const int64_t hrow = static_cast<int64_t>(p.nv) * kDim;
+  const int sm0 = 16 * warp;
+  const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);  // 64 x 128 products
+  const int an0 = 32 * (warp >> 2);                        // 64 x 64 products
+  const uint32_t aQ = mm::saddr(sQ), aK = mm::saddr(sK), aDO = mm::saddr(sDO), aDOs = mm::saddr(sDOs),
+                 aTh = mm::saddr(sTh), aTl = mm::saddr(sTl), aA = mm::saddr(sA), aDSh = mm::saddr(sDSh),
+                 aDSl = mm::saddr(sDSl), aDUh = mm::saddr(sDUh), aDUl = mm::saddr(sDUl);
+
+  float dS[16][4];
+  {
+    const float* d0 = p.dst ? p.dst + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim : nullptr;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float2 x = make_float2(0.f, 0.f);
+        if (d0) x = *reinterpret_cast<const float2*>(d0 + (sm0 + gq + 8 * e) * kDim + 8 * j + 2 * tq);
+        dS[j][2 * e] = x.x;
+        dS[j][2 * e + 1] = x.y;
+      }
+  }
+  bc_store_split<16>(dS, sDSh, sDSl, kLd, sm0, 0);
+  __syncthreads();
+
+  for (int64_t c = nch - 1; c >= 0; --c) {
+    const int64_t r0 = row0 + c * kChunk;
+    const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
+    bc_store_state(p.dsbuf + (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim, sDSh);
+    if (warp == 0) {
+      bc_gates(p, r0, n, h, s_b, s_beta);
+      __syncwarp();
+      s_sc[2 * lane] = __expf(s_b[2 * lane]) * kInvSqrtD;
+      s_sc[2 * lane + 1] = __expf(s_b[2 * lane + 1]) * kInvSqrtD;
+    }
+    bc_load_bf16(sQ, p.q + r0 * p.q_stride + kh * kDim, p.q_stride, n);
+    bc_load_bf16(sK, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
+    bc_load_f32(sDO, p.dout + r0 * hrow + h * kDim, hrow, n, nullptr);
+    bc_load_t(sTh, sTl, p.tm + r0 * hrow + h * kDim, hrow, n);
+    __syncthreads();
+    bc_load_f32(sDOs, p.dout + r0 * hrow + h * kDim, hrow, n, s_sc);
+
+    // (Q K^T . M) / sqrt(dk), lower triangle with the diagonal
+    {
+      float acc[4][4];
+      mm::zero(acc);
+      mm::warp_mma<false, true, 4>(acc, aQ, kLd, aK, kLd, m0, an0, kDim);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = m0 + gq + 8 * e;
+        const float bt = s_b[t];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int jj = an0 + 8 * j + 2 * tq;
+          const float x0 = jj <= t ? acc[j][2 * e] * __expf(bt - s_b[jj]) * kInvSqrtD : 0.f;
+          const float x1 = jj + 1 <= t ? acc[j][2 * e + 1] * __expf(bt - s_b[jj + 1]) * kInvSqrtD : 0.f;
+          *reinterpret_cast<__half2*>(sA + t * kLd64 + jj) = __floats2half2_rn(x0, x1);
+        }
+      }
+    }
+    __syncthreads();
+
+    // du = A~^T dO + (gamma / Gamma) K dS, as fp16 hi + lo
+    {
+      float a1[8][4], a2[8][4];
+      mm::zero(a1);
+      mm::zero(a2);
+      mm::warp_mma<true, false, 8>(a1, aA, kLd64, aDO, kLd, m0, n0, kChunk);
+      mm::warp_mma<false, false, 8>(a2, aK, kLd, aDSh, kLd, m0, n0, kDim);
+      mm::warp_mma<false, false, 8>(a2, aK, kLd, aDSl, kLd, m0, n0, kDim);
+      const float blast = s_b[kChunk - 1];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float sc = __expf(blast - s_b[m0 + gq + 8 * e]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          a1[j][2 * e] = fmaf(sc, a2[j][2 * e], a1[j][2 * e]);
+          a1[j][2 * e + 1] = fmaf(sc, a2[j][2 * e + 1], a1[j][2 * e + 1]);
+        }
+      }
+      bc_store_split<8>(a1, sDUh, sDUl, kLd, m0, n0);
+    }
+    __syncthreads();
+
+    // du' = T^T du (stored), dV = beta du', then -Gamma beta du' as fp16 hi + lo
+    {
+      float acc[8][4];
+      mm::zero(acc);
+      mm::warp_mma<true, false, 8>(acc, aTh, kLd64, aDUh, kLd, m0, n0, kChunk);
+      mm::warp_mma<true, false, 8>(acc, aTh, kLd64, aDUl, kLd, m0, n0, kChunk);
+      mm::warp_mma<true, false, 8>(acc, aTl, kLd64, aDUh, kLd, m0, n0, kChunk);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = m0 + gq + 8 * e;
+        if (t < n) {
+          const float bt = s_beta[t];
+          __half* drow = p.dubuf + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+          float* vrow = p.dv + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            *reinterpret_cast<__half2*>(drow + 8 * j) = __floats2half2_rn(acc[j][2 * e], acc[j][2 * e + 1]);
+            *reinterpret_cast<float2*>(vrow + 8 * j) = make_float2(bt * acc[j][2 * e], bt * acc[j][2 * e + 1]);
+          }
+        }
+      }
+      __syncthreads();  // every warp has read du
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = m0 + gq + 8 * e;
+        const float sc = -__expf(s_b[t]) * s_beta[t];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          acc[j][2 * e] *= sc;
+          acc[j][2 * e + 1] *= sc;
+        }
+      }
+      bc_store_split<8>(acc, sDUh, sDUl, kLd, m0, n0);
+    }
+    __syncthreads();
+
+    // dS = gamma dS + Q^T (Gamma dO / sqrt(dk)) - K^T (Gamma r)
+    {
+      const float gam = __expf(s_b[kChunk - 1]);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+#pragma unroll
+        for (int x = 0; x < 4; ++x) dS[j][x] *= gam;
+      mm::warp_mma<true, false, 16>(dS, aQ, kLd, aDOs, kLd, sm0, 0, kChunk);
+      mm::warp_mma<true, false, 16>(dS, aK, kLd, aDUh, kLd, sm0, 0, kChunk);
+      mm::warp_mma<true, false, 16>(dS, aK, kLd, aDUl, kLd, sm0, 0, kChunk);
+      bc_store_split<16>(dS, sDSh, sDSl, kLd, sm0, 0);
+    }
+    __syncthreads();
+  }
+  if (p.dh0) {
+    float* d = p.dh0 + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        *reinterpret_cast<float2*>(d + (sm0 + gq + 8 * e) * kDim + 8 * j + 2 * tq) =
+            make_float2(dS[j][2 * e], dS[j][2 * e + 1]);
+  }
+}
+
+// ---- per-chunk gradients ----------------------------------------------------------
+// One CTA per (chunk, v-head), items head-fastest so the v-heads of a GQA group read
+// their chunk's q and k tiles close together in time.
+constexpr int kGradsSmem = 5 * kTile128 + kTileState + 2 * kTile64;
+
+// Sums of a fragment row pair over the 4 lanes of a quad (lanes 4g .. 4g + 3).
+__device__ __forceinline__ float bc_quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
+// Sum over the 8 quads (lanes t, t + 4, ..., t + 28).
+__device__ __forceinline__ float bc_column_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 4);
+  x += __shfl_xor_sync(0xffffffffu, x, 8);
+  return x + __shfl_xor_sync(0xffffffffu, x, 16);
+}
+
+__global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdChunkParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __half* sQ = reinterpret_cast<__half*>(smem);
+  __half* sK = sQ + kChunk * kLd;
+  __half* sDO = sK + kChunk * kLd;
+  __half* sU = sDO + kChunk * kLd;
+  __half* sDU = sU + kChunk * kLd;  // du'
+  __half* sS = sDU + kChunk * kLd;  // S0, then dS_end
+  __half* sP0 = sS + kDim * kLd;    // dA = lower(dO u^T) . M / sqrt(dk)
+  __half* sP1 = sP0 + kChunk * kLd64;  // E = beta F
+  __shared__ float s_b[kChunk], s_beta[kChunk];
+  // per-token partial sums: q.(dO S0^T), k.P, rows/columns of dA . QK^T and of E . G,
+  // rows of F . G, w, du'.v
+  __shared__ float s_rq[kChunk], s_rkp[kChunk], s_r1[kChunk], s_c1[kChunk], s_r2[kChunk], s_c2[kChunk],
+      s_rf[kChunk], s_rw[kChunk], s_rdv[kChunk];
+  __shared__ float s_dot;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
+  const int ci = blockIdx.x / p.nv, h = blockIdx.x % p.nv, kh = h / (p.nv / p.nk);
+  int s;
+  int64_t c;
+  if (p.cu_seqlens) {
+    if (ci >= p.cu_chunks[p.B]) return;
+    int lo = 0, hi = p.B - 1;  // the sequence with cu_chunks[s] <= ci < cu_chunks[s + 1]
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.cu_chunks[mid] <= ci) lo = mid;
+      else hi = mid - 1;
+    }
+    s = lo;
+    c = ci - p.cu_chunks[s];
+  } else {
+    const int nch = (p.T + kChunk - 1) / kChunk;
+    s = ci / nch;
+    c = ci % nch;
+    if (s >= p.B) return;
+  }
+  int64_t row0, len;
+  if (!bc_sequence(p, s, row0, len)) return;
+  const int64_t r0 = row0 + c * kChunk;
+  if (c * kChunk >= len) return;
+  const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
+  const int64_t hrow = static_cast<int64_t>(p.nv) * kDim;
+  const int64_t state_off = (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim;
+  const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2), an0 = 32 * (warp >> 2);
+  const uint32_t aQ = mm::saddr(sQ), aK = mm::saddr(sK), aDO = mm::saddr(sDO), aU = mm::saddr(sU),
+                 aDU = mm::saddr(sDU), aS = mm::saddr(sS), aP0 = mm::saddr(sP0), aP1 = mm::saddr(sP1);
+
+  if (tid < kChunk) {
+    s_rq[tid] = s_rkp[tid] = s_r1[tid] = s_c1[tid] = s_r2[tid] = s_c2[tid] = s_rf[tid] = s_rw[tid] = 0.f;
+    if (tid == 0) s_dot = 0.f;
+  }
+  if (warp == 0) bc_gates(p, r0, n, h, s_b, s_beta);
+  bc_load_bf16(sQ, p.q + r0 * p.q_stride + kh * kDim, p.q_stride, n);
+  bc_load_bf16(sK, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
+  bc_load_f32(sDO, p.dout + r0 * hrow + h * kDim, hrow, n, nullptr);
+  bc_load_half(sU, p.ubuf + r0 * hrow + h * kDim, hrow, n);
+  bc_load_half(sDU, p.dubuf + r0 * hrow + h * kDim, hrow, n);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = tid + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+    *reinterpret_cast<uint4*>(sS + row * kLd + 8 * c8) =
+        __ldg(reinterpret_cast<const uint4*>(p.s0buf + state_off + row * kDim) + c8);
+  }
+  __syncthreads();
+
+  // dQ <- Gamma dO S0^T / sqrt(dk), dK <- -Gamma beta P with P = du' S0^T
+  float dQ[8][4], dK[8][4];
+  mm::zero(dQ);
+  mm::zero(dK);
+  mm::warp_mma<false, true, 8>(dQ, aDO, kLd, aS, kLd, m0, n0, kDim);
+  mm::warp_mma<false, true, 8>(dK, aDU, kLd, aS, kLd, m0, n0, kDim);
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int t = m0 + gq + 8 * e;
+    float sq = 0.f, sk = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int col = n0 + 8 * j + 2 * tq;
+      const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(sQ + t * kLd + col));
+      const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + col));
+      sq = fmaf(q2.x, dQ[j][2 * e], fmaf(q2.y, dQ[j][2 * e + 1], sq));
+      sk = fmaf(k2.x, dK[j][2 * e], fmaf(k2.y, dK[j][2 * e + 1], sk));
+    }
+    sq = bc_quad_sum(sq);
+    sk = bc_quad_sum(sk);
+    if (tq == 0) {
+      atomicAdd(&s_rq[t], sq);
+      atomicAdd(&s_rkp[t], sk);
+    }
+    const float G = __expf(s_b[t]), fq = G * kInvSqrtD, fk = -G * s_beta[t];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      dQ[j][2 * e] *= fq;
+      dQ[j][2 * e + 1] *= fq;
+      dK[j][2 * e] *= fk;
+      dK[j][2 * e + 1] *= fk;
+    }
+  }
+  __syncthreads();  // every warp is done with S0
+
+  // dS_end over S0, accumulating <dS_end, S0>
+  {
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = tid + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+      uint4* dst = reinterpret_cast<uint4*>(sS + row * kLd + 8 * c8);
+      const uint4 old = *dst;
+      const uint4 nw = __ldg(reinterpret_cast<const uint4*>(p.dsbuf + state_off + row * kDim) + c8);
+      const __half2* a2 = reinterpret_cast<const __half2*>(&old);
+      const __half2* b2 = reinterpret_cast<const __half2*>(&nw);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const float2 fa = __half22float2(a2[x]), fb = __half22float2(b2[x]);
+        dot = fmaf(fa.x, fb.x, fmaf(fa.y, fb.y, dot));
+      }
+      *dst = nw;
+    }
+    dot = bc_column_sum(bc_quad_sum(dot));
+    if (lane == 0) atomicAdd(&s_dot, dot);
+  }
+
+  // dA = lower(dO u^T) . M / sqrt(dk) and the row/column sums of dA . (Q K^T)
+  {
+    float aA[4][4], aD[4][4], col[4][2];
+    mm::zero(aA);
+    mm::zero(aD);
+    mm::warp_mma<false, true, 4>(aA, aQ, kLd, aK, kLd, m0, an0, kDim);
+    mm::warp_mma<false, true, 4>(aD, aDO, kLd, aU, kLd, m0, an0, kDim);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) col[j][0] = col[j][1] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = m0 + gq + 8 * e;
+      const float bt = s_b[t];
+      float row = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const int jj = an0 + 8 * j + 2 * tq + x;
+          const float m = jj <= t ? __expf(bt - s_b[jj]) * kInvSqrtD : 0.f;
+          const float da = aD[j][2 * e + x] * m, y = da * aA[j][2 * e + x];
+          aD[j][2 * e + x] = da;
+          row += y;
+          col[j][x] += y;
+        }
+      row = bc_quad_sum(row);
+      if (tq == 0) atomicAdd(&s_r1[t], row);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const float v = bc_column_sum(col[j][x]);
+        if (gq == 0) atomicAdd(&s_c1[an0 + 8 * j + 2 * tq + x], v);
+      }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        *reinterpret_cast<__half2*>(sP0 + (m0 + gq + 8 * e) * kLd64 + an0 + 8 * j + 2 * tq) =
+            __floats2half2_rn(aD[j][2 * e], aD[j][2 * e + 1]);
+  }
+
+  // F = -strict_lower(du' u^T) . M, E = beta F; rows of F . G; rows/columns of E . G
+  {
+    float aG[4][4], aF[4][4], col[4][2];
+    mm::zero(aG);
+    mm::zero(aF);
+    mm::warp_mma<false, true, 4>(aG, aK, kLd, aK, kLd, m0, an0, kDim);
+    mm::warp_mma<false, true, 4>(aF, aDU, kLd, aU, kLd, m0, an0, kDim);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) col[j][0] = col[j][1] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = m0 + gq + 8 * e;
+      const float bt = s_b[t], be = s_beta[t];
+      float rf = 0.f, rz = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const int jj = an0 + 8 * j + 2 * tq + x;
+          const float m = jj < t ? __expf(bt - s_b[jj]) : 0.f;
+          const float f = -aF[j][2 * e + x] * m, gv = aG[j][2 * e + x], ee = be * f, z = ee * gv;
+          aF[j][2 * e + x] = ee;
+          rf = fmaf(f, gv, rf);
+          rz += z;
+          col[j][x] += z;
+        }
+      rf = bc_quad_sum(rf);
+      rz = bc_quad_sum(rz);
+      if (tq == 0) {
+        atomicAdd(&s_rf[t], rf);
+        atomicAdd(&s_r2[t], rz);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const float v = bc_column_sum(col[j][x]);
+        if (gq == 0) atomicAdd(&s_c2[an0 + 8 * j + 2 * tq + x], v);
+      }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        *reinterpret_cast<__half2*>(sP1 + (m0 + gq + 8 * e) * kLd64 + an0 + 8 * j + 2 * tq) =
+            __floats2half2_rn(aF[j][2 * e], aF[j][2 * e + 1]);
+  }
+  __syncthreads();  // dA, E and dS_end are in shared memory
+
+  // dQ += dA K; dK += E K + E^T K + dA^T Q + (gamma / Gamma) u dS_end^T
+  mm::warp_mma<false, false, 8>(dQ, aP0, kLd64, aK, kLd, m0, n0, kChunk);
+  mm::warp_mma<false, false, 8>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
+  mm::warp_mma<true, false, 8>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
+  mm::warp_mma<true, false, 8>(dK, aP0, kLd64, aQ, kLd, m0, n0, kChunk);
+  {
+    float uD[8][4];
+    mm::zero(uD);
+    mm::warp_mma<false, true, 8>(uD, aU, kLd, aS, kLd, m0, n0, kDim);
+    const float blast = s_b[kChunk - 1];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = m0 + gq + 8 * e;
+      const float sc = __expf(blast - s_b[t]);
+      float rw = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int colx = n0 + 8 * j + 2 * tq;
+        const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + colx));
+        const float a = sc * uD[j][2 * e], b = sc * uD[j][2 * e + 1];
+        dK[j][2 * e] += a;
+        dK[j][2 * e + 1] += b;
+        rw = fmaf(k2.x, a, fmaf(k2.y, b, rw));
+      }
+      rw = bc_quad_sum(rw);
+      if (tq == 0) atomicAdd(&s_rw[t], rw);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int t = m0 + gq + 8 * e;
+    if (t < n) {
+      float* qrow = p.dq_part + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+      float* krow = p.dk_part + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        *reinterpret_cast<float2*>(qrow + 8 * j) = make_float2(dQ[j][2 * e], dQ[j][2 * e + 1]);
+        *reinterpret_cast<float2*>(krow + 8 * j) = make_float2(dK[j][2 * e], dK[j][2 * e + 1]);
+      }
+    }
+  }
+  // du'_t . v_t: four threads per token, 32 columns each
+  {
+    const int t = tid >> 2, qq = tid & 3;
+    float d = 0.f;
+    if (t < n) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float vf[8];
+        unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.v + (r0 + t) * p.v_stride + h * kDim + 32 * qq) + i), vf);
+        const uint4 draw = *reinterpret_cast<const uint4*>(sDU + t * kLd + 32 * qq + 8 * i);
+        const __half2* d2 = reinterpret_cast<const __half2*>(&draw);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float2 f = __half22float2(d2[x]);
+          d = fmaf(f.x, vf[2 * x], fmaf(f.y, vf[2 * x + 1], d));
+        }
+      }
+    }
+    d = bc_quad_sum(d);
+    if (qq == 0) s_rdv[t] = d;
+  }
+  __syncthreads();
+
+  // per-token dbeta and d b, then dg = suffix sums of d b over the chunk (warp 0)
+  if (warp == 0) {
+    const float gam = __expf(s_b[kChunk - 1]);
+    float wsum = s_rw[2 * lane] + s_rw[2 * lane + 1];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    float db[2], dbe[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const int t = 2 * lane + x;
+      const float G = __expf(s_b[t]);
+      db[x] = G * kInvSqrtD * s_rq[t] - G * s_beta[t] * s_rkp[t] + (s_r2[t] - s_c2[t]) + (s_r1[t] - s_c1[t]) -
+              s_rw[t];
+      dbe[x] = s_rdv[t] - G * s_rkp[t] + s_rf[t];
+    }
+    if (lane == 31) db[1] += gam * s_dot + wsum;
+    // suffix sums over the token pairs of the lanes
+    const float pair = db[0] + db[1];
+    float incl = pair;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    const float dg0 = incl, dg1 = incl - db[0];
+    const int t0 = 2 * lane, t1 = t0 + 1;
+    if (t0 < n) {
+      p.dg[(r0 + t0) * p.nv + h] = dg0;
+      p.dbeta[(r0 + t0) * p.nv + h] = dbe[0];
+    }
+    if (t1 < n) {
+      p.dg[(r0 + t1) * p.nv + h] = dg1;
+      p.dbeta[(r0 + t1) * p.nv + h] = dbe[1];
+    }
+  }
+}
+
+// dq[r][kh] and dk[r][kh]: the per-v-head parts summed over the value heads of key head kh.
+__global__ void gdn_bwd_reduce_kernel(const BwdChunkParams p, float* dq, float* dk, int64_t rows) {
+  const int group = p.nv / p.nk;
+  const int64_t n4 = rows * p.nk * (kDim / 4);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const int64_t r = i / (static_cast<int64_t>(p.nk) * (kDim / 4));
+    const int rem = static_cast<int>(i % (static_cast<int64_t>(p.nk) * (kDim / 4)));
+    const int kh = rem / (kDim / 4), e4 = rem % (kDim / 4);
+    float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
+    for (int j = 0; j < group; ++j) {
+      const int64_t o = (r * p.nv + kh * group + j) * kDim + 4 * e4;
+      const float4 a = *reinterpret_cast<const float4*>(p.dq_part + o);
+      const float4 b = *reinterpret_cast<const float4*>(p.dk_part + o);
+      sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
+      sk.x += b.x; sk.y += b.y; sk.z += b.z; sk.w += b.w;
+    }
+    reinterpret_cast<float4*>(dq)[i] = sq;
+    reinterpret_cast<float4*>(dk)[i] = sk;
+  }
+}
+
+}  // namespace gdn

@@ -16,7 +16,8 @@
 //
 // and writes T diag(beta) as an fp16 hi + lo pair (about 22 significant bits)
 // for the spine kernel, which forms U = (T diag beta) V and
-// W = (T diag beta) diag(e^gc) K on the tensor cores.
+// W = (T diag beta) diag(e^gc) K on the tensor cores. For the backward it
+// writes T itself (t_only), into a scratch buffer of the same row layout.
 //
 // Hand-off: row t of a chunk's T diag(beta) (64 hi then 64 lo fp16 values,
 // 256 bytes) is written over the output slice of the same token and head,
@@ -48,6 +49,7 @@ struct WyParams {
   int B, T, nk, nv;
   int chunks_per_seq;         // dense batches: ceil(T / 64)
   int qk_l2norm;              // fused prologue: normalise every key row first
+  int t_only;                 // write T itself instead of T diag(beta) (the backward's operand)
 };
 
 // Operand tiles of the final merge are 16-bit, 128-byte-swizzled rows (see
@@ -511,8 +513,9 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
           const int jb = j0 + q8 * 8;
           const float4 ta = *reinterpret_cast<const float4*>(lf + lf_idx(t, jb));
           const float4 tb = *reinterpret_cast<const float4*>(lf + lf_idx(t, jb + 4));
-          const float4 ba = *reinterpret_cast<const float4*>(s_beta + jb);
-          const float4 bb = *reinterpret_cast<const float4*>(s_beta + jb + 4);
+          float4 ba = *reinterpret_cast<const float4*>(s_beta + jb);
+          float4 bb = *reinterpret_cast<const float4*>(s_beta + jb + 4);
+          if (p.t_only) ba = bb = make_float4(1.f, 1.f, 1.f, 1.f);
           uint32_t hi[4], lo[4];
           split_half2(ta.x * ba.x, ta.y * ba.y, hi[0], lo[0]);
           split_half2(ta.z * ba.z, ta.w * ba.w, hi[1], lo[1]);

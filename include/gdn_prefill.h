@@ -185,9 +185,13 @@ void gdn_set_timing_events(void* before_wy, void* before_spine, void* after_spin
 /* Backward of the prefill (the training pass): gradients of a loss L with
  * respect to every input of the recurrence S_t = e^{g_t}(I - beta_t k_t k_t^T)
  * S_{t-1} + beta_t k_t v_t^T, o_t = S_t^T q_t / sqrt(dk) (the forward of
- * ssm_gdn_a3.rs `gdn_prefill_fla`), given dL/do and dL/dS_T. Computed token by
- * token in reverse in fp32 on the CUDA cores; the states are recomputed from the
- * inputs and h0 (stored every 64 tokens), so the forward's outputs are not needed.
+ * ssm_gdn_a3.rs `gdn_prefill_fla`), given dL/do and dL/dS_T. Computed in the
+ * same chunked form as the forward: the per-chunk WY inverse T, a forward chain
+ * storing each chunk's entry state, a reverse chain storing each chunk's state
+ * gradient, and the per-chunk gradients, all on the tensor cores (fp16 operands,
+ * fp32 accumulation, fp32 chain states). The forward's outputs are not needed.
+ * Enqueues 5 kernels (6 with cu_seqlens). Scratch: about 10 bytes per (row,
+ * v-head, column) plus 64 KB per (64-row chunk, v-head).
  *   q, k, v, g, beta, strides, cu_seqlens, B, T, nk, nv, dk, dv: as gdn_prefill
  *             (qk_l2norm must be 0: pass the normalised q and k).
  *   h0     : the INITIAL state (gdn_prefill updates its state in place, so keep a
@@ -201,7 +205,7 @@ void gdn_set_timing_events(void* before_wy, void* before_spine, void* after_spin
  *   of the rejected sequences hold unspecified values and the status word says so.)
  *   workspace : device scratch of gdn_prefill_backward_workspace_bytes(...) bytes,
  *            256-byte aligned, or NULL to allocate it stream-ordered.
- * dv, dST and dh0 must be 16-byte aligned. Returns GDN_OK or an error code. */
+ * dq, dk, dv, dST and dh0 must be 16-byte aligned. Returns GDN_OK or an error code. */
 size_t gdn_prefill_backward_workspace_bytes(int B, int T, int nv, int dk, int dv, int varlen);
 int gdn_prefill_backward(const void* q, const void* k, const void* v, const float* g, const float* beta,
                          const void* h0, const float* dout, const float* dST, float* dq, float* dk, float* dv,

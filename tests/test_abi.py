@@ -143,20 +143,23 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 
 def test_backward_workspace_sizes(lib):
-    # column-split parts of dq, dk (rows x nv x 4 x 128 fp32 each) and of dg, dbeta
-    # (rows x nv x 4), a state per 64 rows per head (plus B + 1), and a 65-block slot of
-    # 128 x 32 floats per persistent CTA (min(B * nv * 4, 3 * SMs); 152 SMs without a
-    # visible GPU)
+    # varlen schedule (2B + 1 int32), then T, u and du' (16-bit, rows x nv x 128 each),
+    # each chunk slot's S0 and dS_end (fp16 128 x 128 per head, rows / 64 + B + 1
+    # slots), and the per-v-head dq and dk parts (fp32, rows x nv x 128 each)
     def a256(x):
         return (x + 255) // 256 * 256
 
-    state = 128 * 128 * 4
-    B, T, nv = 1, 4096, 32
-    part = B * T * nv * 4
-    off = a256(part * 128 * 4)
-    off = a256(off + part * 128 * 4)
-    off = a256(off + part * 4)
-    off = a256(off + part * 4)
-    off = a256(off + (B * T // 64 + B + 1) * nv * state)
-    assert lib.gdn_prefill_backward_workspace_bytes(B, T, nv, 128, 128, 0) == off + 128 * 65 * 128 * 32 * 4
+    for B, T, nv, varlen in ((1, 4096, 32, 0), (3, 1000, 8, 1)):
+        rows = T if varlen else B * T
+        row16 = rows * nv * 128 * 2
+        state16 = (rows // 64 + B + 1) * nv * 128 * 128 * 2
+        off = a256((2 * B + 1) * 4 if varlen else 0)
+        off = a256(off + row16)
+        off = a256(off + row16)
+        off = a256(off + row16)
+        off = a256(off + state16)
+        off = a256(off + state16)
+        off = a256(off + 2 * row16)
+        off = a256(off + 2 * row16)
+        assert lib.gdn_prefill_backward_workspace_bytes(B, T, nv, 128, 128, varlen) == off
     assert lib.gdn_prefill_backward_workspace_bytes(0, T, nv, 128, 128, 0) == 0

@@ -1,8 +1,11 @@
-"""GPU parity of the backward (gdn_prefill_backward) against the oracle's fp64
-backward (itself pinned by finite differences): every gradient -- q, k, v, g,
-beta and the initial state -- on dense GQA batches with and without a final-state
-cotangent, sequences spanning several 64-token recompute blocks with a ragged
-tail, a varlen batch with an empty sequence and a state table, and nk = nv."""
+"""GPU parity of the chunked backward (gdn_prefill_backward) against the oracle's
+fp64 token-by-token backward (itself pinned by finite differences): every
+gradient -- q, k, v, g, beta and the initial state -- on dense GQA batches with
+and without a final-state cotangent, sequences of many chunks with a ragged last
+chunk, weak decay over long sequences (where errors would build up along both
+chains), a varlen batch with an empty sequence and a state table, nk = nv, more
+(sequence, head) chains than SMs, and one key-head group of the benchmark
+workload."""
 import numpy as np
 import pytest
 
@@ -13,7 +16,10 @@ from tests.gpu_helpers import to_torch_bf16
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
-REL_L2 = 2e-3  # fp32 accumulation over up to ~1000 reverse steps from bf16 inputs
+# fp16 tensor-core operands (2^-11 relative rounding) for every contraction; the two
+# chains carry fp32 states split into fp16 hi + lo. Each gradient is a sum of a few
+# such products, so errors of a few 1e-4 are expected; the bound leaves margin.
+REL_L2 = 3e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -55,17 +61,20 @@ def run_backward(p, seed, with_dst=True, state_table=False, workspace=True):
                  state_is_table=state_table, workspace=ws)
     torch.cuda.synchronize()
     gdn.check()
-    assert gdn.last_launch_count() == 2
+    assert gdn.last_launch_count() == (6 if p.varlen else 5)
     ref = oracle.token_loop_backward(p, dout.astype(np.float64), None if dst is None else dst.astype(np.float64))
     return {n: t.cpu().numpy().astype(np.float64) for n, t in out.items()}, ref
 
 
 def assert_grads(got, ref, label):
+    rels = {}
     for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
         a = got[name].reshape(-1)
         b = ref[name].reshape(-1)
         assert np.isfinite(a).all(), f"{label}: {name} has non-finite values"
-        rel = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+        rels[name] = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+    print(f"{label}: " + " ".join(f"{n} {r:.2e}" for n, r in rels.items()))
+    for name, rel in rels.items():
         assert rel <= REL_L2, f"{label}: {name} rel L2 {rel:.3e}"
 
 
@@ -101,15 +110,56 @@ def test_backward_one_head_per_key():
     assert_grads(got, ref, "nk = nv")
 
 
-@pytest.mark.parametrize("B,cols", [(4, 2), (5, 4)])
-def test_backward_wide_batches_use_wider_column_blocks(B, cols):
-    # 128 chains take 2 CTAs of 64 columns per (sequence, head), 160 chains one CTA of
-    # 128 columns (the kernel variants with 2 and 4 columns per thread); a ragged last
-    # recompute block
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    chains = B * 32
-    expect = 1 if chains * 4 <= 3 * sms else (2 if chains * 2 <= 2 * sms else 4)
-    assert expect == cols, "the case must select the intended variant on this device"
+@pytest.mark.parametrize("B", [4, 5])
+def test_backward_many_chains(B):
+    # 128 and 160 (sequence, head) chains (more than the SMs: a second wave) of 70 tokens
     p = gdn_synth.make_problem(seed=8600 + B, B=B, T=70, nk=16, nv=32, h0_std=0.02)
     got, ref = run_backward(p, 8600 + B)
-    assert_grads(got, ref, f"B={B} nv=32 ({cols} columns per thread)")
+    assert_grads(got, ref, f"B={B} nv=32")
+
+
+def test_backward_weak_decay_long():
+    # 2000 tokens (32 chunks) with gates near zero: both chains carry their state far
+    p = gdn_synth.make_problem(seed=8700, B=1, T=2000, nk=1, nv=2, h0_std=0.02, gate_mu=-5.0, gate_sigma=0.5)
+    got, ref = run_backward(p, 8700)
+    assert_grads(got, ref, "weak decay T=2000")
+
+
+def test_backward_benchmark_workload_one_key_head():
+    # The B=4 T=8192 nk=16 nv=32 workload through the launch configuration the benchmark
+    # times; the oracle runs one key head's group (its two value heads), which fixes
+    # dq and dk of that key head and every gradient of those value heads.
+    import gated_delta_rule_17_gb300 as gdn
+
+    p = gdn_synth.config_problem(2)
+    rng = np.random.default_rng(8800)
+    dout = rng.standard_normal((p.rows, p.nv, p.dv)).astype(np.float32)
+    dst = rng.standard_normal((p.B, p.nv, p.dk, p.dv)).astype(np.float32)
+    dev = "cuda"
+    q, k, v = (to_torch_bf16(x, dev) for x in (p.q, p.k, p.v))
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = {"dq": torch.empty((p.rows, p.nk * p.dk), **f32), "dk": torch.empty((p.rows, p.nk * p.dk), **f32),
+           "dv": torch.empty((p.rows, p.nv * p.dv), **f32), "dg": torch.empty((p.rows, p.nv), **f32),
+           "dbeta": torch.empty((p.rows, p.nv), **f32), "dh0": torch.empty((p.B, p.nv, p.dk, p.dv), **f32)}
+    gdn.backward(q, k, v, torch.from_numpy(p.g).to(dev), torch.from_numpy(p.beta).to(dev),
+                 torch.from_numpy(p.h0.copy()).to(dev), torch.from_numpy(dout.reshape(p.rows, -1)).to(dev),
+                 out["dq"], out["dk"], out["dv"], out["dg"], out["dbeta"], nk=p.nk, nv=p.nv, B=p.B, T=p.T,
+                 dST=torch.from_numpy(dst).to(dev), dh0=out["dh0"])
+    torch.cuda.synchronize()
+    gdn.check()
+    got = {n: t.cpu().numpy().astype(np.float64) for n, t in out.items()}
+    del out, q, k, v
+    kh, grp = 5, p.nv // p.nk
+    hs = slice(kh * grp, (kh + 1) * grp)
+    d = p.dk
+    sub = gdn_synth.Problem(B=p.B, T=p.T, nk=1, nv=grp, dk=d, dv=d,
+                            q=np.ascontiguousarray(p.q[:, kh * d:(kh + 1) * d]),
+                            k=np.ascontiguousarray(p.k[:, kh * d:(kh + 1) * d]),
+                            v=np.ascontiguousarray(p.v[:, hs.start * d:hs.stop * d]),
+                            g=np.ascontiguousarray(p.g[:, hs]), beta=np.ascontiguousarray(p.beta[:, hs]),
+                            h0=np.ascontiguousarray(p.h0[:, hs]))
+    ref = oracle.token_loop_backward(sub, dout[:, hs].astype(np.float64), dst[:, hs].astype(np.float64))
+    mine = {"dq": got["dq"][:, kh * d:(kh + 1) * d], "dk": got["dk"][:, kh * d:(kh + 1) * d],
+            "dv": got["dv"][:, hs.start * d:hs.stop * d], "dg": got["dg"][:, hs], "dbeta": got["dbeta"][:, hs],
+            "dh0": got["dh0"][:, hs]}
+    assert_grads(mine, ref, "B=4 T=8192 nv=32, key head 5")
