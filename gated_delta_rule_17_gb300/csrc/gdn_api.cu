@@ -546,10 +546,9 @@ int noalloc_scratch(int32_t** out) {
 // ---- backward -------------------------------------------------------------------
 // Scratch of the chunked backward: the varlen schedule; T (16-bit, rows x nv x 128),
 // u and du' (fp16, same shape); each chunk's S0 and dS_end (fp16 128 x 128 per
-// (chunk slot, v-head), rows / 64 + B + 1 slots); the per-v-head dq and dk parts
-// (fp32, rows x nv x 128 each).
+// (chunk slot, v-head), rows / 64 + B + 1 slots).
 struct BwdLayout {
-  size_t sched = 0, tm = 0, u = 0, du = 0, s0 = 0, ds = 0, dq = 0, dk = 0, total = 0;
+  size_t sched = 0, tm = 0, u = 0, du = 0, s0 = 0, ds = 0, total = 0;
 };
 
 BwdLayout bwd_layout(int B, int T, int nv, int varlen) {
@@ -564,9 +563,7 @@ BwdLayout bwd_layout(int B, int T, int nv, int varlen) {
   l.du = align256(l.u + row16);
   l.s0 = align256(l.du + row16);
   l.ds = align256(l.s0 + state16);
-  l.dq = align256(l.ds + state16);
-  l.dk = align256(l.dq + 2 * row16);
-  l.total = align256(l.dk + 2 * row16);
+  l.total = align256(l.ds + state16);
   return l;
 }
 
@@ -749,7 +746,8 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   gdn::WyParams w;
   int64_t wy_grid = 0;
   if (int rc = wy_geometry(*d, B, T, nv, cu_seqlens != nullptr, &w.items, &wy_grid)) return rc;
-  const int64_t grad_items = static_cast<int64_t>(w.items);  // (chunk, v-head) items, same bound
+  // (chunk, key head) items: the WY kernel's chunk count (or its varlen bound) times nk
+  const int64_t grad_items = static_cast<int64_t>(w.items) / nv * nk;
   if (static_cast<int64_t>(B) * nv > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "too many (sequence, head) chains");
   void* ws = workspace;
   if (ws) {
@@ -796,8 +794,8 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   p.dubuf = reinterpret_cast<__half*>(w8 + l.du);
   p.s0buf = reinterpret_cast<__half*>(w8 + l.s0);
   p.dsbuf = reinterpret_cast<__half*>(w8 + l.ds);
-  p.dq_part = reinterpret_cast<float*>(w8 + l.dq);
-  p.dk_part = reinterpret_cast<float*>(w8 + l.dk);
+  p.dq = dq;
+  p.dk = dk;
   p.dv = dv;
   p.dg = dg;
   p.dbeta = dbeta;
@@ -816,7 +814,6 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   p.nk = nk;
   p.nv = nv;
   p.state_is_table = r.table;
-  p.items = static_cast<int>(grad_items);
 
   int launches = 0;
   if (cu_seqlens) {
@@ -828,8 +825,7 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   gdn::gdn_bwd_states_kernel<<<chains, gdn::kBcThreads, gdn::kStatesSmem, s>>>(p);
   gdn::gdn_bwd_dstates_kernel<<<chains, gdn::kBcThreads, gdn::kDStatesSmem, s>>>(p);
   gdn::gdn_bwd_grads_kernel<<<static_cast<unsigned>(grad_items), gdn::kBcThreads, gdn::kGradsSmem, s>>>(p);
-  gdn::gdn_bwd_reduce_kernel<<<static_cast<unsigned>(d->sms * 4), 256, 0, s>>>(p, dq, dk, rows);
-  launches += 5;
+  launches += 4;
   int rc = GDN_OK;
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) rc = fail(GDN_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));

@@ -34,8 +34,8 @@
 // Three kernels: gdn_bwd_states_kernel runs the forward chain once per (sequence,
 // v-head), storing every chunk's entry state S0 and u; gdn_bwd_dstates_kernel runs
 // the reverse chain, storing every chunk's dS_end and du' and writing dV;
-// gdn_bwd_grads_kernel takes one (chunk, v-head) each and writes dQ, dK (per
-// v-head, summed over each GQA group by gdn_bwd_reduce_kernel), dbeta and dg.
+// gdn_bwd_grads_kernel takes one (chunk, key head) each and writes dQ, dK (summed
+// over the key head's GQA group of value heads), and dbeta and dg of every value head.
 // T comes from the forward's WY kernel (unscaled by beta). Every contraction is an
 // fp16 tensor-core product with fp32 accumulation (gdn_mma.cuh); the two chains
 // carry their state in fp32 registers and feed it to the tensor cores as an fp16
@@ -71,8 +71,8 @@ struct BwdChunkParams {
   __half* dubuf;       // [rows][nv][128]: du' = T^T du
   __half* s0buf;       // [slots][nv][128][128]: each chunk's entry state S0 ([k][v])
   __half* dsbuf;       // [slots][nv][128][128]: each chunk's dS_end ([k][v])
-  float* dq_part;      // [rows][nv][128]
-  float* dk_part;      // [rows][nv][128]
+  float* dq;           // [rows][nk][128]
+  float* dk;           // [rows][nk][128]
   float* dv;           // [rows][nv][128]
   float* dg;           // [rows][nv]
   float* dbeta;        // [rows][nv]
@@ -84,7 +84,6 @@ struct BwdChunkParams {
   int64_t q_stride, k_stride, v_stride, g_stride, beta_stride;
   int B, T, nk, nv;
   int state_is_table;
-  int items;  // gdn_bwd_grads_kernel: (chunk, v-head) items, an upper bound for varlen
 };
 
 // Rows of sequence s; false (and the status bit) for an invalid cu_seqlens entry.
@@ -108,73 +107,106 @@ __device__ __forceinline__ bool bc_sequence(const BwdChunkParams& p, int s, int6
 // chunks of sequence s occupy row0 / 64 + s + [0, chunks)).
 __device__ __forceinline__ int64_t bc_slot(int64_t row0, int s, int64_t c) { return row0 / kChunk + s + c; }
 
-// 64 x 128 bf16 rows (row stride in elements) -> fp16 tile; rows >= n are zero.
-__device__ __forceinline__ void bc_load_bf16(__half* dst, const __nv_bfloat16* src, int64_t stride, int n) {
+// A chunk's global rows are fetched into registers (all loads of a chunk in flight at
+// once, while the previous chunk computes) and put into shared memory afterwards.
+// Thread tid holds the 16-byte pieces tid + 256 i of a 64 x 128 tile of 16-bit values
+// (row = piece / 16) or of fp32 values (row = piece / 32); rows past the chunk's end
+// are zero.
+struct BcRows16 {
+  uint4 x[4];
+};
+struct BcRows32 {
+  float4 x[8];
+};
+struct BcGates {
+  float g0, g1, b0, b1;  // g and beta of tokens 2 lane and 2 lane + 1
+};
+
+__device__ __forceinline__ void bc_fetch16(BcRows16& r, const void* src, int64_t stride, int n) {
+  const uint16_t* s16 = static_cast<const uint16_t*>(src);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (row < n) {
-      float f[8];
-      unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(src + row * stride) + c8), f);
-      o = pack_half8(f, 1.f);
-    }
-    *reinterpret_cast<uint4*>(dst + row * kLd + 8 * c8) = o;
+    r.x[i] = row < n ? __ldg(reinterpret_cast<const uint4*>(s16 + row * stride) + c8) : make_uint4(0, 0, 0, 0);
   }
 }
 
-// 64 x 128 fp16 rows of a [rows][nv][128] buffer -> tile; rows >= n are zero.
-__device__ __forceinline__ void bc_load_half(__half* dst, const __half* src, int64_t stride, int n) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (row < n) o = __ldg(reinterpret_cast<const uint4*>(src + row * stride) + c8);
-    *reinterpret_cast<uint4*>(dst + row * kLd + 8 * c8) = o;
-  }
-}
-
-// 64 x 128 fp32 rows of dO -> fp16 tile scaled by scale[row] (or 1); rows >= n are zero.
-__device__ __forceinline__ void bc_load_f32(__half* dst, const float* src, int64_t stride, int n,
-                                            const float* scale) {
+__device__ __forceinline__ void bc_fetch32(BcRows32& r, const float* src, int64_t stride, int n) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int idx = threadIdx.x + kBcThreads * i, row = idx >> 5, c4 = idx & 31;
-    uint2 o = make_uint2(0, 0);
-    if (row < n) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(src + row * stride) + c4);
-      const float s = scale ? scale[row] : 1.f;
-      o = make_uint2(pack_half2(x.x * s, x.y * s), pack_half2(x.z * s, x.w * s));
-    }
-    *reinterpret_cast<uint2*>(dst + row * kLd + 4 * c4) = o;
+    r.x[i] = row < n ? __ldg(reinterpret_cast<const float4*>(src + row * stride) + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
-// The chunk's T rows (hi and lo 64 x 64 tiles); rows >= n are zero.
-__device__ __forceinline__ void bc_load_t(__half* th, __half* tl, const uint16_t* src, int64_t stride, int n) {
+__device__ __forceinline__ void bc_fetch_gates(BcGates& x, const BwdChunkParams& p, int64_t r0, int n, int h) {
+  const int t0 = 2 * (threadIdx.x & 31), t1 = t0 + 1;
+  x.g0 = t0 < n ? p.g[(r0 + t0) * p.g_stride + h] : 0.f;
+  x.g1 = t1 < n ? p.g[(r0 + t1) * p.g_stride + h] : 0.f;
+  x.b0 = t0 < n ? p.beta[(r0 + t0) * p.beta_stride + h] : 0.f;
+  x.b1 = t1 < n ? p.beta[(r0 + t1) * p.beta_stride + h] : 0.f;
+}
+
+// bf16 rows -> fp16 tile
+__device__ __forceinline__ void bc_put_bf16_as_f16(__half* dst, const BcRows16& r) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (row < n) o = __ldg(reinterpret_cast<const uint4*>(src + row * stride) + c8);
-    __half* d = (c8 < 8 ? th : tl) + row * kLd64 + 8 * (c8 & 7);
-    *reinterpret_cast<uint4*>(d) = o;
+    float f[8];
+    unpack_bf16x8(r.x[i], f);
+    *reinterpret_cast<uint4*>(dst + row * kLd + 8 * c8) = pack_half8(f, 1.f);
   }
 }
 
-// Gates of a chunk, by warp 0: b (in-chunk log-decay prefix) and beta per token,
-// zero past the chunk's end.
-__device__ __forceinline__ void bc_gates(const BwdChunkParams& p, int64_t r0, int n, int h, float* s_b,
-                                         float* s_beta) {
-  const int lane = threadIdx.x & 31;
-  const int t0 = 2 * lane, t1 = 2 * lane + 1;
-  const float g0 = t0 < n ? p.g[(r0 + t0) * p.g_stride + h] : 0.f;
-  const float g1 = t1 < n ? p.g[(r0 + t1) * p.g_stride + h] : 0.f;
-  const GatePrefix gp = gate_prefix(g0, g1);
-  s_b[t0] = gp.gca;
-  s_b[t1] = gp.gcb;
-  s_beta[t0] = t0 < n ? p.beta[(r0 + t0) * p.beta_stride + h] : 0.f;
-  s_beta[t1] = t1 < n ? p.beta[(r0 + t1) * p.beta_stride + h] : 0.f;
+// 16-bit rows -> tile, unconverted
+__device__ __forceinline__ void bc_put16(void* dst, const BcRows16& r) {
+  uint16_t* d16 = static_cast<uint16_t*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+    *reinterpret_cast<uint4*>(d16 + row * kLd + 8 * c8) = r.x[i];
+  }
+}
+
+// T rows (64 fp16 hi then 64 lo) -> the hi and lo 64 x 64 tiles
+__device__ __forceinline__ void bc_put_t(__half* th, __half* tl, const BcRows16& r) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+    *reinterpret_cast<uint4*>((c8 < 8 ? th : tl) + row * kLd64 + 8 * (c8 & 7)) = r.x[i];
+  }
+}
+
+// fp32 rows -> fp16 tile; row `row` (= warp + 8 i for this thread) scaled by scale_of(row)
+template <typename Scale>
+__device__ __forceinline__ void bc_put_f32(__half* dst, const BcRows32& r, Scale scale_of) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 5, c4 = idx & 31;
+    const float s = scale_of(row);
+    const float4 x = r.x[i];
+    *reinterpret_cast<uint2*>(dst + row * kLd + 4 * c4) =
+        make_uint2(pack_half2(x.x * s, x.y * s), pack_half2(x.z * s, x.w * s));
+  }
+}
+
+// In-chunk log-decay prefix b of the fetched gates (every warp computes it); warp 0
+// also writes b and beta per token to shared memory.
+__device__ __forceinline__ GatePrefix bc_put_gates(const BcGates& x, float* s_b, float* s_beta) {
+  const GatePrefix gp = gate_prefix(x.g0, x.g1);
+  if ((threadIdx.x >> 5) == 0) {
+    const int t0 = 2 * (threadIdx.x & 31);
+    s_b[t0] = gp.gca;
+    s_b[t0 + 1] = gp.gcb;
+    s_beta[t0] = x.b0;
+    s_beta[t0 + 1] = x.b1;
+  }
+  return gp;
+}
+
+// b of token t (0..63) from a warp's prefix; t is uniform over the warp
+__device__ __forceinline__ float bc_b_of(const GatePrefix& gp, int t) {
+  return __shfl_sync(0xffffffffu, (t & 1) ? gp.gcb : gp.gca, t >> 1);
 }
 
 // fp32 accumulator fragment -> fp16 hi and lo tiles (row-major, leading dimension ld).
@@ -200,17 +232,6 @@ __device__ __forceinline__ void bc_store_state(__half* dst, const __half* src) {
   for (int i = 0; i < 8; ++i) {
     const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
     reinterpret_cast<uint4*>(dst + row * kDim)[c8] = *reinterpret_cast<const uint4*>(src + row * kLd + 8 * c8);
-  }
-}
-
-// 64 x 128 bf16 rows -> bf16 tile (no conversion); rows >= n are zero.
-__device__ __forceinline__ void bc_load_raw(__nv_bfloat16* dst, const __nv_bfloat16* src, int64_t stride, int n) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
-    uint4 o = make_uint4(0, 0, 0, 0);
-    if (row < n) o = __ldg(reinterpret_cast<const uint4*>(src + row * stride) + c8);
-    *reinterpret_cast<uint4*>(dst + row * kLd + 8 * c8) = o;
   }
 }
 
@@ -266,17 +287,30 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const Bwd
       }
   }
   bc_store_split<16>(S, sSh, sSl, kLd, sm0, 0);
+
+  BcRows16 fk, fv, ft;
+  BcGates fg;
+  auto fetch = [&](int64_t c) {
+    const int64_t r0 = row0 + c * kChunk;
+    const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
+    bc_fetch16(fk, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
+    bc_fetch16(fv, p.v + r0 * p.v_stride + h * kDim, p.v_stride, n);
+    bc_fetch16(ft, p.tm + r0 * hrow + h * kDim, hrow, n);
+    bc_fetch_gates(fg, p, r0, n, h);
+  };
+  fetch(0);
   __syncthreads();
 
   for (int64_t c = 0; c < nch; ++c) {
     const int64_t r0 = row0 + c * kChunk;
     const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
     bc_store_state(p.s0buf + (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim, sSh);
-    if (warp == 0) bc_gates(p, r0, n, h, s_b, s_beta);
-    bc_load_bf16(sK, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
-    bc_load_raw(sV, p.v + r0 * p.v_stride + h * kDim, p.v_stride, n);
-    bc_load_t(sTh, sTl, p.tm + r0 * hrow + h * kDim, hrow, n);
+    bc_put_gates(fg, s_b, s_beta);
+    bc_put_bf16_as_f16(sK, fk);
+    bc_put16(sV, fv);
+    bc_put_t(sTh, sTl, ft);
     __syncthreads();
+    if (c + 1 < nch) fetch(c + 1);  // in flight while this chunk computes
 
     // K S0, then beta X = beta (V - Gamma K S0) as fp16 hi + lo
     {
@@ -356,7 +390,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const Bw
   __half* sDSl = sDSh + kDim * kLd;
   __half* sDUh = sDSl + kDim * kLd;  // du, then -Gamma r
   __half* sDUl = sDUh + kChunk * kLd;
-  __shared__ float s_b[kChunk], s_beta[kChunk], s_sc[kChunk];
+  __shared__ float s_b[kChunk], s_beta[kChunk];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   const int si = blockIdx.x / p.nv, h = blockIdx.x % p.nv, kh = h / (p.nv / p.nk);
@@ -386,24 +420,35 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const Bw
       }
   }
   bc_store_split<16>(dS, sDSh, sDSl, kLd, sm0, 0);
+
+  BcRows16 fq, fk, ft;
+  BcRows32 fd;
+  BcGates fg;
+  auto fetch = [&](int64_t c) {
+    const int64_t r0 = row0 + c * kChunk;
+    const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
+    bc_fetch16(fq, p.q + r0 * p.q_stride + kh * kDim, p.q_stride, n);
+    bc_fetch16(fk, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
+    bc_fetch16(ft, p.tm + r0 * hrow + h * kDim, hrow, n);
+    bc_fetch32(fd, p.dout + r0 * hrow + h * kDim, hrow, n);
+    bc_fetch_gates(fg, p, r0, n, h);
+  };
+  if (nch > 0) fetch(nch - 1);
   __syncthreads();
 
   for (int64_t c = nch - 1; c >= 0; --c) {
     const int64_t r0 = row0 + c * kChunk;
     const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
     bc_store_state(p.dsbuf + (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim, sDSh);
-    if (warp == 0) {
-      bc_gates(p, r0, n, h, s_b, s_beta);
-      __syncwarp();
-      s_sc[2 * lane] = __expf(s_b[2 * lane]) * kInvSqrtD;
-      s_sc[2 * lane + 1] = __expf(s_b[2 * lane + 1]) * kInvSqrtD;
+    {
+      const GatePrefix gp = bc_put_gates(fg, s_b, s_beta);
+      bc_put_bf16_as_f16(sQ, fq);
+      bc_put_bf16_as_f16(sK, fk);
+      bc_put_t(sTh, sTl, ft);
+      bc_put_f32(sDO, fd, [](int) { return 1.f; });
+      bc_put_f32(sDOs, fd, [&](int row) { return __expf(bc_b_of(gp, row)) * kInvSqrtD; });
     }
-    bc_load_bf16(sQ, p.q + r0 * p.q_stride + kh * kDim, p.q_stride, n);
-    bc_load_bf16(sK, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
-    bc_load_f32(sDO, p.dout + r0 * hrow + h * kDim, hrow, n, nullptr);
-    bc_load_t(sTh, sTl, p.tm + r0 * hrow + h * kDim, hrow, n);
     __syncthreads();
-    bc_load_f32(sDOs, p.dout + r0 * hrow + h * kDim, hrow, n, s_sc);
 
     // (Q K^T . M) / sqrt(dk), lower triangle with the diagonal
     {
@@ -482,6 +527,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const Bw
       bc_store_split<8>(acc, sDUh, sDUl, kLd, m0, n0);
     }
     __syncthreads();
+    if (c > 0) fetch(c - 1);  // in flight during the state update
 
     // dS = gamma dS + Q^T (Gamma dO / sqrt(dk)) - K^T (Gamma r)
     {
@@ -509,9 +555,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const Bw
 }
 
 // ---- per-chunk gradients ----------------------------------------------------------
-// One CTA per (chunk, v-head), items head-fastest so the v-heads of a GQA group read
-// their chunk's q and k tiles close together in time.
-constexpr int kGradsSmem = 5 * kTile128 + kTileState + 2 * kTile64;
+// One CTA per (chunk, key head): it walks the value heads of the key head's GQA group,
+// adding each one's dQ and dK in registers, so q, k, Q K^T and K K^T are formed once and
+// dq, dk are written once.
+constexpr int kGradsSmem = 5 * kTile128 + 2 * kTileState + 2 * kTile64;
 
 // Sums of a fragment row pair over the 4 lanes of a quad (lanes 4g .. 4g + 3).
 __device__ __forceinline__ float bc_quad_sum(float x) {
@@ -532,19 +579,20 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
   __half* sK = sQ + kChunk * kLd;
   __half* sDO = sK + kChunk * kLd;
   __half* sU = sDO + kChunk * kLd;
-  __half* sDU = sU + kChunk * kLd;  // du'
-  __half* sS = sDU + kChunk * kLd;  // S0, then dS_end
-  __half* sP0 = sS + kDim * kLd;    // dA = lower(dO u^T) . M / sqrt(dk)
+  __half* sDU = sU + kChunk * kLd;     // du'
+  __half* sS = sDU + kChunk * kLd;     // S0
+  __half* sE = sS + kDim * kLd;        // dS_end
+  __half* sP0 = sE + kDim * kLd;       // dA = lower(dO u^T) . M / sqrt(dk)
   __half* sP1 = sP0 + kChunk * kLd64;  // E = beta F
   __shared__ float s_b[kChunk], s_beta[kChunk];
-  // per-token partial sums: q.(dO S0^T), k.P, rows/columns of dA . QK^T and of E . G,
-  // rows of F . G, w, du'.v
+  // per-token partial sums of one value head: q.(dO S0^T), k.P, rows/columns of
+  // dA . QK^T and of E . G, rows of F . G, w, du'.v
   __shared__ float s_rq[kChunk], s_rkp[kChunk], s_r1[kChunk], s_c1[kChunk], s_r2[kChunk], s_c2[kChunk],
       s_rf[kChunk], s_rw[kChunk], s_rdv[kChunk];
   __shared__ float s_dot;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-  const int ci = blockIdx.x / p.nv, h = blockIdx.x % p.nv, kh = h / (p.nv / p.nk);
+  const int ci = blockIdx.x / p.nk, kh = blockIdx.x % p.nk, group = p.nv / p.nk;
   int s;
   int64_t c;
   if (p.cu_seqlens) {
@@ -568,299 +616,308 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
   const int64_t r0 = row0 + c * kChunk;
   if (c * kChunk >= len) return;
   const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
-  const int64_t hrow = static_cast<int64_t>(p.nv) * kDim;
-  const int64_t state_off = (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim;
+  const int64_t hrow = static_cast<int64_t>(p.nv) * kDim, krow = static_cast<int64_t>(p.nk) * kDim;
   const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2), an0 = 32 * (warp >> 2);
   const uint32_t aQ = mm::saddr(sQ), aK = mm::saddr(sK), aDO = mm::saddr(sDO), aU = mm::saddr(sU),
-                 aDU = mm::saddr(sDU), aS = mm::saddr(sS), aP0 = mm::saddr(sP0), aP1 = mm::saddr(sP1);
+                 aDU = mm::saddr(sDU), aS = mm::saddr(sS), aE = mm::saddr(sE), aP0 = mm::saddr(sP0),
+                 aP1 = mm::saddr(sP1);
 
-  if (tid < kChunk) {
-    s_rq[tid] = s_rkp[tid] = s_r1[tid] = s_c1[tid] = s_r2[tid] = s_c2[tid] = s_rf[tid] = s_rw[tid] = 0.f;
-    if (tid == 0) s_dot = 0.f;
-  }
-  if (warp == 0) bc_gates(p, r0, n, h, s_b, s_beta);
-  bc_load_bf16(sQ, p.q + r0 * p.q_stride + kh * kDim, p.q_stride, n);
-  bc_load_bf16(sK, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
-  bc_load_f32(sDO, p.dout + r0 * hrow + h * kDim, hrow, n, nullptr);
-  bc_load_half(sU, p.ubuf + r0 * hrow + h * kDim, hrow, n);
-  bc_load_half(sDU, p.dubuf + r0 * hrow + h * kDim, hrow, n);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int idx = tid + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
-    *reinterpret_cast<uint4*>(sS + row * kLd + 8 * c8) =
-        __ldg(reinterpret_cast<const uint4*>(p.s0buf + state_off + row * kDim) + c8);
+  {
+    BcRows16 fq, fk;
+    bc_fetch16(fq, p.q + r0 * p.q_stride + kh * kDim, p.q_stride, n);
+    bc_fetch16(fk, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
+    bc_put_bf16_as_f16(sQ, fq);
+    bc_put_bf16_as_f16(sK, fk);
   }
   __syncthreads();
+  // Q K^T and K K^T of the key head, kept in registers for every value head
+  float aA[4][4], aG[4][4];
+  mm::zero(aA);
+  mm::zero(aG);
+  mm::warp_mma<false, true, 4>(aA, aQ, kLd, aK, kLd, m0, an0, kDim);
+  mm::warp_mma<false, true, 4>(aG, aK, kLd, aK, kLd, m0, an0, kDim);
 
-  // dQ <- Gamma dO S0^T / sqrt(dk), dK <- -Gamma beta P with P = du' S0^T
   float dQ[8][4], dK[8][4];
   mm::zero(dQ);
   mm::zero(dK);
-  mm::warp_mma<false, true, 8>(dQ, aDO, kLd, aS, kLd, m0, n0, kDim);
-  mm::warp_mma<false, true, 8>(dK, aDU, kLd, aS, kLd, m0, n0, kDim);
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int t = m0 + gq + 8 * e;
-    float sq = 0.f, sk = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int col = n0 + 8 * j + 2 * tq;
-      const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(sQ + t * kLd + col));
-      const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + col));
-      sq = fmaf(q2.x, dQ[j][2 * e], fmaf(q2.y, dQ[j][2 * e + 1], sq));
-      sk = fmaf(k2.x, dK[j][2 * e], fmaf(k2.y, dK[j][2 * e + 1], sk));
-    }
-    sq = bc_quad_sum(sq);
-    sk = bc_quad_sum(sk);
-    if (tq == 0) {
-      atomicAdd(&s_rq[t], sq);
-      atomicAdd(&s_rkp[t], sk);
-    }
-    const float G = __expf(s_b[t]), fq = G * kInvSqrtD, fk = -G * s_beta[t];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      dQ[j][2 * e] *= fq;
-      dQ[j][2 * e + 1] *= fq;
-      dK[j][2 * e] *= fk;
-      dK[j][2 * e + 1] *= fk;
-    }
-  }
-  __syncthreads();  // every warp is done with S0
-
-  // dS_end over S0, accumulating <dS_end, S0>
-  {
-    float dot = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = tid + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
-      uint4* dst = reinterpret_cast<uint4*>(sS + row * kLd + 8 * c8);
-      const uint4 old = *dst;
-      const uint4 nw = __ldg(reinterpret_cast<const uint4*>(p.dsbuf + state_off + row * kDim) + c8);
-      const __half2* a2 = reinterpret_cast<const __half2*>(&old);
-      const __half2* b2 = reinterpret_cast<const __half2*>(&nw);
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const float2 fa = __half22float2(a2[x]), fb = __half22float2(b2[x]);
-        dot = fmaf(fa.x, fb.x, fmaf(fa.y, fb.y, dot));
-      }
-      *dst = nw;
-    }
-    dot = bc_column_sum(bc_quad_sum(dot));
-    if (lane == 0) atomicAdd(&s_dot, dot);
-  }
-
-  // dA = lower(dO u^T) . M / sqrt(dk) and the row/column sums of dA . (Q K^T)
-  {
-    float aA[4][4], aD[4][4], col[4][2];
-    mm::zero(aA);
-    mm::zero(aD);
-    mm::warp_mma<false, true, 4>(aA, aQ, kLd, aK, kLd, m0, an0, kDim);
-    mm::warp_mma<false, true, 4>(aD, aDO, kLd, aU, kLd, m0, an0, kDim);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) col[j][0] = col[j][1] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int t = m0 + gq + 8 * e;
-      const float bt = s_b[t];
-      float row = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          const int jj = an0 + 8 * j + 2 * tq + x;
-          const float m = jj <= t ? __expf(bt - s_b[jj]) * kInvSqrtD : 0.f;
-          const float da = aD[j][2 * e + x] * m, y = da * aA[j][2 * e + x];
-          aD[j][2 * e + x] = da;
-          row += y;
-          col[j][x] += y;
-        }
-      row = bc_quad_sum(row);
-      if (tq == 0) atomicAdd(&s_r1[t], row);
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        const float v = bc_column_sum(col[j][x]);
-        if (gq == 0) atomicAdd(&s_c1[an0 + 8 * j + 2 * tq + x], v);
-      }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e)
-        *reinterpret_cast<__half2*>(sP0 + (m0 + gq + 8 * e) * kLd64 + an0 + 8 * j + 2 * tq) =
-            __floats2half2_rn(aD[j][2 * e], aD[j][2 * e + 1]);
-  }
-
-  // F = -strict_lower(du' u^T) . M, E = beta F; rows of F . G; rows/columns of E . G
-  {
-    float aG[4][4], aF[4][4], col[4][2];
-    mm::zero(aG);
-    mm::zero(aF);
-    mm::warp_mma<false, true, 4>(aG, aK, kLd, aK, kLd, m0, an0, kDim);
-    mm::warp_mma<false, true, 4>(aF, aDU, kLd, aU, kLd, m0, an0, kDim);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) col[j][0] = col[j][1] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int t = m0 + gq + 8 * e;
-      const float bt = s_b[t], be = s_beta[t];
-      float rf = 0.f, rz = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          const int jj = an0 + 8 * j + 2 * tq + x;
-          const float m = jj < t ? __expf(bt - s_b[jj]) : 0.f;
-          const float f = -aF[j][2 * e + x] * m, gv = aG[j][2 * e + x], ee = be * f, z = ee * gv;
-          aF[j][2 * e + x] = ee;
-          rf = fmaf(f, gv, rf);
-          rz += z;
-          col[j][x] += z;
-        }
-      rf = bc_quad_sum(rf);
-      rz = bc_quad_sum(rz);
-      if (tq == 0) {
-        atomicAdd(&s_rf[t], rf);
-        atomicAdd(&s_r2[t], rz);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        const float v = bc_column_sum(col[j][x]);
-        if (gq == 0) atomicAdd(&s_c2[an0 + 8 * j + 2 * tq + x], v);
-      }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e)
-        *reinterpret_cast<__half2*>(sP1 + (m0 + gq + 8 * e) * kLd64 + an0 + 8 * j + 2 * tq) =
-            __floats2half2_rn(aF[j][2 * e], aF[j][2 * e + 1]);
-  }
-  __syncthreads();  // dA, E and dS_end are in shared memory
-
-  // dQ += dA K; dK += E K + E^T K + dA^T Q + (gamma / Gamma) u dS_end^T
-  mm::warp_mma<false, false, 8>(dQ, aP0, kLd64, aK, kLd, m0, n0, kChunk);
-  mm::warp_mma<false, false, 8>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
-  mm::warp_mma<true, false, 8>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
-  mm::warp_mma<true, false, 8>(dK, aP0, kLd64, aQ, kLd, m0, n0, kChunk);
-  {
-    float uD[8][4];
-    mm::zero(uD);
-    mm::warp_mma<false, true, 8>(uD, aU, kLd, aS, kLd, m0, n0, kDim);
-    const float blast = s_b[kChunk - 1];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int t = m0 + gq + 8 * e;
-      const float sc = __expf(blast - s_b[t]);
-      float rw = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int colx = n0 + 8 * j + 2 * tq;
-        const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + colx));
-        const float a = sc * uD[j][2 * e], b = sc * uD[j][2 * e + 1];
-        dK[j][2 * e] += a;
-        dK[j][2 * e + 1] += b;
-        rw = fmaf(k2.x, a, fmaf(k2.y, b, rw));
-      }
-      rw = bc_quad_sum(rw);
-      if (tq == 0) atomicAdd(&s_rw[t], rw);
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int t = m0 + gq + 8 * e;
-    if (t < n) {
-      float* qrow = p.dq_part + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
-      float* krow = p.dk_part + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        *reinterpret_cast<float2*>(qrow + 8 * j) = make_float2(dQ[j][2 * e], dQ[j][2 * e + 1]);
-        *reinterpret_cast<float2*>(krow + 8 * j) = make_float2(dK[j][2 * e], dK[j][2 * e + 1]);
-      }
-    }
-  }
-  // du'_t . v_t: four threads per token, 32 columns each
-  {
-    const int t = tid >> 2, qq = tid & 3;
-    float d = 0.f;
-    if (t < n) {
+  for (int j = 0; j < group; ++j) {
+    const int h = kh * group + j;
+    const int64_t state_off = (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim;
+    {
+      // u, du', S0 and dS_end straight into shared memory; dO and the gates through registers
+      const __half* ug = p.ubuf + r0 * hrow + h * kDim;
+      const __half* dg = p.dubuf + r0 * hrow + h * kDim;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float vf[8];
-        unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.v + (r0 + t) * p.v_stride + h * kDim + 32 * qq) + i), vf);
-        const uint4 draw = *reinterpret_cast<const uint4*>(sDU + t * kLd + 32 * qq + 8 * i);
-        const __half2* d2 = reinterpret_cast<const __half2*>(&draw);
+        const int idx = tid + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+        const int64_t src_row = row < n ? row : 0;
+        mm::cp_async16(aU + 2u * (row * kLd + 8 * c8), ug + src_row * hrow + 8 * c8, row < n);
+        mm::cp_async16(aDU + 2u * (row * kLd + 8 * c8), dg + src_row * hrow + 8 * c8, row < n);
+      }
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float2 f = __half22float2(d2[x]);
-          d = fmaf(f.x, vf[2 * x], fmaf(f.y, vf[2 * x + 1], d));
+      for (int i = 0; i < 8; ++i) {
+        const int idx = tid + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+        mm::cp_async16(aS + 2u * (row * kLd + 8 * c8), p.s0buf + state_off + row * kDim + 8 * c8, true);
+        mm::cp_async16(aE + 2u * (row * kLd + 8 * c8), p.dsbuf + state_off + row * kDim + 8 * c8, true);
+      }
+      mm::cp_async_commit();
+      BcRows32 fd;
+      BcGates fg;
+      bc_fetch32(fd, p.dout + r0 * hrow + h * kDim, hrow, n);
+      bc_fetch_gates(fg, p, r0, n, h);
+      if (tid < kChunk) {
+        s_rq[tid] = s_rkp[tid] = s_r1[tid] = s_c1[tid] = s_r2[tid] = s_c2[tid] = s_rf[tid] = s_rw[tid] = 0.f;
+        if (tid == 0) s_dot = 0.f;
+      }
+      bc_put_gates(fg, s_b, s_beta);
+      bc_put_f32(sDO, fd, [](int) { return 1.f; });
+      mm::cp_async_wait_all();
+    }
+    __syncthreads();
+
+    // dQ += Gamma dO S0^T / sqrt(dk); dK -= Gamma beta P with P = du' S0^T
+    {
+      float tq8[8][4], tp8[8][4];
+      mm::zero(tq8);
+      mm::zero(tp8);
+      mm::warp_mma<false, true, 8>(tq8, aDO, kLd, aS, kLd, m0, n0, kDim);
+      mm::warp_mma<false, true, 8>(tp8, aDU, kLd, aS, kLd, m0, n0, kDim);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = m0 + gq + 8 * e;
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int col = n0 + 8 * jj + 2 * tq;
+          const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(sQ + t * kLd + col));
+          const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + col));
+          sq = fmaf(q2.x, tq8[jj][2 * e], fmaf(q2.y, tq8[jj][2 * e + 1], sq));
+          sk = fmaf(k2.x, tp8[jj][2 * e], fmaf(k2.y, tp8[jj][2 * e + 1], sk));
+        }
+        sq = bc_quad_sum(sq);
+        sk = bc_quad_sum(sk);
+        if (tq == 0) {
+          atomicAdd(&s_rq[t], sq);
+          atomicAdd(&s_rkp[t], sk);
+        }
+        const float G = __expf(s_b[t]), fq = G * kInvSqrtD, fk = -G * s_beta[t];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          dQ[jj][2 * e] = fmaf(fq, tq8[jj][2 * e], dQ[jj][2 * e]);
+          dQ[jj][2 * e + 1] = fmaf(fq, tq8[jj][2 * e + 1], dQ[jj][2 * e + 1]);
+          dK[jj][2 * e] = fmaf(fk, tp8[jj][2 * e], dK[jj][2 * e]);
+          dK[jj][2 * e + 1] = fmaf(fk, tp8[jj][2 * e + 1], dK[jj][2 * e + 1]);
         }
       }
     }
-    d = bc_quad_sum(d);
-    if (qq == 0) s_rdv[t] = d;
-  }
-  __syncthreads();
 
-  // per-token dbeta and d b, then dg = suffix sums of d b over the chunk (warp 0)
-  if (warp == 0) {
-    const float gam = __expf(s_b[kChunk - 1]);
-    float wsum = s_rw[2 * lane] + s_rw[2 * lane + 1];
+    // <dS_end, S0>
+    {
+      float dot = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-    float db[2], dbe[2];
+      for (int i = 0; i < 8; ++i) {
+        const int idx = tid + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
+        const uint4 a = *reinterpret_cast<const uint4*>(sS + row * kLd + 8 * c8);
+        const uint4 b = *reinterpret_cast<const uint4*>(sE + row * kLd + 8 * c8);
+        const __half2* a2 = reinterpret_cast<const __half2*>(&a);
+        const __half2* b2 = reinterpret_cast<const __half2*>(&b);
 #pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const int t = 2 * lane + x;
-      const float G = __expf(s_b[t]);
-      db[x] = G * kInvSqrtD * s_rq[t] - G * s_beta[t] * s_rkp[t] + (s_r2[t] - s_c2[t]) + (s_r1[t] - s_c1[t]) -
-              s_rw[t];
-      dbe[x] = s_rdv[t] - G * s_rkp[t] + s_rf[t];
+        for (int x = 0; x < 4; ++x) {
+          const float2 fa = __half22float2(a2[x]), fb = __half22float2(b2[x]);
+          dot = fmaf(fa.x, fb.x, fmaf(fa.y, fb.y, dot));
+        }
+      }
+      dot = bc_column_sum(bc_quad_sum(dot));
+      if (lane == 0) atomicAdd(&s_dot, dot);
     }
-    if (lane == 31) db[1] += gam * s_dot + wsum;
-    // suffix sums over the token pairs of the lanes
-    const float pair = db[0] + db[1];
-    float incl = pair;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_down_sync(0xffffffffu, incl, o);
-      if (lane + o < 32) incl += y;
-    }
-    const float dg0 = incl, dg1 = incl - db[0];
-    const int t0 = 2 * lane, t1 = t0 + 1;
-    if (t0 < n) {
-      p.dg[(r0 + t0) * p.nv + h] = dg0;
-      p.dbeta[(r0 + t0) * p.nv + h] = dbe[0];
-    }
-    if (t1 < n) {
-      p.dg[(r0 + t1) * p.nv + h] = dg1;
-      p.dbeta[(r0 + t1) * p.nv + h] = dbe[1];
-    }
-  }
-}
 
-// dq[r][kh] and dk[r][kh]: the per-v-head parts summed over the value heads of key head kh.
-__global__ void gdn_bwd_reduce_kernel(const BwdChunkParams p, float* dq, float* dk, int64_t rows) {
-  const int group = p.nv / p.nk;
-  const int64_t n4 = rows * p.nk * (kDim / 4);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const int64_t r = i / (static_cast<int64_t>(p.nk) * (kDim / 4));
-    const int rem = static_cast<int>(i % (static_cast<int64_t>(p.nk) * (kDim / 4)));
-    const int kh = rem / (kDim / 4), e4 = rem % (kDim / 4);
-    float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
-    for (int j = 0; j < group; ++j) {
-      const int64_t o = (r * p.nv + kh * group + j) * kDim + 4 * e4;
-      const float4 a = *reinterpret_cast<const float4*>(p.dq_part + o);
-      const float4 b = *reinterpret_cast<const float4*>(p.dk_part + o);
-      sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
-      sk.x += b.x; sk.y += b.y; sk.z += b.z; sk.w += b.w;
+    // dA = lower(dO u^T) . M / sqrt(dk) and the row/column sums of dA . (Q K^T)
+    {
+      float aD[4][4], col[4][2];
+      mm::zero(aD);
+      mm::warp_mma<false, true, 4>(aD, aDO, kLd, aU, kLd, m0, an0, kDim);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) col[jj][0] = col[jj][1] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = m0 + gq + 8 * e;
+        const float bt = s_b[t];
+        float row = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const int i = an0 + 8 * jj + 2 * tq + x;
+            const float m = i <= t ? __expf(bt - s_b[i]) * kInvSqrtD : 0.f;
+            const float da = aD[jj][2 * e + x] * m, y = da * aA[jj][2 * e + x];
+            aD[jj][2 * e + x] = da;
+            row += y;
+            col[jj][x] += y;
+          }
+        row = bc_quad_sum(row);
+        if (tq == 0) atomicAdd(&s_r1[t], row);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const float v = bc_column_sum(col[jj][x]);
+          if (gq == 0) atomicAdd(&s_c1[an0 + 8 * jj + 2 * tq + x], v);
+        }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          *reinterpret_cast<__half2*>(sP0 + (m0 + gq + 8 * e) * kLd64 + an0 + 8 * jj + 2 * tq) =
+              __floats2half2_rn(aD[jj][2 * e], aD[jj][2 * e + 1]);
     }
-    reinterpret_cast<float4*>(dq)[i] = sq;
-    reinterpret_cast<float4*>(dk)[i] = sk;
+
+    // F = -strict_lower(du' u^T) . M, E = beta F; rows of F . G; rows/columns of E . G
+    {
+      float aF[4][4], col[4][2];
+      mm::zero(aF);
+      mm::warp_mma<false, true, 4>(aF, aDU, kLd, aU, kLd, m0, an0, kDim);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) col[jj][0] = col[jj][1] = 0.f;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = m0 + gq + 8 * e;
+        const float bt = s_b[t], be = s_beta[t];
+        float rf = 0.f, rz = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            const int i = an0 + 8 * jj + 2 * tq + x;
+            const float m = i < t ? __expf(bt - s_b[i]) : 0.f;
+            const float f = -aF[jj][2 * e + x] * m, gv = aG[jj][2 * e + x], ee = be * f, z = ee * gv;
+            aF[jj][2 * e + x] = ee;
+            rf = fmaf(f, gv, rf);
+            rz += z;
+            col[jj][x] += z;
+          }
+        rf = bc_quad_sum(rf);
+        rz = bc_quad_sum(rz);
+        if (tq == 0) {
+          atomicAdd(&s_rf[t], rf);
+          atomicAdd(&s_r2[t], rz);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const float v = bc_column_sum(col[jj][x]);
+          if (gq == 0) atomicAdd(&s_c2[an0 + 8 * jj + 2 * tq + x], v);
+        }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          *reinterpret_cast<__half2*>(sP1 + (m0 + gq + 8 * e) * kLd64 + an0 + 8 * jj + 2 * tq) =
+              __floats2half2_rn(aF[jj][2 * e], aF[jj][2 * e + 1]);
+    }
+    __syncthreads();  // dA and E are in shared memory
+
+    // dQ += dA K; dK += E K + E^T K + dA^T Q + (gamma / Gamma) u dS_end^T
+    mm::warp_mma<false, false, 8>(dQ, aP0, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma<false, false, 8>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma<true, false, 8>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma<true, false, 8>(dK, aP0, kLd64, aQ, kLd, m0, n0, kChunk);
+    {
+      float uD[8][4];
+      mm::zero(uD);
+      mm::warp_mma<false, true, 8>(uD, aU, kLd, aE, kLd, m0, n0, kDim);
+      const float blast = s_b[kChunk - 1];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = m0 + gq + 8 * e;
+        const float sc = __expf(blast - s_b[t]);
+        float rw = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int colx = n0 + 8 * jj + 2 * tq;
+          const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + colx));
+          const float a = sc * uD[jj][2 * e], b = sc * uD[jj][2 * e + 1];
+          dK[jj][2 * e] += a;
+          dK[jj][2 * e + 1] += b;
+          rw = fmaf(k2.x, a, fmaf(k2.y, b, rw));
+        }
+        rw = bc_quad_sum(rw);
+        if (tq == 0) atomicAdd(&s_rw[t], rw);
+      }
+    }
+    // du'_t . v_t: four threads per token, 32 columns each
+    {
+      const int t = tid >> 2, qq = tid & 3;
+      float d = 0.f;
+      if (t < n) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float vf[8];
+          unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.v + (r0 + t) * p.v_stride + h * kDim + 32 * qq) + i), vf);
+          const uint4 draw = *reinterpret_cast<const uint4*>(sDU + t * kLd + 32 * qq + 8 * i);
+          const __half2* d2 = reinterpret_cast<const __half2*>(&draw);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float2 f = __half22float2(d2[x]);
+            d = fmaf(f.x, vf[2 * x], fmaf(f.y, vf[2 * x + 1], d));
+          }
+        }
+      }
+      d = bc_quad_sum(d);
+      if (qq == 0) s_rdv[t] = d;
+    }
+    __syncthreads();
+
+    // per-token dbeta and d b of this value head, then dg = suffix sums of d b (warp 0)
+    if (warp == 0) {
+      const float gam = __expf(s_b[kChunk - 1]);
+      float wsum = s_rw[2 * lane] + s_rw[2 * lane + 1];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+      float db[2], dbe[2];
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int t = 2 * lane + x;
+        const float G = __expf(s_b[t]);
+        db[x] = G * kInvSqrtD * s_rq[t] - G * s_beta[t] * s_rkp[t] + (s_r2[t] - s_c2[t]) + (s_r1[t] - s_c1[t]) -
+                s_rw[t];
+        dbe[x] = s_rdv[t] - G * s_rkp[t] + s_rf[t];
+      }
+      if (lane == 31) db[1] += gam * s_dot + wsum;
+      const float pair = db[0] + db[1];
+      float incl = pair;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      const float dg0 = incl, dg1 = incl - db[0];
+      const int t0 = 2 * lane, t1 = t0 + 1;
+      if (t0 < n) {
+        p.dg[(r0 + t0) * p.nv + h] = dg0;
+        p.dbeta[(r0 + t0) * p.nv + h] = dbe[0];
+      }
+      if (t1 < n) {
+        p.dg[(r0 + t1) * p.nv + h] = dg1;
+        p.dbeta[(r0 + t1) * p.nv + h] = dbe[1];
+      }
+    }
+    __syncthreads();  // the next value head reuses the tiles and the sums
+  }
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int t = m0 + gq + 8 * e;
+    if (t < n) {
+      float* qrow = p.dq + (r0 + t) * krow + kh * kDim + n0 + 2 * tq;
+      float* krw = p.dk + (r0 + t) * krow + kh * kDim + n0 + 2 * tq;
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        *reinterpret_cast<float2*>(qrow + 8 * jj) = make_float2(dQ[jj][2 * e], dQ[jj][2 * e + 1]);
+        *reinterpret_cast<float2*>(krw + 8 * jj) = make_float2(dK[jj][2 * e], dK[jj][2 * e + 1]);
+      }
+    }
   }
 }
 

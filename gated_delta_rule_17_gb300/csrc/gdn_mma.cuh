@@ -102,6 +102,15 @@ __device__ __forceinline__ void zero(float (&c)[NT][4]) {
   for (int j = 0; j < NT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
 }
 
+// 16-byte global -> shared copy that bypasses the registers; with valid = false
+// it writes 16 zero bytes and reads nothing (src must still be a mapped address).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
 // fp16 hi + lo of a pair: hi = fp16(x), lo = fp16(x - hi)
 __device__ __forceinline__ void split2(float x, float y, __half2& hi, __half2& lo) {
   hi = __floats2half2_rn(x, y);

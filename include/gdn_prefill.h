@@ -190,8 +190,8 @@ void gdn_set_timing_events(void* before_wy, void* before_spine, void* after_spin
  * storing each chunk's entry state, a reverse chain storing each chunk's state
  * gradient, and the per-chunk gradients, all on the tensor cores (fp16 operands,
  * fp32 accumulation, fp32 chain states). The forward's outputs are not needed.
- * Enqueues 5 kernels (6 with cu_seqlens). Scratch: about 10 bytes per (row,
- * v-head, column) plus 64 KB per (64-row chunk, v-head).
+ * Enqueues 4 kernels (5 with cu_seqlens). Scratch: 6 bytes per (row, v-head,
+ * column) plus 64 KB per (64-row chunk, v-head).
  *   q, k, v, g, beta, strides, cu_seqlens, B, T, nk, nv, dk, dv: as gdn_prefill
  *             (qk_l2norm must be 0: pass the normalised q and k).
  *   h0     : the INITIAL state (gdn_prefill updates its state in place, so keep a

@@ -143,9 +143,9 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 
 def test_backward_workspace_sizes(lib):
-    # varlen schedule (2B + 1 int32), then T, u and du' (16-bit, rows x nv x 128 each),
-    # each chunk slot's S0 and dS_end (fp16 128 x 128 per head, rows / 64 + B + 1
-    # slots), and the per-v-head dq and dk parts (fp32, rows x nv x 128 each)
+    # varlen schedule (2B + 1 int32), then T, u and du' (16-bit, rows x nv x 128 each)
+    # and each chunk slot's S0 and dS_end (fp16 128 x 128 per head, rows / 64 + B + 1
+    # slots)
     def a256(x):
         return (x + 255) // 256 * 256
 
@@ -159,7 +159,5 @@ def test_backward_workspace_sizes(lib):
         off = a256(off + row16)
         off = a256(off + state16)
         off = a256(off + state16)
-        off = a256(off + 2 * row16)
-        off = a256(off + 2 * row16)
         assert lib.gdn_prefill_backward_workspace_bytes(B, T, nv, 128, 128, varlen) == off
     assert lib.gdn_prefill_backward_workspace_bytes(0, T, nv, 128, 128, 0) == 0

@@ -61,7 +61,7 @@ def run_backward(p, seed, with_dst=True, state_table=False, workspace=True):
                  state_is_table=state_table, workspace=ws)
     torch.cuda.synchronize()
     gdn.check()
-    assert gdn.last_launch_count() == (6 if p.varlen else 5)
+    assert gdn.last_launch_count() == (5 if p.varlen else 4)
     ref = oracle.token_loop_backward(p, dout.astype(np.float64), None if dst is None else dst.astype(np.float64))
     return {n: t.cpu().numpy().astype(np.float64) for n, t in out.items()}, ref
 
