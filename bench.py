@@ -494,7 +494,7 @@ def run_backward(args, world, rank, local):
                        "l2": "no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": None,
-                         "kernel": "whole backward (WY, two chains, per-chunk gradients, GQA reduce)",
+                         "kernel": "whole backward (WY, two chains, per-chunk gradients)",
                          "algorithmic_bytes": io, "peak_source": peak_src},
             "gpu_launches": launches * args.steps, "clocks": clk.summary()}), flush=True)
 

@@ -226,6 +226,19 @@ __device__ __forceinline__ void bc_store_split(const float (&c)[NT][4], __half* 
     }
 }
 
+template <int NT>
+__device__ __forceinline__ void bc_store_split2(const float (&c)[2][NT][4], __half* hi, __half* lo, int ld, int m0,
+                                                int n0) {
+  bc_store_split<NT>(c[0], hi, lo, ld, m0, n0);
+  bc_store_split<NT>(c[1], hi, lo, ld, m0 + 16, n0);
+}
+
+// Warp tiles. A 64 x 128 product gives warp w the 32 x 32 block at rows 32 (w % 2),
+// columns 32 (w / 2); a 128 x 128 product (a chain's state) the 32 x 64 block at rows
+// 32 (w % 4), columns 64 (w / 4); a 64 x 64 product the 16 x 32 block at rows
+// 16 (w % 4), columns 32 (w / 4). Element (mt, j, x) of a thread's two-row-tile
+// accumulator sits at row m0 + 16 mt + g + 8 (x / 2), column n0 + 8 j + 2 t + x % 2.
+
 // 128 x 128 fp16 tile (leading dimension kLd) -> global [128][128].
 __device__ __forceinline__ void bc_store_state(__half* dst, const __half* src) {
 #pragma unroll
@@ -242,8 +255,8 @@ __device__ __forceinline__ const float* bc_h0(const BwdChunkParams& p, int s, in
 }
 
 // ---- forward chain: every chunk's entry state S0 and u ------------------------------
-// One CTA per (sequence, v-head). The state lives in fp32 registers: warp w holds
-// rows 16 w .. 16 w + 15 (k) and all 128 columns (v).
+// One CTA per (sequence, v-head). The state lives in fp32 registers (warp tiles of
+// the 128 x 128 state, k by v).
 constexpr int kStatesSmem = 2 * kTile128 + 2 * kTile64 + 2 * kTileState + 4 * kTile128;
 
 __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const BwdChunkParams p) {
@@ -268,25 +281,28 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const Bwd
   const int64_t nch = (len + kChunk - 1) / kChunk;
   if (nch == 0) return;
   const int64_t hrow = static_cast<int64_t>(p.nv) * kDim;  // row stride of the [rows][nv][128] buffers
-  const int sm0 = 16 * warp;
-  const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);  // 64 x 128 products
+  const int sm0 = 32 * (warp & 3), sn0 = 64 * (warp >> 2);  // state tile
+  const int m0 = 32 * (warp & 1), n0 = 32 * (warp >> 1);    // 64 x 128 products
   const uint32_t aK = mm::saddr(sK), aTh = mm::saddr(sTh), aTl = mm::saddr(sTl), aSh = mm::saddr(sSh),
                  aSl = mm::saddr(sSl), aXh = mm::saddr(sXh), aXl = mm::saddr(sXl), aUh = mm::saddr(sUh),
                  aUl = mm::saddr(sUl);
 
-  float S[16][4];
+  float S[2][8][4];
   {
     const float* h0 = bc_h0(p, s, h);
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float2 x = *reinterpret_cast<const float2*>(h0 + (sm0 + gq + 8 * e) * kDim + 8 * j + 2 * tq);
-        S[j][2 * e] = x.x;
-        S[j][2 * e + 1] = x.y;
-      }
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float2 x =
+              *reinterpret_cast<const float2*>(h0 + (sm0 + 16 * mt + gq + 8 * e) * kDim + sn0 + 8 * j + 2 * tq);
+          S[mt][j][2 * e] = x.x;
+          S[mt][j][2 * e + 1] = x.y;
+        }
   }
-  bc_store_split<16>(S, sSh, sSl, kLd, sm0, 0);
+  bc_store_split2<8>(S, sSh, sSl, kLd, sm0, sn0);
 
   BcRows16 fk, fv, ft;
   BcGates fg;
@@ -314,46 +330,52 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const Bwd
 
     // K S0, then beta X = beta (V - Gamma K S0) as fp16 hi + lo
     {
-      float acc[8][4];
+      float acc[2][4][4];
       mm::zero(acc);
-      mm::warp_mma<false, false, 8>(acc, aK, kLd, aSh, kLd, m0, n0, kDim);
-      mm::warp_mma<false, false, 8>(acc, aK, kLd, aSl, kLd, m0, n0, kDim);
+      mm::warp_mma2<false, false, 4>(acc, aK, kLd, aSh, kLd, m0, n0, kDim);
+      mm::warp_mma2<false, false, 4>(acc, aK, kLd, aSl, kLd, m0, n0, kDim);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = m0 + gq + 8 * e;
-        const float G = __expf(s_b[t]), bt = s_beta[t];
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float2 vv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sV + t * kLd + n0 + 8 * j + 2 * tq));
-          acc[j][2 * e] = bt * (vv.x - G * acc[j][2 * e]);
-          acc[j][2 * e + 1] = bt * (vv.y - G * acc[j][2 * e + 1]);
+        for (int e = 0; e < 2; ++e) {
+          const int t = m0 + 16 * mt + gq + 8 * e;
+          const float G = __expf(s_b[t]), bt = s_beta[t];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 vv =
+                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sV + t * kLd + n0 + 8 * j + 2 * tq));
+            acc[mt][j][2 * e] = bt * (vv.x - G * acc[mt][j][2 * e]);
+            acc[mt][j][2 * e + 1] = bt * (vv.y - G * acc[mt][j][2 * e + 1]);
+          }
         }
-      }
-      bc_store_split<8>(acc, sXh, sXl, kLd, m0, n0);
+      bc_store_split2<4>(acc, sXh, sXl, kLd, m0, n0);
     }
     __syncthreads();
 
     // u = T (beta X): stored for the gradient kernel; (gamma / Gamma) u as fp16 hi + lo
     {
-      float acc[8][4];
+      float acc[2][4][4];
       mm::zero(acc);
-      mm::warp_mma<false, false, 8>(acc, aTh, kLd64, aXh, kLd, m0, n0, kChunk);
-      mm::warp_mma<false, false, 8>(acc, aTh, kLd64, aXl, kLd, m0, n0, kChunk);
-      mm::warp_mma<false, false, 8>(acc, aTl, kLd64, aXh, kLd, m0, n0, kChunk);
+      mm::warp_mma2<false, false, 4>(acc, aTh, kLd64, aXh, kLd, m0, n0, kChunk);
+      mm::warp_mma2<false, false, 4>(acc, aTh, kLd64, aXl, kLd, m0, n0, kChunk);
+      mm::warp_mma2<false, false, 4>(acc, aTl, kLd64, aXh, kLd, m0, n0, kChunk);
       const float blast = s_b[kChunk - 1];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = m0 + gq + 8 * e;
-        const float sc = __expf(blast - s_b[t]);
-        __half* urow = p.ubuf + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (t < n) *reinterpret_cast<__half2*>(urow + 8 * j) = __floats2half2_rn(acc[j][2 * e], acc[j][2 * e + 1]);
-          acc[j][2 * e] *= sc;
-          acc[j][2 * e + 1] *= sc;
+        for (int e = 0; e < 2; ++e) {
+          const int t = m0 + 16 * mt + gq + 8 * e;
+          const float sc = __expf(blast - s_b[t]);
+          __half* urow = p.ubuf + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (t < n)
+              *reinterpret_cast<__half2*>(urow + 8 * j) = __floats2half2_rn(acc[mt][j][2 * e], acc[mt][j][2 * e + 1]);
+            acc[mt][j][2 * e] *= sc;
+            acc[mt][j][2 * e + 1] *= sc;
+          }
         }
-      }
-      bc_store_split<8>(acc, sUh, sUl, kLd, m0, n0);
+      bc_store_split2<4>(acc, sUh, sUl, kLd, m0, n0);
     }
     __syncthreads();
 
@@ -361,12 +383,14 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const Bwd
     {
       const float gam = __expf(s_b[kChunk - 1]);
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) S[j][x] *= gam;
-      mm::warp_mma<true, false, 16>(S, aK, kLd, aUh, kLd, sm0, 0, kChunk);
-      mm::warp_mma<true, false, 16>(S, aK, kLd, aUl, kLd, sm0, 0, kChunk);
-      bc_store_split<16>(S, sSh, sSl, kLd, sm0, 0);
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) S[mt][j][x] *= gam;
+      mm::warp_mma2<true, false, 8>(S, aK, kLd, aUh, kLd, sm0, sn0, kChunk);
+      mm::warp_mma2<true, false, 8>(S, aK, kLd, aUl, kLd, sm0, sn0, kChunk);
+      bc_store_split2<8>(S, sSh, sSl, kLd, sm0, sn0);
     }
     __syncthreads();
   }
@@ -399,27 +423,29 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const Bw
   if (!bc_sequence(p, s, row0, len)) return;
   const int64_t nch = (len + kChunk - 1) / kChunk;
   const int64_t hrow = static_cast<int64_t>(p.nv) * kDim;
-  const int sm0 = 16 * warp;
-  const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2);  // 64 x 128 products
-  const int an0 = 32 * (warp >> 2);                        // 64 x 64 products
+  const int sm0 = 32 * (warp & 3), sn0 = 64 * (warp >> 2);  // state tile
+  const int m0 = 32 * (warp & 1), n0 = 32 * (warp >> 1);    // 64 x 128 products
+  const int am0 = 16 * (warp & 3), an0 = 32 * (warp >> 2);  // 64 x 64 products
   const uint32_t aQ = mm::saddr(sQ), aK = mm::saddr(sK), aDO = mm::saddr(sDO), aDOs = mm::saddr(sDOs),
                  aTh = mm::saddr(sTh), aTl = mm::saddr(sTl), aA = mm::saddr(sA), aDSh = mm::saddr(sDSh),
                  aDSl = mm::saddr(sDSl), aDUh = mm::saddr(sDUh), aDUl = mm::saddr(sDUl);
 
-  float dS[16][4];
+  float dS[2][8][4];
   {
     const float* d0 = p.dst ? p.dst + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim : nullptr;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float2 x = make_float2(0.f, 0.f);
-        if (d0) x = *reinterpret_cast<const float2*>(d0 + (sm0 + gq + 8 * e) * kDim + 8 * j + 2 * tq);
-        dS[j][2 * e] = x.x;
-        dS[j][2 * e + 1] = x.y;
-      }
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float2 x = make_float2(0.f, 0.f);
+          if (d0) x = *reinterpret_cast<const float2*>(d0 + (sm0 + 16 * mt + gq + 8 * e) * kDim + sn0 + 8 * j + 2 * tq);
+          dS[mt][j][2 * e] = x.x;
+          dS[mt][j][2 * e + 1] = x.y;
+        }
   }
-  bc_store_split<16>(dS, sDSh, sDSl, kLd, sm0, 0);
+  bc_store_split2<8>(dS, sDSh, sDSl, kLd, sm0, sn0);
 
   BcRows16 fq, fk, ft;
   BcRows32 fd;
@@ -454,10 +480,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const Bw
     {
       float acc[4][4];
       mm::zero(acc);
-      mm::warp_mma<false, true, 4>(acc, aQ, kLd, aK, kLd, m0, an0, kDim);
+      mm::warp_mma<false, true, 4>(acc, aQ, kLd, aK, kLd, am0, an0, kDim);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int t = m0 + gq + 8 * e;
+        const int t = am0 + gq + 8 * e;
         const float bt = s_b[t];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -472,59 +498,65 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const Bw
 
     // du = A~^T dO + (gamma / Gamma) K dS, as fp16 hi + lo
     {
-      float a1[8][4], a2[8][4];
+      float a1[2][4][4], a2[2][4][4];
       mm::zero(a1);
       mm::zero(a2);
-      mm::warp_mma<true, false, 8>(a1, aA, kLd64, aDO, kLd, m0, n0, kChunk);
-      mm::warp_mma<false, false, 8>(a2, aK, kLd, aDSh, kLd, m0, n0, kDim);
-      mm::warp_mma<false, false, 8>(a2, aK, kLd, aDSl, kLd, m0, n0, kDim);
+      mm::warp_mma2<true, false, 4>(a1, aA, kLd64, aDO, kLd, m0, n0, kChunk);
+      mm::warp_mma2<false, false, 4>(a2, aK, kLd, aDSh, kLd, m0, n0, kDim);
+      mm::warp_mma2<false, false, 4>(a2, aK, kLd, aDSl, kLd, m0, n0, kDim);
       const float blast = s_b[kChunk - 1];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float sc = __expf(blast - s_b[m0 + gq + 8 * e]);
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          a1[j][2 * e] = fmaf(sc, a2[j][2 * e], a1[j][2 * e]);
-          a1[j][2 * e + 1] = fmaf(sc, a2[j][2 * e + 1], a1[j][2 * e + 1]);
+        for (int e = 0; e < 2; ++e) {
+          const float sc = __expf(blast - s_b[m0 + 16 * mt + gq + 8 * e]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            a1[mt][j][2 * e] = fmaf(sc, a2[mt][j][2 * e], a1[mt][j][2 * e]);
+            a1[mt][j][2 * e + 1] = fmaf(sc, a2[mt][j][2 * e + 1], a1[mt][j][2 * e + 1]);
+          }
         }
-      }
-      bc_store_split<8>(a1, sDUh, sDUl, kLd, m0, n0);
+      bc_store_split2<4>(a1, sDUh, sDUl, kLd, m0, n0);
     }
     __syncthreads();
 
     // du' = T^T du (stored), dV = beta du', then -Gamma beta du' as fp16 hi + lo
     {
-      float acc[8][4];
+      float acc[2][4][4];
       mm::zero(acc);
-      mm::warp_mma<true, false, 8>(acc, aTh, kLd64, aDUh, kLd, m0, n0, kChunk);
-      mm::warp_mma<true, false, 8>(acc, aTh, kLd64, aDUl, kLd, m0, n0, kChunk);
-      mm::warp_mma<true, false, 8>(acc, aTl, kLd64, aDUh, kLd, m0, n0, kChunk);
+      mm::warp_mma2<true, false, 4>(acc, aTh, kLd64, aDUh, kLd, m0, n0, kChunk);
+      mm::warp_mma2<true, false, 4>(acc, aTh, kLd64, aDUl, kLd, m0, n0, kChunk);
+      mm::warp_mma2<true, false, 4>(acc, aTl, kLd64, aDUh, kLd, m0, n0, kChunk);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = m0 + gq + 8 * e;
-        if (t < n) {
-          const float bt = s_beta[t];
-          __half* drow = p.dubuf + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
-          float* vrow = p.dv + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            *reinterpret_cast<__half2*>(drow + 8 * j) = __floats2half2_rn(acc[j][2 * e], acc[j][2 * e + 1]);
-            *reinterpret_cast<float2*>(vrow + 8 * j) = make_float2(bt * acc[j][2 * e], bt * acc[j][2 * e + 1]);
+        for (int e = 0; e < 2; ++e) {
+          const int t = m0 + 16 * mt + gq + 8 * e;
+          if (t < n) {
+            const float bt = s_beta[t];
+            __half* drow = p.dubuf + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+            float* vrow = p.dv + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              *reinterpret_cast<__half2*>(drow + 8 * j) = __floats2half2_rn(acc[mt][j][2 * e], acc[mt][j][2 * e + 1]);
+              *reinterpret_cast<float2*>(vrow + 8 * j) = make_float2(bt * acc[mt][j][2 * e], bt * acc[mt][j][2 * e + 1]);
+            }
           }
         }
-      }
       __syncthreads();  // every warp has read du
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = m0 + gq + 8 * e;
-        const float sc = -__expf(s_b[t]) * s_beta[t];
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          acc[j][2 * e] *= sc;
-          acc[j][2 * e + 1] *= sc;
+        for (int e = 0; e < 2; ++e) {
+          const int t = m0 + 16 * mt + gq + 8 * e;
+          const float sc = -__expf(s_b[t]) * s_beta[t];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[mt][j][2 * e] *= sc;
+            acc[mt][j][2 * e + 1] *= sc;
+          }
         }
-      }
-      bc_store_split<8>(acc, sDUh, sDUl, kLd, m0, n0);
+      bc_store_split2<4>(acc, sDUh, sDUl, kLd, m0, n0);
     }
     __syncthreads();
     if (c > 0) fetch(c - 1);  // in flight during the state update
@@ -533,24 +565,28 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const Bw
     {
       const float gam = __expf(s_b[kChunk - 1]);
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int x = 0; x < 4; ++x) dS[j][x] *= gam;
-      mm::warp_mma<true, false, 16>(dS, aQ, kLd, aDOs, kLd, sm0, 0, kChunk);
-      mm::warp_mma<true, false, 16>(dS, aK, kLd, aDUh, kLd, sm0, 0, kChunk);
-      mm::warp_mma<true, false, 16>(dS, aK, kLd, aDUl, kLd, sm0, 0, kChunk);
-      bc_store_split<16>(dS, sDSh, sDSl, kLd, sm0, 0);
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int x = 0; x < 4; ++x) dS[mt][j][x] *= gam;
+      mm::warp_mma2<true, false, 8>(dS, aQ, kLd, aDOs, kLd, sm0, sn0, kChunk);
+      mm::warp_mma2<true, false, 8>(dS, aK, kLd, aDUh, kLd, sm0, sn0, kChunk);
+      mm::warp_mma2<true, false, 8>(dS, aK, kLd, aDUl, kLd, sm0, sn0, kChunk);
+      bc_store_split2<8>(dS, sDSh, sDSl, kLd, sm0, sn0);
     }
     __syncthreads();
   }
   if (p.dh0) {
     float* d = p.dh0 + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim;
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int e = 0; e < 2; ++e)
-        *reinterpret_cast<float2*>(d + (sm0 + gq + 8 * e) * kDim + 8 * j + 2 * tq) =
-            make_float2(dS[j][2 * e], dS[j][2 * e + 1]);
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          *reinterpret_cast<float2*>(d + (sm0 + 16 * mt + gq + 8 * e) * kDim + sn0 + 8 * j + 2 * tq) =
+              make_float2(dS[mt][j][2 * e], dS[mt][j][2 * e + 1]);
   }
 }
 
@@ -617,7 +653,8 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
   if (c * kChunk >= len) return;
   const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
   const int64_t hrow = static_cast<int64_t>(p.nv) * kDim, krow = static_cast<int64_t>(p.nk) * kDim;
-  const int m0 = 16 * (warp & 3), n0 = 64 * (warp >> 2), an0 = 32 * (warp >> 2);
+  const int m0 = 32 * (warp & 1), n0 = 32 * (warp >> 1);    // 64 x 128 products
+  const int am0 = 16 * (warp & 3), an0 = 32 * (warp >> 2);  // 64 x 64 products
   const uint32_t aQ = mm::saddr(sQ), aK = mm::saddr(sK), aDO = mm::saddr(sDO), aU = mm::saddr(sU),
                  aDU = mm::saddr(sDU), aS = mm::saddr(sS), aE = mm::saddr(sE), aP0 = mm::saddr(sP0),
                  aP1 = mm::saddr(sP1);
@@ -634,10 +671,10 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
   float aA[4][4], aG[4][4];
   mm::zero(aA);
   mm::zero(aG);
-  mm::warp_mma<false, true, 4>(aA, aQ, kLd, aK, kLd, m0, an0, kDim);
-  mm::warp_mma<false, true, 4>(aG, aK, kLd, aK, kLd, m0, an0, kDim);
+  mm::warp_mma<false, true, 4>(aA, aQ, kLd, aK, kLd, am0, an0, kDim);
+  mm::warp_mma<false, true, 4>(aG, aK, kLd, aK, kLd, am0, an0, kDim);
 
-  float dQ[8][4], dK[8][4];
+  float dQ[2][4][4], dK[2][4][4];
   mm::zero(dQ);
   mm::zero(dK);
   for (int j = 0; j < group; ++j) {
@@ -677,38 +714,40 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
 
     // dQ += Gamma dO S0^T / sqrt(dk); dK -= Gamma beta P with P = du' S0^T
     {
-      float tq8[8][4], tp8[8][4];
+      float tq8[2][4][4], tp8[2][4][4];
       mm::zero(tq8);
       mm::zero(tp8);
-      mm::warp_mma<false, true, 8>(tq8, aDO, kLd, aS, kLd, m0, n0, kDim);
-      mm::warp_mma<false, true, 8>(tp8, aDU, kLd, aS, kLd, m0, n0, kDim);
+      mm::warp_mma2<false, true, 4>(tq8, aDO, kLd, aS, kLd, m0, n0, kDim);
+      mm::warp_mma2<false, true, 4>(tp8, aDU, kLd, aS, kLd, m0, n0, kDim);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = m0 + gq + 8 * e;
-        float sq = 0.f, sk = 0.f;
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int col = n0 + 8 * jj + 2 * tq;
-          const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(sQ + t * kLd + col));
-          const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + col));
-          sq = fmaf(q2.x, tq8[jj][2 * e], fmaf(q2.y, tq8[jj][2 * e + 1], sq));
-          sk = fmaf(k2.x, tp8[jj][2 * e], fmaf(k2.y, tp8[jj][2 * e + 1], sk));
-        }
-        sq = bc_quad_sum(sq);
-        sk = bc_quad_sum(sk);
-        if (tq == 0) {
-          atomicAdd(&s_rq[t], sq);
-          atomicAdd(&s_rkp[t], sk);
-        }
-        const float G = __expf(s_b[t]), fq = G * kInvSqrtD, fk = -G * s_beta[t];
+        for (int e = 0; e < 2; ++e) {
+          const int t = m0 + 16 * mt + gq + 8 * e;
+          float sq = 0.f, sk = 0.f;
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          dQ[jj][2 * e] = fmaf(fq, tq8[jj][2 * e], dQ[jj][2 * e]);
-          dQ[jj][2 * e + 1] = fmaf(fq, tq8[jj][2 * e + 1], dQ[jj][2 * e + 1]);
-          dK[jj][2 * e] = fmaf(fk, tp8[jj][2 * e], dK[jj][2 * e]);
-          dK[jj][2 * e + 1] = fmaf(fk, tp8[jj][2 * e + 1], dK[jj][2 * e + 1]);
+          for (int jj = 0; jj < 4; ++jj) {
+            const int col = n0 + 8 * jj + 2 * tq;
+            const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(sQ + t * kLd + col));
+            const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + col));
+            sq = fmaf(q2.x, tq8[mt][jj][2 * e], fmaf(q2.y, tq8[mt][jj][2 * e + 1], sq));
+            sk = fmaf(k2.x, tp8[mt][jj][2 * e], fmaf(k2.y, tp8[mt][jj][2 * e + 1], sk));
+          }
+          sq = bc_quad_sum(sq);
+          sk = bc_quad_sum(sk);
+          if (tq == 0) {
+            atomicAdd(&s_rq[t], sq);
+            atomicAdd(&s_rkp[t], sk);
+          }
+          const float G = __expf(s_b[t]), fq = G * kInvSqrtD, fk = -G * s_beta[t];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+              dQ[mt][jj][2 * e + x] = fmaf(fq, tq8[mt][jj][2 * e + x], dQ[mt][jj][2 * e + x]);
+              dK[mt][jj][2 * e + x] = fmaf(fk, tp8[mt][jj][2 * e + x], dK[mt][jj][2 * e + x]);
+            }
         }
-      }
     }
 
     // <dS_end, S0>
@@ -735,12 +774,12 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
     {
       float aD[4][4], col[4][2];
       mm::zero(aD);
-      mm::warp_mma<false, true, 4>(aD, aDO, kLd, aU, kLd, m0, an0, kDim);
+      mm::warp_mma<false, true, 4>(aD, aDO, kLd, aU, kLd, am0, an0, kDim);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) col[jj][0] = col[jj][1] = 0.f;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int t = m0 + gq + 8 * e;
+        const int t = am0 + gq + 8 * e;
         const float bt = s_b[t];
         float row = 0.f;
 #pragma unroll
@@ -768,7 +807,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
       for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
         for (int e = 0; e < 2; ++e)
-          *reinterpret_cast<__half2*>(sP0 + (m0 + gq + 8 * e) * kLd64 + an0 + 8 * jj + 2 * tq) =
+          *reinterpret_cast<__half2*>(sP0 + (am0 + gq + 8 * e) * kLd64 + an0 + 8 * jj + 2 * tq) =
               __floats2half2_rn(aD[jj][2 * e], aD[jj][2 * e + 1]);
     }
 
@@ -776,12 +815,12 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
     {
       float aF[4][4], col[4][2];
       mm::zero(aF);
-      mm::warp_mma<false, true, 4>(aF, aDU, kLd, aU, kLd, m0, an0, kDim);
+      mm::warp_mma<false, true, 4>(aF, aDU, kLd, aU, kLd, am0, an0, kDim);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) col[jj][0] = col[jj][1] = 0.f;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int t = m0 + gq + 8 * e;
+        const int t = am0 + gq + 8 * e;
         const float bt = s_b[t], be = s_beta[t];
         float rf = 0.f, rz = 0.f;
 #pragma unroll
@@ -814,38 +853,40 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
       for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
         for (int e = 0; e < 2; ++e)
-          *reinterpret_cast<__half2*>(sP1 + (m0 + gq + 8 * e) * kLd64 + an0 + 8 * jj + 2 * tq) =
+          *reinterpret_cast<__half2*>(sP1 + (am0 + gq + 8 * e) * kLd64 + an0 + 8 * jj + 2 * tq) =
               __floats2half2_rn(aF[jj][2 * e], aF[jj][2 * e + 1]);
     }
     __syncthreads();  // dA and E are in shared memory
 
     // dQ += dA K; dK += E K + E^T K + dA^T Q + (gamma / Gamma) u dS_end^T
-    mm::warp_mma<false, false, 8>(dQ, aP0, kLd64, aK, kLd, m0, n0, kChunk);
-    mm::warp_mma<false, false, 8>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
-    mm::warp_mma<true, false, 8>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
-    mm::warp_mma<true, false, 8>(dK, aP0, kLd64, aQ, kLd, m0, n0, kChunk);
+    mm::warp_mma2<false, false, 4>(dQ, aP0, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma2<false, false, 4>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma2<true, false, 4>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma2<true, false, 4>(dK, aP0, kLd64, aQ, kLd, m0, n0, kChunk);
     {
-      float uD[8][4];
+      float uD[2][4][4];
       mm::zero(uD);
-      mm::warp_mma<false, true, 8>(uD, aU, kLd, aE, kLd, m0, n0, kDim);
+      mm::warp_mma2<false, true, 4>(uD, aU, kLd, aE, kLd, m0, n0, kDim);
       const float blast = s_b[kChunk - 1];
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = m0 + gq + 8 * e;
-        const float sc = __expf(blast - s_b[t]);
-        float rw = 0.f;
+      for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int colx = n0 + 8 * jj + 2 * tq;
-          const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + colx));
-          const float a = sc * uD[jj][2 * e], b = sc * uD[jj][2 * e + 1];
-          dK[jj][2 * e] += a;
-          dK[jj][2 * e + 1] += b;
-          rw = fmaf(k2.x, a, fmaf(k2.y, b, rw));
+        for (int e = 0; e < 2; ++e) {
+          const int t = m0 + 16 * mt + gq + 8 * e;
+          const float sc = __expf(blast - s_b[t]);
+          float rw = 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int colx = n0 + 8 * jj + 2 * tq;
+            const float2 k2 = __half22float2(*reinterpret_cast<const __half2*>(sK + t * kLd + colx));
+            const float a = sc * uD[mt][jj][2 * e], b = sc * uD[mt][jj][2 * e + 1];
+            dK[mt][jj][2 * e] += a;
+            dK[mt][jj][2 * e + 1] += b;
+            rw = fmaf(k2.x, a, fmaf(k2.y, b, rw));
+          }
+          rw = bc_quad_sum(rw);
+          if (tq == 0) atomicAdd(&s_rw[t], rw);
         }
-        rw = bc_quad_sum(rw);
-        if (tq == 0) atomicAdd(&s_rw[t], rw);
-      }
     }
     // du'_t . v_t: four threads per token, 32 columns each
     {
@@ -907,18 +948,20 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
     __syncthreads();  // the next value head reuses the tiles and the sums
   }
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int t = m0 + gq + 8 * e;
-    if (t < n) {
-      float* qrow = p.dq + (r0 + t) * krow + kh * kDim + n0 + 2 * tq;
-      float* krw = p.dk + (r0 + t) * krow + kh * kDim + n0 + 2 * tq;
+  for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        *reinterpret_cast<float2*>(qrow + 8 * jj) = make_float2(dQ[jj][2 * e], dQ[jj][2 * e + 1]);
-        *reinterpret_cast<float2*>(krw + 8 * jj) = make_float2(dK[jj][2 * e], dK[jj][2 * e + 1]);
+    for (int e = 0; e < 2; ++e) {
+      const int t = m0 + 16 * mt + gq + 8 * e;
+      if (t < n) {
+        float* qrow = p.dq + (r0 + t) * krow + kh * kDim + n0 + 2 * tq;
+        float* krw = p.dk + (r0 + t) * krow + kh * kDim + n0 + 2 * tq;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          *reinterpret_cast<float2*>(qrow + 8 * jj) = make_float2(dQ[mt][jj][2 * e], dQ[mt][jj][2 * e + 1]);
+          *reinterpret_cast<float2*>(krw + 8 * jj) = make_float2(dK[mt][jj][2 * e], dK[mt][jj][2 * e + 1]);
+        }
       }
     }
-  }
 }
 
 }  // namespace gdn

@@ -96,10 +96,68 @@ __device__ __forceinline__ void warp_mma(float (&c)[NT][4], uint32_t a, int lda,
   }
 }
 
+// Two m16 row tiles per warp: c[m][j] += A[m0 + 16 m : +16, 0 : K] * B[0 : K, n0 + 8 j : +8].
+// Each B fragment feeds both row tiles, halving B's shared-memory traffic per MMA.
+template <bool kAT, bool kBT, int NT>
+__device__ __forceinline__ void warp_mma2(float (&c)[2][NT][4], uint32_t a, int lda, uint32_t b, int ldb, int m0,
+                                          int n0, int K) {
+  static_assert(NT % 2 == 0, "B operands are loaded two n8 tiles at a time");
+  const int lane = threadIdx.x & 31;
+  uint32_t a_lane, b_lane;
+  int a_step, b_step;
+  uint32_t a_next;  // bytes from row tile 0 to row tile 1
+  if (!kAT) {
+    a_lane = a + 2u * static_cast<uint32_t>((m0 + (lane & 15)) * lda + (lane >> 4) * 8);
+    a_step = 32;
+    a_next = 32u * lda;
+  } else {
+    a_lane = a + 2u * static_cast<uint32_t>(((lane & 7) + ((lane >> 4) << 3)) * lda + m0 + ((lane >> 3) & 1) * 8);
+    a_step = 32 * lda;
+    a_next = 32u;
+  }
+  if (kBT) {
+    b_lane = b + 2u * static_cast<uint32_t>((n0 + (lane & 7) + ((lane >> 4) << 3)) * ldb + ((lane >> 3) & 1) * 8);
+    b_step = 32;
+  } else {
+    b_lane = b + 2u * static_cast<uint32_t>((lane & 15) * ldb + n0 + (lane >> 4) * 8);
+    b_step = 32 * ldb;
+  }
+  const uint32_t b_pair = kBT ? 32u * ldb : 32u;
+#pragma unroll 2
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t af0[4], af1[4];
+    if (!kAT) {
+      ldsm_x4(a_lane, af0);
+      ldsm_x4(a_lane + a_next, af1);
+    } else {
+      ldsm_x4_t(a_lane, af0);
+      ldsm_x4_t(a_lane + a_next, af1);
+    }
+#pragma unroll
+    for (int j = 0; j < NT / 2; ++j) {
+      uint32_t bf[4];
+      if (kBT) ldsm_x4(b_lane + j * b_pair, bf);
+      else ldsm_x4_t(b_lane + j * b_pair, bf);
+      mma16816(c[0][2 * j], af0, bf[0], bf[1]);
+      mma16816(c[0][2 * j + 1], af0, bf[2], bf[3]);
+      mma16816(c[1][2 * j], af1, bf[0], bf[1]);
+      mma16816(c[1][2 * j + 1], af1, bf[2], bf[3]);
+    }
+    a_lane += a_step;
+    b_lane += b_step;
+  }
+}
+
 template <int NT>
 __device__ __forceinline__ void zero(float (&c)[NT][4]) {
 #pragma unroll
   for (int j = 0; j < NT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+}
+
+template <int NT>
+__device__ __forceinline__ void zero(float (&c)[2][NT][4]) {
+  zero(c[0]);
+  zero(c[1]);
 }
 
 // 16-byte global -> shared copy that bypasses the registers; with valid = false
