@@ -228,7 +228,8 @@ def backward_workspace_bytes(B, T, nv, varlen, dk=128, dv=128) -> int:
 def backward(q, k, v, g, beta, h0, dout, dq, dk, dv, dg, dbeta, *, nk: int, nv: int, dST=None, dh0=None,
              B: int | None = None, T: int | None = None, cu_seqlens=None, state_is_table: bool = False,
              workspace=None, stream=None, dk_dim: int = 128, dv_dim: int = 128) -> None:
-    """Enqueue the backward of ``prefill`` (``gdn_prefill_backward``).
+    """Enqueue the backward of ``prefill`` (``gdn_prefill_backward``): the chunked form
+    on the tensor cores, 4 launches (5 with ``cu_seqlens``).
 
     q, k, v, g, beta, cu_seqlens, state_is_table: as ``prefill``; ``h0`` is the initial
     state the forward started from. ``dout`` fp32 [rows, nv*dv] (dL/do), ``dST`` fp32
