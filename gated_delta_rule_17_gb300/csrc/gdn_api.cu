@@ -22,6 +22,7 @@
 #include "gdn_wy_kernel.cuh"
 #include "gdn_decode_kernel.cuh"
 #include "gdn_bwd_chunk_kernel.cuh"
+#include "gdn_bwd_dstates_tc.cuh"
 
 namespace {
 
@@ -89,7 +90,7 @@ int device_info(DeviceInfo** out) {
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     const std::pair<const void*, int> bwd[] = {
         {reinterpret_cast<const void*>(gdn::gdn_bwd_states_kernel), gdn::kStatesSmem},
-        {reinterpret_cast<const void*>(gdn::gdn_bwd_dstates_kernel), gdn::kDStatesSmem},
+        {reinterpret_cast<const void*>(gdn::gdn_bwd_dstates_tc_kernel), gdn::DsPlan::DYN_SMEM},
         {reinterpret_cast<const void*>(gdn::gdn_bwd_grads_kernel), gdn::kGradsSmem}};
     for (const auto& f : bwd) {
       e = cudaFuncSetAttribute(f.first, cudaFuncAttributeMaxDynamicSharedMemorySize, f.second);
@@ -741,7 +742,8 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   if (rows > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "%lld token rows exceed the 2^31 TMA coordinate range", (long long)rows);
   const BwdLayout l = bwd_layout(B, T, nv, cu_seqlens != nullptr);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  CUtensorMap mk;
+  CUtensorMap mq, mk;
+  if (int rc = make_map(&mq, q, static_cast<int64_t>(nk) * gdn::kDim, rows, r.q, "q")) return rc;
   if (int rc = make_map(&mk, k, static_cast<int64_t>(nk) * gdn::kDim, rows, r.k, "k")) return rc;
   gdn::WyParams w;
   int64_t wy_grid = 0;
@@ -823,7 +825,7 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   gdn::gdn_wy_kernel<<<static_cast<unsigned>(wy_grid), gdn::kWyThreads, gdn::WyPlan::DYN_SMEM, s>>>(mk, w);
   const unsigned chains = static_cast<unsigned>(static_cast<int64_t>(B) * nv);
   gdn::gdn_bwd_states_kernel<<<chains, gdn::kBcThreads, gdn::kStatesSmem, s>>>(p);
-  gdn::gdn_bwd_dstates_kernel<<<chains, gdn::kBcThreads, gdn::kDStatesSmem, s>>>(p);
+  gdn::gdn_bwd_dstates_tc_kernel<<<chains, gdn::kDsThreads, gdn::DsPlan::DYN_SMEM, s>>>(mq, mk, p);
   gdn::gdn_bwd_grads_kernel<<<static_cast<unsigned>(grad_items), gdn::kBcThreads, gdn::kGradsSmem, s>>>(p);
   launches += 4;
   int rc = GDN_OK;

@@ -32,14 +32,16 @@
 //     dg_t = sum of d b over the chunk's tokens t .. 63
 //
 // Three kernels: gdn_bwd_states_kernel runs the forward chain once per (sequence,
-// v-head), storing every chunk's entry state S0 and u; gdn_bwd_dstates_kernel runs
-// the reverse chain, storing every chunk's dS_end and du' and writing dV;
+// v-head), storing every chunk's entry state S0 and u; gdn_bwd_dstates_tc_kernel
+// (gdn_bwd_dstates_tc.cuh, on tcgen05) runs the reverse chain, storing every chunk's
+// dS_end and du' and writing dV;
 // gdn_bwd_grads_kernel takes one (chunk, key head) each and writes dQ, dK (summed
 // over the key head's GQA group of value heads), and dbeta and dg of every value head.
-// T comes from the forward's WY kernel (unscaled by beta). Every contraction is an
-// fp16 tensor-core product with fp32 accumulation (gdn_mma.cuh); the two chains
-// carry their state in fp32 registers and feed it to the tensor cores as an fp16
-// hi + lo pair, as do the operands that enter the chains (T, beta X, u, du, r).
+// T comes from the forward's WY kernel (unscaled by beta). In the two kernels here
+// every contraction is an fp16 tensor-core product with fp32 accumulation
+// (gdn_mma.cuh); the forward chain carries its state in fp32 registers and feeds it
+// to the tensor cores as an fp16 hi + lo pair, as it does the operands that enter
+// the chain (T, beta X, u).
 //
 // Padding tokens of a ragged last chunk are loaded as q = k = v = dO = 0,
 // g = beta = 0, and T's rows past the chunk's end as 0: every product then
@@ -393,200 +395,6 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const Bwd
       bc_store_split2<8>(S, sSh, sSl, kLd, sm0, sn0);
     }
     __syncthreads();
-  }
-}
-
-// ---- reverse chain: every chunk's dS_end and du', and dV ----------------------------
-// One CTA per (sequence, v-head), walking the chunks from the last; dS lives in fp32
-// registers like the forward chain's state. It needs no forward state.
-constexpr int kDStatesSmem = 4 * kTile128 + 3 * kTile64 + 2 * kTileState + 2 * kTile128;
-
-__global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_dstates_kernel(const BwdChunkParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __half* sQ = reinterpret_cast<__half*>(smem);
-  __half* sK = sQ + kChunk * kLd;
-  __half* sDO = sK + kChunk * kLd;
-  __half* sDOs = sDO + kChunk * kLd;  // Gamma dO / sqrt(dk)
-  __half* sTh = sDOs + kChunk * kLd;
-  __half* sTl = sTh + kChunk * kLd64;
-  __half* sA = sTl + kChunk * kLd64;  // (Q K^T . M) / sqrt(dk)
-  __half* sDSh = sA + kChunk * kLd64;
-  __half* sDSl = sDSh + kDim * kLd;
-  __half* sDUh = sDSl + kDim * kLd;  // du, then -Gamma r
-  __half* sDUl = sDUh + kChunk * kLd;
-  __shared__ float s_b[kChunk], s_beta[kChunk];
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-  const int si = blockIdx.x / p.nv, h = blockIdx.x % p.nv, kh = h / (p.nv / p.nk);
-  const int s = p.order ? p.order[si] : si;
-  int64_t row0, len;
-  if (!bc_sequence(p, s, row0, len)) return;
-  const int64_t nch = (len + kChunk - 1) / kChunk;
-  const int64_t hrow = static_cast<int64_t>(p.nv) * kDim;
-  const int sm0 = 32 * (warp & 3), sn0 = 64 * (warp >> 2);  // state tile
-  const int m0 = 32 * (warp & 1), n0 = 32 * (warp >> 1);    // 64 x 128 products
-  const int am0 = 16 * (warp & 3), an0 = 32 * (warp >> 2);  // 64 x 64 products
-  const uint32_t aQ = mm::saddr(sQ), aK = mm::saddr(sK), aDO = mm::saddr(sDO), aDOs = mm::saddr(sDOs),
-                 aTh = mm::saddr(sTh), aTl = mm::saddr(sTl), aA = mm::saddr(sA), aDSh = mm::saddr(sDSh),
-                 aDSl = mm::saddr(sDSl), aDUh = mm::saddr(sDUh), aDUl = mm::saddr(sDUl);
-
-  float dS[2][8][4];
-  {
-    const float* d0 = p.dst ? p.dst + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim : nullptr;
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float2 x = make_float2(0.f, 0.f);
-          if (d0) x = *reinterpret_cast<const float2*>(d0 + (sm0 + 16 * mt + gq + 8 * e) * kDim + sn0 + 8 * j + 2 * tq);
-          dS[mt][j][2 * e] = x.x;
-          dS[mt][j][2 * e + 1] = x.y;
-        }
-  }
-  bc_store_split2<8>(dS, sDSh, sDSl, kLd, sm0, sn0);
-
-  BcRows16 fq, fk, ft;
-  BcRows32 fd;
-  BcGates fg;
-  auto fetch = [&](int64_t c) {
-    const int64_t r0 = row0 + c * kChunk;
-    const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
-    bc_fetch16(fq, p.q + r0 * p.q_stride + kh * kDim, p.q_stride, n);
-    bc_fetch16(fk, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
-    bc_fetch16(ft, p.tm + r0 * hrow + h * kDim, hrow, n);
-    bc_fetch32(fd, p.dout + r0 * hrow + h * kDim, hrow, n);
-    bc_fetch_gates(fg, p, r0, n, h);
-  };
-  if (nch > 0) fetch(nch - 1);
-  __syncthreads();
-
-  for (int64_t c = nch - 1; c >= 0; --c) {
-    const int64_t r0 = row0 + c * kChunk;
-    const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
-    bc_store_state(p.dsbuf + (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim, sDSh);
-    {
-      const GatePrefix gp = bc_put_gates(fg, s_b, s_beta);
-      bc_put_bf16_as_f16(sQ, fq);
-      bc_put_bf16_as_f16(sK, fk);
-      bc_put_t(sTh, sTl, ft);
-      bc_put_f32(sDO, fd, [](int) { return 1.f; });
-      bc_put_f32(sDOs, fd, [&](int row) { return __expf(bc_b_of(gp, row)) * kInvSqrtD; });
-    }
-    __syncthreads();
-
-    // (Q K^T . M) / sqrt(dk), lower triangle with the diagonal
-    {
-      float acc[4][4];
-      mm::zero(acc);
-      mm::warp_mma<false, true, 4>(acc, aQ, kLd, aK, kLd, am0, an0, kDim);
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = am0 + gq + 8 * e;
-        const float bt = s_b[t];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int jj = an0 + 8 * j + 2 * tq;
-          const float x0 = jj <= t ? acc[j][2 * e] * __expf(bt - s_b[jj]) * kInvSqrtD : 0.f;
-          const float x1 = jj + 1 <= t ? acc[j][2 * e + 1] * __expf(bt - s_b[jj + 1]) * kInvSqrtD : 0.f;
-          *reinterpret_cast<__half2*>(sA + t * kLd64 + jj) = __floats2half2_rn(x0, x1);
-        }
-      }
-    }
-    __syncthreads();
-
-    // du = A~^T dO + (gamma / Gamma) K dS, as fp16 hi + lo
-    {
-      float a1[2][4][4], a2[2][4][4];
-      mm::zero(a1);
-      mm::zero(a2);
-      mm::warp_mma2<true, false, 4>(a1, aA, kLd64, aDO, kLd, m0, n0, kChunk);
-      mm::warp_mma2<false, false, 4>(a2, aK, kLd, aDSh, kLd, m0, n0, kDim);
-      mm::warp_mma2<false, false, 4>(a2, aK, kLd, aDSl, kLd, m0, n0, kDim);
-      const float blast = s_b[kChunk - 1];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float sc = __expf(blast - s_b[m0 + 16 * mt + gq + 8 * e]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            a1[mt][j][2 * e] = fmaf(sc, a2[mt][j][2 * e], a1[mt][j][2 * e]);
-            a1[mt][j][2 * e + 1] = fmaf(sc, a2[mt][j][2 * e + 1], a1[mt][j][2 * e + 1]);
-          }
-        }
-      bc_store_split2<4>(a1, sDUh, sDUl, kLd, m0, n0);
-    }
-    __syncthreads();
-
-    // du' = T^T du (stored), dV = beta du', then -Gamma beta du' as fp16 hi + lo
-    {
-      float acc[2][4][4];
-      mm::zero(acc);
-      mm::warp_mma2<true, false, 4>(acc, aTh, kLd64, aDUh, kLd, m0, n0, kChunk);
-      mm::warp_mma2<true, false, 4>(acc, aTh, kLd64, aDUl, kLd, m0, n0, kChunk);
-      mm::warp_mma2<true, false, 4>(acc, aTl, kLd64, aDUh, kLd, m0, n0, kChunk);
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = m0 + 16 * mt + gq + 8 * e;
-          if (t < n) {
-            const float bt = s_beta[t];
-            __half* drow = p.dubuf + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
-            float* vrow = p.dv + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              *reinterpret_cast<__half2*>(drow + 8 * j) = __floats2half2_rn(acc[mt][j][2 * e], acc[mt][j][2 * e + 1]);
-              *reinterpret_cast<float2*>(vrow + 8 * j) = make_float2(bt * acc[mt][j][2 * e], bt * acc[mt][j][2 * e + 1]);
-            }
-          }
-        }
-      __syncthreads();  // every warp has read du
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = m0 + 16 * mt + gq + 8 * e;
-          const float sc = -__expf(s_b[t]) * s_beta[t];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[mt][j][2 * e] *= sc;
-            acc[mt][j][2 * e + 1] *= sc;
-          }
-        }
-      bc_store_split2<4>(acc, sDUh, sDUl, kLd, m0, n0);
-    }
-    __syncthreads();
-    if (c > 0) fetch(c - 1);  // in flight during the state update
-
-    // dS = gamma dS + Q^T (Gamma dO / sqrt(dk)) - K^T (Gamma r)
-    {
-      const float gam = __expf(s_b[kChunk - 1]);
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int x = 0; x < 4; ++x) dS[mt][j][x] *= gam;
-      mm::warp_mma2<true, false, 8>(dS, aQ, kLd, aDOs, kLd, sm0, sn0, kChunk);
-      mm::warp_mma2<true, false, 8>(dS, aK, kLd, aDUh, kLd, sm0, sn0, kChunk);
-      mm::warp_mma2<true, false, 8>(dS, aK, kLd, aDUl, kLd, sm0, sn0, kChunk);
-      bc_store_split2<8>(dS, sDSh, sDSl, kLd, sm0, sn0);
-    }
-    __syncthreads();
-  }
-  if (p.dh0) {
-    float* d = p.dh0 + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim;
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          *reinterpret_cast<float2*>(d + (sm0 + 16 * mt + gq + 8 * e) * kDim + sn0 + 8 * j + 2 * tq) =
-              make_float2(dS[mt][j][2 * e], dS[mt][j][2 * e + 1]);
   }
 }
 
