@@ -1,7 +1,7 @@
 // Reverse chain of the chunked backward on the 5th-generation tensor cores.
 //
-// The same recurrence as gdn_bwd_dstates_kernel (see gdn_bwd_chunk_kernel.cuh), per
-// chunk c from the last:
+// The reverse chain of the chunk-level derivative (derived in the header of
+// gdn_bwd_chunk_kernel.cuh), per chunk c from the last:
 //
 //     du  = (Q K^T . M)^T dO / sqrt(dk) + (gamma / Gamma) K dS_end
 //     du' = T^T du,  dV = beta du'
