@@ -33,13 +33,13 @@ struct DsPlan {
   static constexpr int KQ0 = 0;            // [K;Q] bf16: 2 k-blocks of 128 rows x 128 B
   static constexpr int KQ1 = 32768;
   static constexpr int DO16 = 65536;       // dO fp16 [t][v]: 2 v-blocks of 64 rows x 128 B
-  static constexpr int DOSH = 81920;       // Gamma dO / sqrt(dk), bf16 hi, same layout
-  static constexpr int DOSL = 98304;       // ... lo
-  static constexpr int AT = 114688;        // A~ fp16 [t'][t]: 64 rows x 128 B
-  static constexpr int TB0 = 122880;       // T fp16 [i][t]: hi, then lo at +8192
-  static constexpr int TB1 = 139264;
-  static constexpr int DOST = 155648;      // dO fp32 staging, row-major 64 x 512 B
-  static constexpr int BYTES = 188416;
+  static constexpr int DOS0 = 81920;       // Gamma dO / sqrt(dk), bf16 hi, then lo at +16384;
+  static constexpr int DOS1 = 114688;      //   two buffers by chunk parity
+  static constexpr int AT = 147456;        // A~ fp16 [t'][t]: 64 rows x 128 B
+  static constexpr int TB0 = 155648;       // T fp16 [i][t]: hi, then lo at +8192
+  static constexpr int TB1 = 172032;
+  static constexpr int DOST = 188416;      // dO fp32 staging, row-major 64 x 512 B
+  static constexpr int BYTES = 221184;
   static constexpr int DYN_SMEM = BYTES + 1024;  // slack for 1024-byte alignment
   // tensor-memory columns
   static constexpr uint32_t COL_DS = 0;    // dS^T fp32 (128)
@@ -68,7 +68,7 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
   // per token: log-decay prefix b, beta, Gamma / sqrt(dk), gamma / Gamma, -Gamma beta
   __shared__ float s_b[kChunk], s_beta[kChunk], s_sc[kChunk], s_gd[kChunk], s_ngb[kChunk];
   __shared__ float s_gam;
-  __shared__ __align__(8) uint64_t s_mb[6];
+  __shared__ __align__(8) uint64_t s_mb[7];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, part = warp >> 2;  // lane quarter; column quarter
@@ -85,12 +85,12 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
   const uint32_t sb = tc::smem_u32(sm);
   const uint32_t mb_kq0 = tc::smem_u32(&s_mb[0]), mb_kq1 = tc::smem_u32(&s_mb[1]);
   const uint32_t mb_a = tc::smem_u32(&s_mb[2]), mb_b = tc::smem_u32(&s_mb[3]), mb_c = tc::smem_u32(&s_mb[4]),
-                 mb_d = tc::smem_u32(&s_mb[5]);
+                 mb_d = tc::smem_u32(&s_mb[5]), mb_g = tc::smem_u32(&s_mb[6]);
 
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), P::TMEM_COLS);
   if (tid == 0) {
 #pragma unroll
-    for (int i = 0; i < 6; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), 1);
+    for (int i = 0; i < 7; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), 1);
     tc::mbar_fence_init();
   }
   tc::fence_before_sync();
@@ -151,55 +151,31 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
     tc::fence_after_sync();
   };
 
-  // ---- dS^T from dL/dS_T (or zero), and its bf16 hi + lo operand copy ----------------------
-  {
-    const float* d0 = p.dst ? p.dst + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim : nullptr;
-    uint32_t x[32], hi[16], lo[16];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(d0 ? d0[(part * 32 + e) * kDim + v] : 0.f);
-    tc::tmem_st32(lanes + P::COL_DS + part * 32, x);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) split_bf162(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]), hi[e], lo[e]);
-    tc::tmem_st16u(lanes + P::COL_DSH + part * 16, hi);
-    tc::tmem_st16u(lanes + P::COL_DSL + part * 16, lo);
-    tc::tmem_st_wait();
-  }
-  if (nch > 0) {
-    if (tid == 0) issue_kq(nch - 1);
-    issue_copies(nch - 1);
-  }
-
-  for (int it = 0; it < nch && ok; ++it) {
-    const int c = nch - 1 - it;
+  // Per-token factors of chunk c (warp 0) and its dO operands from the staged rows.
+  auto gates = [&](int c) {
     const int n = chunk_len(c);
     const int64_t r0 = row0 + static_cast<int64_t>(c) * kChunk;
-    const uint32_t ph = static_cast<uint32_t>(it) & 1u;
-
-    // ---- per-token factors; the chunk's dO and T have landed ---------------------------------
-    if (warp == 0) {
-      const int t0 = 2 * lane, t1 = t0 + 1;
-      const float g0 = t0 < n ? p.g[(r0 + t0) * p.g_stride + h] : 0.f;
-      const float g1 = t1 < n ? p.g[(r0 + t1) * p.g_stride + h] : 0.f;
-      const float be0 = t0 < n ? p.beta[(r0 + t0) * p.beta_stride + h] : 0.f;
-      const float be1 = t1 < n ? p.beta[(r0 + t1) * p.beta_stride + h] : 0.f;
-      const GatePrefix gp = gate_prefix(g0, g1);
-      const float e0 = __expf(gp.gca), e1 = __expf(gp.gcb);
-      s_b[t0] = gp.gca;
-      s_b[t1] = gp.gcb;
-      s_beta[t0] = be0;
-      s_beta[t1] = be1;
-      s_sc[t0] = e0 * kInvSqrtD;
-      s_sc[t1] = e1 * kInvSqrtD;
-      s_gd[t0] = __expf(gp.last - gp.gca);
-      s_gd[t1] = __expf(gp.last - gp.gcb);
-      s_ngb[t0] = -e0 * be0;
-      s_ngb[t1] = -e1 * be1;
-      if (lane == 0) s_gam = __expf(gp.last);
-    }
-    mm::cp_async_wait_all();
-    __syncthreads();
-
-    // ---- dO as fp16 and (Gamma / sqrt(dk)) dO as bf16 hi + lo, swizzled ---------------------
+    const int t0 = 2 * lane, t1 = t0 + 1;
+    const float g0 = t0 < n ? p.g[(r0 + t0) * p.g_stride + h] : 0.f;
+    const float g1 = t1 < n ? p.g[(r0 + t1) * p.g_stride + h] : 0.f;
+    const float be0 = t0 < n ? p.beta[(r0 + t0) * p.beta_stride + h] : 0.f;
+    const float be1 = t1 < n ? p.beta[(r0 + t1) * p.beta_stride + h] : 0.f;
+    const GatePrefix gp = gate_prefix(g0, g1);
+    const float e0 = __expf(gp.gca), e1 = __expf(gp.gcb);
+    s_b[t0] = gp.gca;
+    s_b[t1] = gp.gcb;
+    s_beta[t0] = be0;
+    s_beta[t1] = be1;
+    s_sc[t0] = e0 * kInvSqrtD;
+    s_sc[t1] = e1 * kInvSqrtD;
+    s_gd[t0] = __expf(gp.last - gp.gca);
+    s_gd[t1] = __expf(gp.last - gp.gcb);
+    s_ngb[t0] = -e0 * be0;
+    s_ngb[t1] = -e1 * be1;
+    if (lane == 0) s_gam = __expf(gp.last);
+  };
+  auto convert_do = [&](int c) {  // dO as fp16 and (Gamma / sqrt(dk)) dO as bf16 hi + lo
+    uint8_t* dos = sm + ((c & 1) ? P::DOS1 : P::DOS0);
 #pragma unroll
     for (int i = 0; i < 1024 / kDsThreads; ++i) {
       const int idx = tid + kDsThreads * i, row = idx >> 4, c8 = idx & 15;
@@ -215,89 +191,148 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
       }
       const uint32_t o = (c8 >> 3) * 8192 + tc::sw128(row, (c8 & 7) * 16);
       *reinterpret_cast<uint4*>(sm + P::DO16 + o) = make_uint4(h16[0], h16[1], h16[2], h16[3]);
-      *reinterpret_cast<uint4*>(sm + P::DOSH + o) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
-      *reinterpret_cast<uint4*>(sm + P::DOSL + o) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
+      *reinterpret_cast<uint4*>(dos + o) = make_uint4(bh[0], bh[1], bh[2], bh[3]);
+      *reinterpret_cast<uint4*>(dos + 16384 + o) = make_uint4(bl[0], bl[1], bl[2], bl[3]);
     }
-    // ---- dS_end of this chunk out (fp16, [k][v]), then dS^T <- gamma dS^T --------------------
-    {
-      const float gam = s_gam;
-      __half* dsrow = p.dsbuf + (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim + v;
-      uint32_t x[32];
-      tc::tmem_ld32(lanes + P::COL_DS + part * 32, x);
-      tc::tmem_ld_wait();
+  };
+  // The state gradient in COL_DS is dS_end of chunk c: stage it (fp16, [k][v], in the
+  // dO staging buffer, which is free until the next chunk's copies), make its bf16 hi + lo
+  // copy (chunk c's P2 operand) and decay it by chunk c's gamma (for P4).
+  auto state_pass = [&](const uint32_t (&x)[32]) {
+    const float gam = s_gam;
+    __half* stage = reinterpret_cast<__half*>(sm + P::DOST) + v;
+    uint32_t hi[16], lo[16], y[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float f = __uint_as_float(x[e]);
-        dsrow[(part * 32 + e) * kDim] = __float2half_rn(f);
-        x[e] = __float_as_uint(gam * f);
-      }
-      tc::tmem_st32(lanes + P::COL_DS + part * 32, x);
-      tc::tmem_st_wait();
+    for (int e = 0; e < 16; ++e) {
+      const float f0 = __uint_as_float(x[2 * e]), f1 = __uint_as_float(x[2 * e + 1]);
+      stage[(part * 32 + 2 * e) * kDim] = __float2half_rn(f0);
+      stage[(part * 32 + 2 * e + 1) * kDim] = __float2half_rn(f1);
+      split_bf162(f0, f1, hi[e], lo[e]);
+      y[2 * e] = __float_as_uint(gam * f0);
+      y[2 * e + 1] = __float_as_uint(gam * f1);
     }
+    tc::tmem_st16u(lanes + P::COL_DSH + part * 16, hi);
+    tc::tmem_st16u(lanes + P::COL_DSL + part * 16, lo);
+    tc::tmem_st32(lanes + P::COL_DS + part * 32, y);
+    tc::tmem_st_wait();
+  };
+
+  // Gram of chunk c (thread 0), once its K/Q tile has landed; false on expiry
+  auto issue_gram = [&](int c) {
+    const int b = c & 1;
+    const bool w = tc::mbar_wait_timed(b ? mb_kq1 : mb_kq0, (kq_phase >> b) & 1u, kWaitLimitNs);
+    kq_phase ^= 1u << b;
+    if (!w) return false;
+    tc::fence_after_sync();
+    // descriptors step by adding (byte offset >> 4) to the start-address field
+    const uint64_t dkq = tc::desc_sw128(sb + (b ? P::KQ1 : P::KQ0), 16, 1024);
+    constexpr uint32_t id_g = tc::idesc_f16(128, 64, tc::kBF16, false, false);
+#pragma unroll
+    for (int st = 0; st < 8; ++st) {
+      const uint64_t a = dkq + (((st >> 2) * 16384 + (st & 3) * 32) >> 4);
+      tc::mma_f16(tmem + P::COL_G, a, a, id_g, st > 0);
+    }
+    tc::mma_commit(mb_g);
+    return true;
+  };
+  // A~ of chunk c from the Gram (lanes 64-127, rows t'), 16 columns per warp
+  auto a_tilde = [&](int c) {
+    if (quarter < 2) return;
+    const int n = chunk_len(c);
+    const int tp = v - 64;
+    const float bt = s_b[tp];
+    float d[16];
+    tc::tmem_ld16(lanes + P::COL_G + part * 16, d);
+    tc::tmem_ld_wait();
+    uint32_t pk[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int j0 = part * 16 + 2 * e, j1 = j0 + 1;
+      const float a0 = (j0 <= tp && tp < n) ? d[2 * e] * __expf(bt - s_b[j0]) * kInvSqrtD : 0.f;
+      const float a1 = (j1 <= tp && tp < n) ? d[2 * e + 1] * __expf(bt - s_b[j1]) * kInvSqrtD : 0.f;
+      pk[e] = pack_half2(a0, a1);
+    }
+    *reinterpret_cast<uint4*>(sm + P::AT + tc::sw128(tp, part * 32)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    *reinterpret_cast<uint4*>(sm + P::AT + tc::sw128(tp, part * 32 + 16)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  };
+  auto issue_p1 = [&]() {  // P1 = dO^T A~ onto the Gram columns (thread 0)
+    constexpr uint32_t id_1 = tc::idesc_f16(128, 64, tc::kF16, true, true);
+    const uint64_t ddo = tc::desc_sw128(sb + P::DO16, 8192, 1024), dat = tc::desc_sw128(sb + P::AT, 8192, 1024);
+#pragma unroll
+    for (int st = 0; st < 4; ++st) tc::mma_f16(tmem + P::COL_G, ddo + st * 128, dat + st * 128, id_1, st > 0);
+    tc::mma_commit(mb_b);
+  };
+  uint32_t g_count = 0;  // completions of mb_g waited so far
+
+  // ---- the last chunk: operands, dS_end = dL/dS_T (or zero), its Gram, A~ and P1 --------------
+  if (nch > 0) {
+    if (tid == 0) {
+      issue_kq(nch - 1);
+      if (nch > 1) issue_kq(nch - 2);
+    }
+    issue_copies(nch - 1);
+    if (warp == 0) gates(nch - 1);
+    mm::cp_async_wait_all();
+    __syncthreads();
+    convert_do(nch - 1);
+    const float* d0 = p.dst ? p.dst + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim : nullptr;
+    uint32_t x[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(d0 ? d0[(part * 32 + e) * kDim + v] : 0.f);
+    __syncthreads();  // the staging buffer's dO rows are converted
+    state_pass(x);
     tc::fence_proxy_async();
     sync_tmem();
+    if (tid == 0 && !issue_gram(nch - 1)) {
+      atomicOr(p.status, kStatusTimeout);
+      ok = false;
+    }
+    if (wait_mb(mb_g, g_count++ & 1u)) {
+      a_tilde(nch - 1);
+      tc::fence_proxy_async();
+      sync_tmem();
+      if (tid == 0) issue_p1();
+    }
+  } else {
+    const float* d0 = p.dst ? p.dst + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim : nullptr;
+    uint32_t x[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) x[e] = __float_as_uint(d0 ? d0[(part * 32 + e) * kDim + v] : 0.f);
+    tc::tmem_st32(lanes + P::COL_DS + part * 32, x);
+    tc::tmem_st_wait();
+    sync_tmem();
+  }
 
-    // ---- Gram and P2, once this chunk's K/Q have landed; the next chunk's copies -------------
+  for (int it = 0; it < nch && ok; ++it) {
+    const int c = nch - 1 - it;
+    const int n = chunk_len(c);
+    const int64_t r0 = row0 + static_cast<int64_t>(c) * kChunk;
+    const uint32_t ph = static_cast<uint32_t>(it) & 1u;
+
+    // ---- P2 = dS^T K^T; the previous chunk's copies ----------------------------------------
     if (tid == 0) {
-      const int b = c & 1;
-      bool w = tc::mbar_wait_timed(b ? mb_kq1 : mb_kq0, (kq_phase >> b) & 1u, kWaitLimitNs);
-      kq_phase ^= 1u << b;
-      if (w) {
-        tc::fence_after_sync();
-        const uint32_t kq = sb + (b ? P::KQ1 : P::KQ0);
-        constexpr uint32_t id_g = tc::idesc_f16(128, 64, tc::kBF16, false, false);
+      constexpr uint32_t id_2 = tc::idesc_f16(128, 64, tc::kBF16, false, false);
+      const uint64_t dkq = tc::desc_sw128(sb + ((c & 1) ? P::KQ1 : P::KQ0), 16, 1024);
 #pragma unroll
-        for (int st = 0; st < 8; ++st) {
-          const uint32_t a = kq + (st >> 2) * 16384 + (st & 3) * 32;
-          tc::mma_f16(tmem + P::COL_G, tc::desc_sw128(a, 16, 1024), tc::desc_sw128(a, 16, 1024), id_g, st > 0);
-        }
+      for (int st = 0; st < 8; ++st) {
+        const uint64_t bk = dkq + (((st >> 2) * 16384 + (st & 3) * 32) >> 4);
+        tc::mma_f16_ts(tmem + P::COL_A2, tmem + P::COL_DSH + st * 8, bk, id_2, st > 0);
+        tc::mma_f16_ts(tmem + P::COL_A2, tmem + P::COL_DSL + st * 8, bk, id_2, 1);
+      }
+      tc::mma_commit(mb_a);
+    }
+    {  // this chunk's dS_end, staged by the state pass, out to global memory
+      __half* dst = p.dsbuf + (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim;
 #pragma unroll
-        for (int st = 0; st < 8; ++st) {
-          const uint64_t bk = tc::desc_sw128(kq + (st >> 2) * 16384 + (st & 3) * 32, 16, 1024);
-          tc::mma_f16_ts(tmem + P::COL_A2, tmem + P::COL_DSH + st * 8, bk, id_g, st > 0);
-          tc::mma_f16_ts(tmem + P::COL_A2, tmem + P::COL_DSL + st * 8, bk, id_g, 1);
-        }
-        tc::mma_commit(mb_a);
-        if (c > 0) issue_kq(c - 1);  // its buffer's last reader was the previous chunk's P4
-      } else {
-        atomicOr(p.status, kStatusTimeout);
-        ok = false;
+      for (int i = 0; i < 2048 / kDsThreads; ++i) {
+        const int idx = tid + kDsThreads * i;
+        reinterpret_cast<uint4*>(dst)[idx] = *reinterpret_cast<const uint4*>(sm + P::DOST + idx * 16);
       }
     }
+    __syncthreads();
     if (c > 0) issue_copies(c - 1);  // the staging and T buffer c - 1 uses are free
-    if (!wait_mb(mb_a, ph)) break;
-
-    // ---- A~ = (Q K^T . M) / sqrt(dk) from lanes 64-127 (rows t'), 16 columns per warp ---------
-    if (quarter >= 2) {
-      const int tp = v - 64;
-      const float bt = s_b[tp];
-      float d[16];
-      tc::tmem_ld16(lanes + P::COL_G + part * 16, d);
-      tc::tmem_ld_wait();
-      uint32_t pk[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int j0 = part * 16 + 2 * e, j1 = j0 + 1;
-        const float a0 = (j0 <= tp && tp < n) ? d[2 * e] * __expf(bt - s_b[j0]) * kInvSqrtD : 0.f;
-        const float a1 = (j1 <= tp && tp < n) ? d[2 * e + 1] * __expf(bt - s_b[j1]) * kInvSqrtD : 0.f;
-        pk[e] = pack_half2(a0, a1);
-      }
-      *reinterpret_cast<uint4*>(sm + P::AT + tc::sw128(tp, part * 32)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(sm + P::AT + tc::sw128(tp, part * 32 + 16)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-    }
-    tc::fence_proxy_async();
-    sync_tmem();
-
-    // ---- P1 = dO^T A~ (onto the Gram columns) ------------------------------------------
-    if (tid == 0) {
-      constexpr uint32_t id_1 = tc::idesc_f16(128, 64, tc::kF16, true, true);
-#pragma unroll
-      for (int st = 0; st < 4; ++st)
-        tc::mma_f16(tmem + P::COL_G, tc::desc_sw128(sb + P::DO16 + st * 2048, 8192, 1024),
-                    tc::desc_sw128(sb + P::AT + st * 2048, 8192, 1024), id_1, st > 0);
-      tc::mma_commit(mb_b);
-    }
-    if (!wait_mb(mb_b, ph)) break;
+    // P1 of this chunk was issued one step earlier
+    if (!wait_mb(mb_b, ph) || !wait_mb(mb_a, ph)) break;
 
     // ---- du^T = P1 + (gamma / Gamma_t) P2, zero past the chunk's end, as fp16 hi + lo ---------
     {
@@ -319,20 +354,23 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
     }
     sync_tmem();
 
-    // ---- P3 = du^T T -------------------------------------------------------------------
+    // ---- P3 = du^T T; the previous chunk's Gram onto the columns P1 has left ------------------
+    bool gram_ok = true;
     if (tid == 0) {
       constexpr uint32_t id_3 = tc::idesc_f16(128, 64, tc::kF16, false, true);
-      const uint32_t tb = sb + ((c & 1) ? P::TB1 : P::TB0);
+      const uint64_t dtb = tc::desc_sw128(sb + ((c & 1) ? P::TB1 : P::TB0), 8192, 1024);
 #pragma unroll
       for (int st = 0; st < 4; ++st) {
-        const uint64_t th = tc::desc_sw128(tb + st * 2048, 8192, 1024);
-        const uint64_t tl = tc::desc_sw128(tb + 8192 + st * 2048, 8192, 1024);
+        const uint64_t th = dtb + st * 128, tl = dtb + 512 + st * 128;
         tc::mma_f16_ts(tmem + P::COL_DUP, tmem + P::COL_DU + st * 8, th, id_3, st > 0);
         tc::mma_f16_ts(tmem + P::COL_DUP, tmem + P::COL_DU + st * 8, tl, id_3, 1);
         tc::mma_f16_ts(tmem + P::COL_DUP, tmem + P::COL_DU + 32 + st * 8, th, id_3, 1);
       }
       tc::mma_commit(mb_c);
+      if (c > 0) gram_ok = issue_gram(c - 1);
+      if (!gram_ok) atomicOr(p.status, kStatusTimeout);
     }
+    if (!gram_ok) ok = false;
     if (!wait_mb(mb_c, ph)) break;
 
     // ---- du' and dV rows out; (-Gamma beta du')^T as bf16 hi + lo over du^T's columns --------
@@ -367,30 +405,41 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
     if (tid == 0) {
       constexpr uint32_t id_s = tc::idesc_f16(128, 128, tc::kBF16, true, true);
       constexpr uint32_t id_t = tc::idesc_f16(128, 128, tc::kBF16, false, true);
-      const uint32_t kq = sb + ((c & 1) ? P::KQ1 : P::KQ0);
+      const uint64_t dkq = tc::desc_sw128(sb + ((c & 1) ? P::KQ1 : P::KQ0), 16384, 1024);
+      const uint64_t dds = tc::desc_sw128(sb + ((c & 1) ? P::DOS1 : P::DOS0), 8192, 1024);
 #pragma unroll
       for (int st = 0; st < 4; ++st) {
-        const uint64_t bq = tc::desc_sw128(kq + 8192 + st * 2048, 16384, 1024);
-        const uint64_t bk = tc::desc_sw128(kq + st * 2048, 16384, 1024);
-        tc::mma_f16(tmem + P::COL_DS, tc::desc_sw128(sb + P::DOSH + st * 2048, 8192, 1024), bq, id_s, 1);
-        tc::mma_f16(tmem + P::COL_DS, tc::desc_sw128(sb + P::DOSL + st * 2048, 8192, 1024), bq, id_s, 1);
+        const uint64_t bq = dkq + 512 + st * 128, bk = dkq + st * 128;
+        tc::mma_f16(tmem + P::COL_DS, dds + st * 128, bq, id_s, 1);
+        tc::mma_f16(tmem + P::COL_DS, dds + 1024 + st * 128, bq, id_s, 1);
         tc::mma_f16_ts(tmem + P::COL_DS, tmem + P::COL_DU + st * 8, bk, id_t, 1);
         tc::mma_f16_ts(tmem + P::COL_DS, tmem + P::COL_DU + 32 + st * 8, bk, id_t, 1);
       }
       tc::mma_commit(mb_d);
     }
+    // meanwhile, the previous chunk's chain-free work: factors, dO operands (its own scaled
+    // buffer; the fp16 dO tile's last reader, this chunk's P1, is done), A~ and P1
+    if (c > 0) {
+      mm::cp_async_wait_all();
+      if (warp == 0) gates(c - 1);
+      __syncthreads();
+      convert_do(c - 1);
+      if (!wait_mb(mb_g, g_count++ & 1u)) break;
+      a_tilde(c - 1);
+      tc::fence_proxy_async();
+      sync_tmem();
+      if (tid == 0) issue_p1();
+    }
     if (!wait_mb(mb_d, ph)) break;
 
-    // ---- the next chunk's bf16 hi + lo copy of dS^T ------------------------------------------
-    {
-      uint32_t x[32], hi[16], lo[16];
+    // ---- dS_end of the previous chunk: stored, copied for its P2, decayed for its P4; the
+    //      K/Q of the chunk after it into this chunk's buffer ----------------------------------
+    if (c > 0) {
+      if (tid == 0 && c > 1) issue_kq(c - 2);
+      uint32_t x[32];
       tc::tmem_ld32(lanes + P::COL_DS + part * 32, x);
       tc::tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 16; ++e) split_bf162(__uint_as_float(x[2 * e]), __uint_as_float(x[2 * e + 1]), hi[e], lo[e]);
-      tc::tmem_st16u(lanes + P::COL_DSH + part * 16, hi);
-      tc::tmem_st16u(lanes + P::COL_DSL + part * 16, lo);
-      tc::tmem_st_wait();
+      state_pass(x);
     }
     sync_tmem();
   }
