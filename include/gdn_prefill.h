@@ -188,8 +188,9 @@ void gdn_set_timing_events(void* before_wy, void* before_spine, void* after_spin
  * ssm_gdn_a3.rs `gdn_prefill_fla`), given dL/do and dL/dS_T. Computed in the
  * same chunked form as the forward: the per-chunk WY inverse T, a forward chain
  * storing each chunk's entry state, a reverse chain storing each chunk's state
- * gradient, and the per-chunk gradients, all on the tensor cores (fp16 operands,
- * fp32 accumulation, fp32 chain states). The forward's outputs are not needed.
+ * gradient, and the per-chunk gradients, all on the tensor cores (fp16 or bf16
+ * operands, hi + lo pairs where they carry a chain, fp32 accumulation and chain
+ * states). The forward's outputs are not needed.
  * Enqueues 4 kernels (5 with cu_seqlens). Scratch: 6 bytes per (row, v-head,
  * column) plus 64 KB per (64-row chunk, v-head).
  *   q, k, v, g, beta, strides, cu_seqlens, B, T, nk, nv, dk, dv: as gdn_prefill
