@@ -151,16 +151,22 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
     tc::fence_after_sync();
   };
 
-  // Per-token factors of chunk c (warp 0) and its dO operands from the staged rows.
-  auto gates = [&](int c) {
+  // Gates of chunk c into registers (warp 0), fetched with the chunk's other copies
+  float fg0 = 0.f, fg1 = 0.f, fb0 = 0.f, fb1 = 0.f;
+  auto fetch_gates = [&](int c) {
     const int n = chunk_len(c);
     const int64_t r0 = row0 + static_cast<int64_t>(c) * kChunk;
     const int t0 = 2 * lane, t1 = t0 + 1;
-    const float g0 = t0 < n ? p.g[(r0 + t0) * p.g_stride + h] : 0.f;
-    const float g1 = t1 < n ? p.g[(r0 + t1) * p.g_stride + h] : 0.f;
-    const float be0 = t0 < n ? p.beta[(r0 + t0) * p.beta_stride + h] : 0.f;
-    const float be1 = t1 < n ? p.beta[(r0 + t1) * p.beta_stride + h] : 0.f;
-    const GatePrefix gp = gate_prefix(g0, g1);
+    fg0 = t0 < n ? p.g[(r0 + t0) * p.g_stride + h] : 0.f;
+    fg1 = t1 < n ? p.g[(r0 + t1) * p.g_stride + h] : 0.f;
+    fb0 = t0 < n ? p.beta[(r0 + t0) * p.beta_stride + h] : 0.f;
+    fb1 = t1 < n ? p.beta[(r0 + t1) * p.beta_stride + h] : 0.f;
+  };
+  // Per-token factors of the fetched chunk (warp 0) and its dO operands from the staged rows.
+  auto gates = [&]() {
+    const int t0 = 2 * lane, t1 = t0 + 1;
+    const float be0 = fb0, be1 = fb1;
+    const GatePrefix gp = gate_prefix(fg0, fg1);
     const float e0 = __expf(gp.gca), e1 = __expf(gp.gcb);
     s_b[t0] = gp.gca;
     s_b[t1] = gp.gcb;
@@ -271,7 +277,10 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
       if (nch > 1) issue_kq(nch - 2);
     }
     issue_copies(nch - 1);
-    if (warp == 0) gates(nch - 1);
+    if (warp == 0) {
+      fetch_gates(nch - 1);
+      gates();
+    }
     mm::cp_async_wait_all();
     __syncthreads();
     convert_do(nch - 1);
@@ -330,7 +339,10 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
       }
     }
     __syncthreads();
-    if (c > 0) issue_copies(c - 1);  // the staging and T buffer c - 1 uses are free
+    if (c > 0) {
+      issue_copies(c - 1);  // the staging and T buffer c - 1 uses are free
+      if (warp == 0) fetch_gates(c - 1);
+    }
     // P1 of this chunk was issued one step earlier
     if (!wait_mb(mb_b, ph) || !wait_mb(mb_a, ph)) break;
 
@@ -421,7 +433,7 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
     // buffer; the fp16 dO tile's last reader, this chunk's P1, is done), A~ and P1
     if (c > 0) {
       mm::cp_async_wait_all();
-      if (warp == 0) gates(c - 1);
+      if (warp == 0) gates();
       __syncthreads();
       convert_do(c - 1);
       if (!wait_mb(mb_g, g_count++ & 1u)) break;
