@@ -161,3 +161,31 @@ def test_backward_workspace_sizes(lib):
         off = a256(off + state16)
         assert lib.gdn_prefill_backward_workspace_bytes(B, T, nv, 128, 128, varlen) == off
     assert lib.gdn_prefill_backward_workspace_bytes(0, T, nv, 128, 128, 0) == 0
+
+
+def _bwd(lib, B=1, T=64, nk=1, nv=1, dk=128, dv=128, strides=None, ptr=16, grad=16):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    gp = ctypes.c_void_p(grad) if grad else None
+    st = ctypes.byref(strides) if strides is not None else None
+    rc = lib.gdn_prefill_backward(p, p, p, p, p, p, p, None, gp, gp, gp, gp, gp, None, B, T, nk, nv, dk, dv, st,
+                                  None, None, 0, None)
+    return rc, lib.gdn_last_error().decode()
+
+
+def test_backward_host_checks(lib):
+    # every rejection below happens before the device is touched
+    import gated_delta_rule_17_gb300 as gdn
+
+    rc, msg = _bwd(lib, strides=gdn.Strides(128, 128, 128, 1, 1, 128, 0, 1))
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "normalised" in msg
+    rc, msg = _bwd(lib, grad=0)
+    assert rc == gdn.GDN_ERR_ARG and "gradient output pointer is NULL" in msg
+    rc, msg = _bwd(lib, grad=24)
+    assert rc == gdn.GDN_ERR_ARG and "16-byte aligned" in msg
+    rc, msg = _bwd(lib, dk=64)
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "128" in msg
+    rc, msg = _bwd(lib, nk=3, nv=4)
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "multiple of nk" in msg
+    assert _bwd(lib, B=-1)[0] == gdn.GDN_ERR_ARG
+    assert _bwd(lib, B=0, ptr=0, grad=0)[0] == gdn.GDN_OK
+    assert lib.gdn_last_launch_count() == 0
