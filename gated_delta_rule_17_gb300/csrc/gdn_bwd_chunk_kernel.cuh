@@ -206,10 +206,6 @@ __device__ __forceinline__ GatePrefix bc_put_gates(const BcGates& x, float* s_b,
   return gp;
 }
 
-// b of token t (0..63) from a warp's prefix; t is uniform over the warp
-__device__ __forceinline__ float bc_b_of(const GatePrefix& gp, int t) {
-  return __shfl_sync(0xffffffffu, (t & 1) ? gp.gcb : gp.gca, t >> 1);
-}
 
 // fp32 accumulator fragment -> fp16 hi and lo tiles (row-major, leading dimension ld).
 template <int NT>
