@@ -407,6 +407,14 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + half * 32, d);
       tc::tmem_ld_wait();
       signal(x.mb_wrd);  // the W columns are read: the next Gram MMA may go
+      if constexpr (!kOut) {
+        // The single -W^T tile and the hand-off barrier need the consumer past chunk c - 1:
+        // its u split of c - 1 comes after the MMA that read the previous tile and after its
+        // wait for the previous hand-off, so the barrier cannot complete twice ahead of that
+        // wait (a parity wait would then miss its phase). Runs with outputs get this order
+        // from the producer's longer chunk (its Gram and A epilogue).
+        if (c > 0 && !group_wait(x, p, x.mb_usp, (c - 1) & 1, kBarProducer, kProducerThreads, leader)) break;
+      }
       const int k = quad * 32 + lane;
 #pragma unroll
       for (int j8 = 0; j8 < 4; ++j8) {
