@@ -125,14 +125,16 @@ def test_backward_weak_decay_long():
     assert_grads(got, ref, "weak decay T=2000")
 
 
-def test_backward_benchmark_workload_one_key_head():
-    # The B=4 T=8192 nk=16 nv=32 workload through the launch configuration the benchmark
-    # times; the oracle runs one key head's group (its two value heads), which fixes
-    # dq and dk of that key head and every gradient of those value heads.
+@pytest.mark.parametrize("config,kh", [(2, 5), (4, 11)])
+def test_backward_large_workloads_one_key_head(config, kh):
+    # The B=4 T=8192 nk=16 nv=32 workload (the benchmark's launch configuration) and the
+    # B=1 T=65536 long-context one (1024 chunks of gates near zero: errors could build up
+    # along both chains); the oracle runs one key head's group (its two value heads),
+    # which fixes dq and dk of that key head and every gradient of those value heads.
     import gated_delta_rule_17_gb300 as gdn
 
-    p = gdn_synth.config_problem(2)
-    rng = np.random.default_rng(8800)
+    p = gdn_synth.config_problem(config)
+    rng = np.random.default_rng(8800 + config)
     dout = rng.standard_normal((p.rows, p.nv, p.dv)).astype(np.float32)
     dst = rng.standard_normal((p.B, p.nv, p.dk, p.dv)).astype(np.float32)
     dev = "cuda"
@@ -149,7 +151,7 @@ def test_backward_benchmark_workload_one_key_head():
     gdn.check()
     got = {n: t.cpu().numpy().astype(np.float64) for n, t in out.items()}
     del out, q, k, v
-    kh, grp = 5, p.nv // p.nk
+    grp = p.nv // p.nk
     hs = slice(kh * grp, (kh + 1) * grp)
     d = p.dk
     sub = gdn_synth.Problem(B=p.B, T=p.T, nk=1, nv=grp, dk=d, dv=d,
@@ -162,4 +164,4 @@ def test_backward_benchmark_workload_one_key_head():
     mine = {"dq": got["dq"][:, kh * d:(kh + 1) * d], "dk": got["dk"][:, kh * d:(kh + 1) * d],
             "dv": got["dv"][:, hs.start * d:hs.stop * d], "dg": got["dg"][:, hs], "dbeta": got["dbeta"][:, hs],
             "dh0": got["dh0"][:, hs]}
-    assert_grads(mine, ref, "B=4 T=8192 nv=32, key head 5")
+    assert_grads(mine, ref, f"{gdn_synth.CONFIG_NAMES[config]}, key head {kh}")
