@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const Bwd
 // One CTA per (chunk, key head): it walks the value heads of the key head's GQA group,
 // adding each one's dQ and dK in registers, so q, k, Q K^T and K K^T are formed once and
 // dq, dk are written once.
-constexpr int kGradsSmem = 5 * kTile128 + 2 * kTileState + 2 * kTile64;
+constexpr int kGradsSmem = 6 * kTile128 + 2 * kTileState + 2 * kTile64;
 
 // Sums of a fragment row pair over the 4 lanes of a quad (lanes 4g .. 4g + 3).
 __device__ __forceinline__ float bc_quad_sum(float x) {
@@ -424,6 +424,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
   __half* sE = sS + kDim * kLd;        // dS_end
   __half* sP0 = sE + kDim * kLd;       // dA = lower(dO u^T) . M / sqrt(dk)
   __half* sP1 = sP0 + kChunk * kLd64;  // E = beta F
+  __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(sP1 + kChunk * kLd64);  // v rows (bf16)
   __shared__ float s_b[kChunk], s_beta[kChunk];
   // per-token partial sums of one value head: q.(dO S0^T), k.P, rows/columns of
   // dA . QK^T and of E . G, rows of F . G, w, du'.v
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
   const int am0 = 16 * (warp & 3), an0 = 32 * (warp >> 2);  // 64 x 64 products
   const uint32_t aQ = mm::saddr(sQ), aK = mm::saddr(sK), aDO = mm::saddr(sDO), aU = mm::saddr(sU),
                  aDU = mm::saddr(sDU), aS = mm::saddr(sS), aE = mm::saddr(sE), aP0 = mm::saddr(sP0),
-                 aP1 = mm::saddr(sP1);
+                 aP1 = mm::saddr(sP1), aV = mm::saddr(sV);
 
   {
     BcRows16 fq, fk;
@@ -485,15 +486,17 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
     const int h = kh * group + j;
     const int64_t state_off = (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim;
     {
-      // u, du', S0 and dS_end straight into shared memory; dO and the gates through registers
+      // u, du', v, S0 and dS_end straight into shared memory; dO and the gates through registers
       const __half* ug = p.ubuf + r0 * hrow + h * kDim;
       const __half* dg = p.dubuf + r0 * hrow + h * kDim;
+      const __nv_bfloat16* vg = p.v + r0 * p.v_stride + h * kDim;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int idx = tid + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
         const int64_t src_row = row < n ? row : 0;
         mm::cp_async16(aU + 2u * (row * kLd + 8 * c8), ug + src_row * hrow + 8 * c8, row < n);
         mm::cp_async16(aDU + 2u * (row * kLd + 8 * c8), dg + src_row * hrow + 8 * c8, row < n);
+        mm::cp_async16(aV + 2u * (row * kLd + 8 * c8), vg + src_row * p.v_stride + 8 * c8, row < n);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -700,7 +703,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           float vf[8];
-          unpack_bf16x8(__ldg(reinterpret_cast<const uint4*>(p.v + (r0 + t) * p.v_stride + h * kDim + 32 * qq) + i), vf);
+          unpack_bf16x8(*reinterpret_cast<const uint4*>(sV + t * kLd + 32 * qq + 8 * i), vf);
           const uint4 draw = *reinterpret_cast<const uint4*>(sDU + t * kLd + 32 * qq + 8 * i);
           const __half2* d2 = reinterpret_cast<const __half2*>(&draw);
 #pragma unroll
