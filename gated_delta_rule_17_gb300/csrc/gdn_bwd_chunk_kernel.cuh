@@ -577,74 +577,44 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
       if (lane == 0) atomicAdd(&s_dot, dot);
     }
 
-    // dA = lower(dO u^T) . M / sqrt(dk) and the row/column sums of dA . (Q K^T)
+    // dA = lower(dO u^T) . M / sqrt(dk) with the row/column sums of dA . (Q K^T), and
+    // F = -strict_lower(du' u^T) . M, E = beta F with the rows of F . G and the
+    // rows/columns of E . G; the decays M_ti = e^{b_t - b_i} are formed once for both
     {
-      float aD[4][4], col[4][2];
+      float aD[4][4], aF[4][4], c1[4][2], c2[4][2];
       mm::zero(aD);
-      mm::warp_mma<false, true, 4>(aD, aDO, kLd, aU, kLd, am0, an0, kDim);
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) col[jj][0] = col[jj][1] = 0.f;
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = am0 + gq + 8 * e;
-        const float bt = s_b[t];
-        float row = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const int i = an0 + 8 * jj + 2 * tq + x;
-            const float m = i <= t ? __expf(bt - s_b[i]) * kInvSqrtD : 0.f;
-            const float da = aD[jj][2 * e + x] * m, y = da * aA[jj][2 * e + x];
-            aD[jj][2 * e + x] = da;
-            row += y;
-            col[jj][x] += y;
-          }
-        row = bc_quad_sum(row);
-        if (tq == 0) atomicAdd(&s_r1[t], row);
-      }
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          const float v = bc_column_sum(col[jj][x]);
-          if (gq == 0) atomicAdd(&s_c1[an0 + 8 * jj + 2 * tq + x], v);
-        }
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          *reinterpret_cast<__half2*>(sP0 + (am0 + gq + 8 * e) * kLd64 + an0 + 8 * jj + 2 * tq) =
-              __floats2half2_rn(aD[jj][2 * e], aD[jj][2 * e + 1]);
-    }
-
-    // F = -strict_lower(du' u^T) . M, E = beta F; rows of F . G; rows/columns of E . G
-    {
-      float aF[4][4], col[4][2];
       mm::zero(aF);
+      mm::warp_mma<false, true, 4>(aD, aDO, kLd, aU, kLd, am0, an0, kDim);
       mm::warp_mma<false, true, 4>(aF, aDU, kLd, aU, kLd, am0, an0, kDim);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) col[jj][0] = col[jj][1] = 0.f;
+      for (int jj = 0; jj < 4; ++jj) c1[jj][0] = c1[jj][1] = c2[jj][0] = c2[jj][1] = 0.f;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int t = am0 + gq + 8 * e;
         const float bt = s_b[t], be = s_beta[t];
-        float rf = 0.f, rz = 0.f;
+        float r1 = 0.f, rf = 0.f, rz = 0.f;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             const int i = an0 + 8 * jj + 2 * tq + x;
-            const float m = i < t ? __expf(bt - s_b[i]) : 0.f;
-            const float f = -aF[jj][2 * e + x] * m, gv = aG[jj][2 * e + x], ee = be * f, z = ee * gv;
+            const float m = i <= t ? __expf(bt - s_b[i]) : 0.f;
+            const float da = aD[jj][2 * e + x] * (m * kInvSqrtD), y = da * aA[jj][2 * e + x];
+            aD[jj][2 * e + x] = da;
+            r1 += y;
+            c1[jj][x] += y;
+            const float f = i < t ? -aF[jj][2 * e + x] * m : 0.f;
+            const float gv = aG[jj][2 * e + x], ee = be * f, z = ee * gv;
             aF[jj][2 * e + x] = ee;
             rf = fmaf(f, gv, rf);
             rz += z;
-            col[jj][x] += z;
+            c2[jj][x] += z;
           }
+        r1 = bc_quad_sum(r1);
         rf = bc_quad_sum(rf);
         rz = bc_quad_sum(rz);
         if (tq == 0) {
+          atomicAdd(&s_r1[t], r1);
           atomicAdd(&s_rf[t], rf);
           atomicAdd(&s_r2[t], rz);
         }
@@ -653,15 +623,21 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
       for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-          const float v = bc_column_sum(col[jj][x]);
-          if (gq == 0) atomicAdd(&s_c2[an0 + 8 * jj + 2 * tq + x], v);
+          const float v1 = bc_column_sum(c1[jj][x]), v2 = bc_column_sum(c2[jj][x]);
+          if (gq == 0) {
+            atomicAdd(&s_c1[an0 + 8 * jj + 2 * tq + x], v1);
+            atomicAdd(&s_c2[an0 + 8 * jj + 2 * tq + x], v2);
+          }
         }
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
+        for (int e = 0; e < 2; ++e) {
+          *reinterpret_cast<__half2*>(sP0 + (am0 + gq + 8 * e) * kLd64 + an0 + 8 * jj + 2 * tq) =
+              __floats2half2_rn(aD[jj][2 * e], aD[jj][2 * e + 1]);
           *reinterpret_cast<__half2*>(sP1 + (am0 + gq + 8 * e) * kLd64 + an0 + 8 * jj + 2 * tq) =
               __floats2half2_rn(aF[jj][2 * e], aF[jj][2 * e + 1]);
+        }
     }
     __syncthreads();  // dA and E are in shared memory
 
