@@ -425,12 +425,12 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
   __half* sP0 = sE + kDim * kLd;       // dA = lower(dO u^T) . M / sqrt(dk)
   __half* sP1 = sP0 + kChunk * kLd64;  // E = beta F
   __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(sP1 + kChunk * kLd64);  // v rows (bf16)
-  __shared__ float s_b[kChunk], s_beta[kChunk];
-  // per-token partial sums of one value head: q.(dO S0^T), k.P, rows/columns of
-  // dA . QK^T and of E . G, rows of F . G, w, du'.v
-  __shared__ float s_rq[kChunk], s_rkp[kChunk], s_r1[kChunk], s_c1[kChunk], s_r2[kChunk], s_c2[kChunk],
-      s_rf[kChunk], s_rw[kChunk], s_rdv[kChunk];
-  __shared__ float s_dot;
+  // by value-head parity (so warp 0's per-token pass of one head overlaps the next
+  // head's loads): b and beta, and the per-token partial sums q.(dO S0^T), k.P,
+  // rows/columns of dA . QK^T and of E . G, rows of F . G, w, du'.v, and <dS_end, S0>
+  __shared__ float s_gate[2][2][kChunk];
+  __shared__ float s_sum[2][9][kChunk];
+  __shared__ float s_dots[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
   const int ci = blockIdx.x / p.nk, kh = blockIdx.x % p.nk, group = p.nv / p.nk;
@@ -484,6 +484,18 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
   mm::zero(dK);
   for (int j = 0; j < group; ++j) {
     const int h = kh * group + j;
+    float* s_b = s_gate[j & 1][0];
+    float* s_beta = s_gate[j & 1][1];
+    float* s_rq = s_sum[j & 1][0];
+    float* s_rkp = s_sum[j & 1][1];
+    float* s_r1 = s_sum[j & 1][2];
+    float* s_c1 = s_sum[j & 1][3];
+    float* s_r2 = s_sum[j & 1][4];
+    float* s_c2 = s_sum[j & 1][5];
+    float* s_rf = s_sum[j & 1][6];
+    float* s_rw = s_sum[j & 1][7];
+    float* s_rdv = s_sum[j & 1][8];
+    float& s_dot = s_dots[j & 1];
     const int64_t state_off = (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim;
     {
       // u, du', v, S0 and dS_end straight into shared memory; dO and the gates through registers
@@ -728,7 +740,8 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
         p.dbeta[(r0 + t1) * p.nv + h] = dbe[1];
       }
     }
-    __syncthreads();  // the next value head reuses the tiles and the sums
+    // (no barrier: the next head's loads only touch tiles this head has finished with,
+    // behind the barrier above, and the other parity of the per-token arrays)
   }
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt)
