@@ -189,3 +189,29 @@ def test_backward_host_checks(lib):
     assert _bwd(lib, B=-1)[0] == gdn.GDN_ERR_ARG
     assert _bwd(lib, B=0, ptr=0, grad=0)[0] == gdn.GDN_OK
     assert lib.gdn_last_launch_count() == 0
+
+
+def _dec(lib, B=1, nk=1, nv=1, dk=128, dv=128, strides=None, ptr=16):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    st = ctypes.byref(strides) if strides is not None else None
+    rc = lib.gdn_decode(p, p, p, p, p, p, p, B, nk, nv, dk, dv, st, None)
+    return rc, lib.gdn_last_error().decode()
+
+
+def test_decode_host_checks(lib):
+    # the decode step shares the prefill's argument rules; each rejection happens on the host
+    import gated_delta_rule_17_gb300 as gdn
+
+    rc, msg = _dec(lib, dv=64)
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "128" in msg
+    rc, msg = _dec(lib, nk=2, nv=3)
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "multiple of nk" in msg
+    assert _dec(lib, B=-2)[0] == gdn.GDN_ERR_ARG
+    rc, msg = _dec(lib, ptr=0)
+    assert rc == gdn.GDN_ERR_ARG and "NULL" in msg
+    rc, msg = _dec(lib, ptr=18)
+    assert rc == gdn.GDN_ERR_ARG and "aligned" in msg
+    rc, msg = _dec(lib, strides=gdn.Strides(132, 128, 128, 1, 1, 128, 0))
+    assert rc == gdn.GDN_ERR_ARG and "q row stride" in msg
+    assert _dec(lib, B=0, ptr=0)[0] == gdn.GDN_OK
+    assert lib.gdn_last_launch_count() == 0
