@@ -413,6 +413,10 @@ __device__ __forceinline__ float bc_column_sum(float x) {
   return x + __shfl_xor_sync(0xffffffffu, x, 16);
 }
 
+// K steps per unrolled MMA loop in the gradient kernel (4 measured 2.5% faster than 2
+// there; the forward chain kernel keeps 2)
+constexpr int kGradsUnroll = 4;
+
 __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdChunkParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   __half* sQ = reinterpret_cast<__half*>(smem);
@@ -476,8 +480,8 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
   float aA[4][4], aG[4][4];
   mm::zero(aA);
   mm::zero(aG);
-  mm::warp_mma<false, true, 4>(aA, aQ, kLd, aK, kLd, am0, an0, kDim);
-  mm::warp_mma<false, true, 4>(aG, aK, kLd, aK, kLd, am0, an0, kDim);
+  mm::warp_mma<false, true, 4, kGradsUnroll>(aA, aQ, kLd, aK, kLd, am0, an0, kDim);
+  mm::warp_mma<false, true, 4, kGradsUnroll>(aG, aK, kLd, aK, kLd, am0, an0, kDim);
 
   float dQ[2][4][4], dK[2][4][4];
   mm::zero(dQ);
@@ -536,8 +540,8 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
       float tq8[2][4][4], tp8[2][4][4];
       mm::zero(tq8);
       mm::zero(tp8);
-      mm::warp_mma2<false, true, 4>(tq8, aDO, kLd, aS, kLd, m0, n0, kDim);
-      mm::warp_mma2<false, true, 4>(tp8, aDU, kLd, aS, kLd, m0, n0, kDim);
+      mm::warp_mma2<false, true, 4, kGradsUnroll>(tq8, aDO, kLd, aS, kLd, m0, n0, kDim);
+      mm::warp_mma2<false, true, 4, kGradsUnroll>(tp8, aDU, kLd, aS, kLd, m0, n0, kDim);
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -596,8 +600,8 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
       float aD[4][4], aF[4][4], c1[4][2], c2[4][2];
       mm::zero(aD);
       mm::zero(aF);
-      mm::warp_mma<false, true, 4>(aD, aDO, kLd, aU, kLd, am0, an0, kDim);
-      mm::warp_mma<false, true, 4>(aF, aDU, kLd, aU, kLd, am0, an0, kDim);
+      mm::warp_mma<false, true, 4, kGradsUnroll>(aD, aDO, kLd, aU, kLd, am0, an0, kDim);
+      mm::warp_mma<false, true, 4, kGradsUnroll>(aF, aDU, kLd, aU, kLd, am0, an0, kDim);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) c1[jj][0] = c1[jj][1] = c2[jj][0] = c2[jj][1] = 0.f;
 #pragma unroll
@@ -654,14 +658,14 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
     __syncthreads();  // dA and E are in shared memory
 
     // dQ += dA K; dK += E K + E^T K + dA^T Q + (gamma / Gamma) u dS_end^T
-    mm::warp_mma2<false, false, 4>(dQ, aP0, kLd64, aK, kLd, m0, n0, kChunk);
-    mm::warp_mma2<false, false, 4>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
-    mm::warp_mma2<true, false, 4>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
-    mm::warp_mma2<true, false, 4>(dK, aP0, kLd64, aQ, kLd, m0, n0, kChunk);
+    mm::warp_mma2<false, false, 4, kGradsUnroll>(dQ, aP0, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma2<false, false, 4, kGradsUnroll>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma2<true, false, 4, kGradsUnroll>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma2<true, false, 4, kGradsUnroll>(dK, aP0, kLd64, aQ, kLd, m0, n0, kChunk);
     {
       float uD[2][4][4];
       mm::zero(uD);
-      mm::warp_mma2<false, true, 4>(uD, aU, kLd, aE, kLd, m0, n0, kDim);
+      mm::warp_mma2<false, true, 4, kGradsUnroll>(uD, aU, kLd, aE, kLd, m0, n0, kDim);
       const float blast = s_b[kChunk - 1];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)

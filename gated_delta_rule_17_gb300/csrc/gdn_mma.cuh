@@ -52,8 +52,8 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 //   kBT = false: B is stored [K][N];
 //   kBT = true:  B is given by its transpose, stored [N][K].
 // a, b are shared-space byte addresses of element (0, 0); K is a multiple of 16,
-// NT of 2.
-template <bool kAT, bool kBT, int NT>
+// NT of 2. kUnroll: K steps unrolled together (more fragments in flight, more registers).
+template <bool kAT, bool kBT, int NT, int kUnroll = 2>
 __device__ __forceinline__ void warp_mma(float (&c)[NT][4], uint32_t a, int lda, uint32_t b, int ldb, int m0, int n0,
                                          int K) {
   static_assert(NT % 2 == 0, "B operands are loaded two n8 tiles at a time");
@@ -78,7 +78,7 @@ __device__ __forceinline__ void warp_mma(float (&c)[NT][4], uint32_t a, int lda,
     b_step = 32 * ldb;
   }
   const uint32_t b_pair = kBT ? 32u * ldb : 32u;  // bytes to the next pair of n8 tiles
-#pragma unroll 2
+#pragma unroll kUnroll
   for (int k0 = 0; k0 < K; k0 += 16) {
     uint32_t af[4];
     if (!kAT) ldsm_x4(a_lane, af);
@@ -98,7 +98,7 @@ __device__ __forceinline__ void warp_mma(float (&c)[NT][4], uint32_t a, int lda,
 
 // Two m16 row tiles per warp: c[m][j] += A[m0 + 16 m : +16, 0 : K] * B[0 : K, n0 + 8 j : +8].
 // Each B fragment feeds both row tiles, halving B's shared-memory traffic per MMA.
-template <bool kAT, bool kBT, int NT>
+template <bool kAT, bool kBT, int NT, int kUnroll = 2>
 __device__ __forceinline__ void warp_mma2(float (&c)[2][NT][4], uint32_t a, int lda, uint32_t b, int ldb, int m0,
                                           int n0, int K) {
   static_assert(NT % 2 == 0, "B operands are loaded two n8 tiles at a time");
@@ -123,7 +123,7 @@ __device__ __forceinline__ void warp_mma2(float (&c)[2][NT][4], uint32_t a, int 
     b_step = 32 * ldb;
   }
   const uint32_t b_pair = kBT ? 32u * ldb : 32u;
-#pragma unroll 2
+#pragma unroll kUnroll
   for (int k0 = 0; k0 < K; k0 += 16) {
     uint32_t af0[4], af1[4];
     if (!kAT) {
