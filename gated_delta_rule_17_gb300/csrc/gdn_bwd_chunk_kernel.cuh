@@ -540,8 +540,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
       float tq8[2][4][4], tp8[2][4][4];
       mm::zero(tq8);
       mm::zero(tp8);
-      mm::warp_mma2<false, true, 4, kGradsUnroll>(tq8, aDO, kLd, aS, kLd, m0, n0, kDim);
-      mm::warp_mma2<false, true, 4, kGradsUnroll>(tp8, aDU, kLd, aS, kLd, m0, n0, kDim);
+      mm::warp_mma2_pair<false, true, 4, kGradsUnroll>(tq8, tp8, aDO, aDU, kLd, aS, kLd, m0, n0, kDim);
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -600,8 +599,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
       float aD[4][4], aF[4][4], c1[4][2], c2[4][2];
       mm::zero(aD);
       mm::zero(aF);
-      mm::warp_mma<false, true, 4, kGradsUnroll>(aD, aDO, kLd, aU, kLd, am0, an0, kDim);
-      mm::warp_mma<false, true, 4, kGradsUnroll>(aF, aDU, kLd, aU, kLd, am0, an0, kDim);
+      mm::warp_mma_pair<false, true, 4, kGradsUnroll>(aD, aF, aDO, aDU, kLd, aU, kLd, am0, an0, kDim);
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) c1[jj][0] = c1[jj][1] = c2[jj][0] = c2[jj][1] = 0.f;
 #pragma unroll
@@ -658,8 +656,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_grads_kernel(const BwdC
     __syncthreads();  // dA and E are in shared memory
 
     // dQ += dA K; dK += E K + E^T K + dA^T Q + (gamma / Gamma) u dS_end^T
-    mm::warp_mma2<false, false, 4, kGradsUnroll>(dQ, aP0, kLd64, aK, kLd, m0, n0, kChunk);
-    mm::warp_mma2<false, false, 4, kGradsUnroll>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
+    mm::warp_mma2_pair<false, false, 4, kGradsUnroll>(dQ, dK, aP0, aP1, kLd64, aK, kLd, m0, n0, kChunk);
     mm::warp_mma2<true, false, 4, kGradsUnroll>(dK, aP1, kLd64, aK, kLd, m0, n0, kChunk);
     mm::warp_mma2<true, false, 4, kGradsUnroll>(dK, aP0, kLd64, aQ, kLd, m0, n0, kChunk);
     {

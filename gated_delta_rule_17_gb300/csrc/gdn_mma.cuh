@@ -148,6 +148,117 @@ __device__ __forceinline__ void warp_mma2(float (&c)[2][NT][4], uint32_t a, int 
   }
 }
 
+// Two products that share their B operand: c += A B and d += A2 B, where A2 is a second
+// tile with A's orientation and leading dimension (shared address a2). Each B fragment
+// is loaded once for both, so the pair costs three quarters of the two calls' ldmatrix.
+template <bool kAT, bool kBT, int NT, int kUnroll = 2>
+__device__ __forceinline__ void warp_mma_pair(float (&c)[NT][4], float (&d)[NT][4], uint32_t a, uint32_t a2, int lda,
+                                              uint32_t b, int ldb, int m0, int n0, int K) {
+  static_assert(NT % 2 == 0, "B operands are loaded two n8 tiles at a time");
+  const int lane = threadIdx.x & 31;
+  uint32_t a_lane, b_lane;
+  int a_step, b_step;
+  if (!kAT) {
+    a_lane = a + 2u * static_cast<uint32_t>((m0 + (lane & 15)) * lda + (lane >> 4) * 8);
+    a_step = 32;
+  } else {
+    a_lane = a + 2u * static_cast<uint32_t>(((lane & 7) + ((lane >> 4) << 3)) * lda + m0 + ((lane >> 3) & 1) * 8);
+    a_step = 32 * lda;
+  }
+  if (kBT) {
+    b_lane = b + 2u * static_cast<uint32_t>((n0 + (lane & 7) + ((lane >> 4) << 3)) * ldb + ((lane >> 3) & 1) * 8);
+    b_step = 32;
+  } else {
+    b_lane = b + 2u * static_cast<uint32_t>((lane & 15) * ldb + n0 + (lane >> 4) * 8);
+    b_step = 32 * ldb;
+  }
+  const uint32_t a_other = a2 - a;  // bytes from A's tile to A2's
+  const uint32_t b_pair = kBT ? 32u * ldb : 32u;
+#pragma unroll kUnroll
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t af[4], ag[4];
+    if (!kAT) {
+      ldsm_x4(a_lane, af);
+      ldsm_x4(a_lane + a_other, ag);
+    } else {
+      ldsm_x4_t(a_lane, af);
+      ldsm_x4_t(a_lane + a_other, ag);
+    }
+#pragma unroll
+    for (int j = 0; j < NT / 2; ++j) {
+      uint32_t bf[4];
+      if (kBT) ldsm_x4(b_lane + j * b_pair, bf);
+      else ldsm_x4_t(b_lane + j * b_pair, bf);
+      mma16816(c[2 * j], af, bf[0], bf[1]);
+      mma16816(c[2 * j + 1], af, bf[2], bf[3]);
+      mma16816(d[2 * j], ag, bf[0], bf[1]);
+      mma16816(d[2 * j + 1], ag, bf[2], bf[3]);
+    }
+    a_lane += a_step;
+    b_lane += b_step;
+  }
+}
+
+// warp_mma2 for two products that share B: c += A B and d += A2 B over two m16 row tiles.
+template <bool kAT, bool kBT, int NT, int kUnroll = 2>
+__device__ __forceinline__ void warp_mma2_pair(float (&c)[2][NT][4], float (&d)[2][NT][4], uint32_t a, uint32_t a2,
+                                               int lda, uint32_t b, int ldb, int m0, int n0, int K) {
+  static_assert(NT % 2 == 0, "B operands are loaded two n8 tiles at a time");
+  const int lane = threadIdx.x & 31;
+  uint32_t a_lane, b_lane;
+  int a_step, b_step;
+  uint32_t a_next;
+  if (!kAT) {
+    a_lane = a + 2u * static_cast<uint32_t>((m0 + (lane & 15)) * lda + (lane >> 4) * 8);
+    a_step = 32;
+    a_next = 32u * lda;
+  } else {
+    a_lane = a + 2u * static_cast<uint32_t>(((lane & 7) + ((lane >> 4) << 3)) * lda + m0 + ((lane >> 3) & 1) * 8);
+    a_step = 32 * lda;
+    a_next = 32u;
+  }
+  if (kBT) {
+    b_lane = b + 2u * static_cast<uint32_t>((n0 + (lane & 7) + ((lane >> 4) << 3)) * ldb + ((lane >> 3) & 1) * 8);
+    b_step = 32;
+  } else {
+    b_lane = b + 2u * static_cast<uint32_t>((lane & 15) * ldb + n0 + (lane >> 4) * 8);
+    b_step = 32 * ldb;
+  }
+  const uint32_t a_other = a2 - a;
+  const uint32_t b_pair = kBT ? 32u * ldb : 32u;
+#pragma unroll kUnroll
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t af0[4], af1[4], ag0[4], ag1[4];
+    if (!kAT) {
+      ldsm_x4(a_lane, af0);
+      ldsm_x4(a_lane + a_next, af1);
+      ldsm_x4(a_lane + a_other, ag0);
+      ldsm_x4(a_lane + a_other + a_next, ag1);
+    } else {
+      ldsm_x4_t(a_lane, af0);
+      ldsm_x4_t(a_lane + a_next, af1);
+      ldsm_x4_t(a_lane + a_other, ag0);
+      ldsm_x4_t(a_lane + a_other + a_next, ag1);
+    }
+#pragma unroll
+    for (int j = 0; j < NT / 2; ++j) {
+      uint32_t bf[4];
+      if (kBT) ldsm_x4(b_lane + j * b_pair, bf);
+      else ldsm_x4_t(b_lane + j * b_pair, bf);
+      mma16816(c[0][2 * j], af0, bf[0], bf[1]);
+      mma16816(c[0][2 * j + 1], af0, bf[2], bf[3]);
+      mma16816(c[1][2 * j], af1, bf[0], bf[1]);
+      mma16816(c[1][2 * j + 1], af1, bf[2], bf[3]);
+      mma16816(d[0][2 * j], ag0, bf[0], bf[1]);
+      mma16816(d[0][2 * j + 1], ag0, bf[2], bf[3]);
+      mma16816(d[1][2 * j], ag1, bf[0], bf[1]);
+      mma16816(d[1][2 * j + 1], ag1, bf[2], bf[3]);
+    }
+    a_lane += a_step;
+    b_lane += b_step;
+  }
+}
+
 template <int NT>
 __device__ __forceinline__ void zero(float (&c)[NT][4]) {
 #pragma unroll
