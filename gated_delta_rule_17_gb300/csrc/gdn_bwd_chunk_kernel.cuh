@@ -330,8 +330,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const Bwd
     {
       float acc[2][4][4];
       mm::zero(acc);
-      mm::warp_mma2<false, false, 4>(acc, aK, kLd, aSh, kLd, m0, n0, kDim);
-      mm::warp_mma2<false, false, 4>(acc, aK, kLd, aSl, kLd, m0, n0, kDim);
+      mm::warp_mma2_sum<false, false, 4>(acc, aK, kLd, aSh, aSl, kLd, m0, n0, kDim);
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -354,8 +353,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const Bwd
     {
       float acc[2][4][4];
       mm::zero(acc);
-      mm::warp_mma2<false, false, 4>(acc, aTh, kLd64, aXh, kLd, m0, n0, kChunk);
-      mm::warp_mma2<false, false, 4>(acc, aTh, kLd64, aXl, kLd, m0, n0, kChunk);
+      mm::warp_mma2_sum<false, false, 4>(acc, aTh, kLd64, aXh, aXl, kLd, m0, n0, kChunk);
       mm::warp_mma2<false, false, 4>(acc, aTl, kLd64, aXh, kLd, m0, n0, kChunk);
       const float blast = s_b[kChunk - 1];
 #pragma unroll
@@ -386,8 +384,7 @@ __global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const Bwd
         for (int j = 0; j < 8; ++j)
 #pragma unroll
           for (int x = 0; x < 4; ++x) S[mt][j][x] *= gam;
-      mm::warp_mma2<true, false, 8>(S, aK, kLd, aUh, kLd, sm0, sn0, kChunk);
-      mm::warp_mma2<true, false, 8>(S, aK, kLd, aUl, kLd, sm0, sn0, kChunk);
+      mm::warp_mma2_sum<true, false, 8>(S, aK, kLd, aUh, aUl, kLd, sm0, sn0, kChunk);
       bc_store_split2<8>(S, sSh, sSl, kLd, sm0, sn0);
     }
     __syncthreads();
