@@ -106,6 +106,39 @@ def workspace_bytes(B, T, nv, varlen, dk=128, dv=128) -> int:
     return int(load().gdn_prefill_workspace_bytes(B, T, nv, dk, dv, 1 if varlen else 0))
 
 
+# The library takes raw device addresses, so a host tensor or a wrong element type
+# handed to it would reach a kernel; these checks turn that into a GdnError first.
+def _check_rows(torch, named):
+    for name, t, dt in named:
+        if t.dtype != dt:
+            raise GdnError(GDN_ERR_ARG, f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_cuda:
+            raise GdnError(GDN_ERR_ARG, f"{name} must be a CUDA tensor")
+
+
+def _check_state(torch, state, state_is_table, name="state"):
+    if not state.is_cuda:
+        raise GdnError(GDN_ERR_ARG, f"{name} must be a CUDA tensor")
+    if state_is_table:
+        if state.dtype != torch.int64 or not state.is_contiguous():
+            raise GdnError(GDN_ERR_ARG, f"a {name} table must be a contiguous int64 tensor of device addresses")
+    elif state.dtype != torch.float32 or not state.is_contiguous():
+        raise GdnError(GDN_ERR_ARG, f"{name} must be a contiguous fp32 tensor [B, nv, dk, dv]")
+
+
+def _check_aux(torch, cu_seqlens, workspace):
+    if cu_seqlens is not None and (cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda
+                                   or not cu_seqlens.is_contiguous()):
+        raise GdnError(GDN_ERR_ARG, "cu_seqlens must be a contiguous int32 CUDA tensor")
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise GdnError(GDN_ERR_ARG, "workspace must be a contiguous CUDA tensor")
+
+
+def _io_rows(torch, q, k, v, g, beta, last):
+    return (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+            ("g", g, torch.float32), ("beta", beta, torch.float32), last)
+
+
 def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = None, T: int | None = None,
             cu_seqlens=None, state_is_table: bool = False, workspace=None, stream=None, dk: int = 128,
             dv: int = 128, qk_l2norm: bool = False) -> None:
@@ -122,16 +155,11 @@ def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = N
     import torch
 
     lib = load()
-    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
-                        ("g", g, torch.float32), ("beta", beta, torch.float32), ("out", out, torch.bfloat16)):
-        if t.dtype != dt:
-            raise GdnError(GDN_ERR_ARG, f"{name} must be {dt}, got {t.dtype}")
-        if not t.is_cuda:
-            raise GdnError(GDN_ERR_ARG, f"{name} must be a CUDA tensor")
+    _check_rows(torch, _io_rows(torch, q, k, v, g, beta, ("out", out, torch.bfloat16)))
+    _check_state(torch, state, state_is_table)
+    _check_aux(torch, cu_seqlens, workspace)
     rows = q.shape[0]
     if cu_seqlens is not None:
-        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
-            raise GdnError(GDN_ERR_ARG, "cu_seqlens must be an int32 CUDA tensor")
         B = cu_seqlens.numel() - 1
         T = rows
     elif B is None or T is None:
@@ -139,11 +167,6 @@ def prefill(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = N
     st = Strides(_row_stride(q, "q", nk * dk), _row_stride(k, "k", nk * dk), _row_stride(v, "v", nv * dv),
                  _row_stride(g, "g", nv), _row_stride(beta, "beta", nv), _row_stride(out, "out", nv * dv),
                  1 if state_is_table else 0, 1 if qk_l2norm else 0)
-    if state_is_table:
-        if state.dtype != torch.int64:
-            raise GdnError(GDN_ERR_ARG, "a state table must be an int64 tensor of device addresses")
-    elif state.dtype != torch.float32 or not state.is_contiguous():
-        raise GdnError(GDN_ERR_ARG, "state must be a contiguous fp32 tensor [B, nv, dk, dv]")
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
@@ -170,6 +193,9 @@ def prefill_noalloc(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | 
     import torch
 
     lib = load()
+    _check_rows(torch, _io_rows(torch, q, k, v, g, beta, ("out", out, torch.bfloat16)))
+    _check_state(torch, state, state_is_table)
+    _check_aux(torch, cu_seqlens, None)
     if cu_seqlens is not None:
         B = cu_seqlens.numel() - 1
         T = q.shape[0]
@@ -197,20 +223,11 @@ def decode(q, k, v, g, beta, state, out, *, nk: int, nv: int, state_is_table: bo
     import torch
 
     lib = load()
-    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
-                        ("g", g, torch.float32), ("beta", beta, torch.float32), ("out", out, torch.bfloat16)):
-        if t.dtype != dt:
-            raise GdnError(GDN_ERR_ARG, f"{name} must be {dt}, got {t.dtype}")
-        if not t.is_cuda:
-            raise GdnError(GDN_ERR_ARG, f"{name} must be a CUDA tensor")
+    _check_rows(torch, _io_rows(torch, q, k, v, g, beta, ("out", out, torch.bfloat16)))
+    _check_state(torch, state, state_is_table)
     st = Strides(_row_stride(q, "q", nk * dk), _row_stride(k, "k", nk * dk), _row_stride(v, "v", nv * dv),
                  _row_stride(g, "g", nv), _row_stride(beta, "beta", nv), _row_stride(out, "out", nv * dv),
                  1 if state_is_table else 0, 1 if qk_l2norm else 0)
-    if state_is_table:
-        if state.dtype != torch.int64:
-            raise GdnError(GDN_ERR_ARG, "a state table must be an int64 tensor of device addresses")
-    elif state.dtype != torch.float32 or not state.is_contiguous():
-        raise GdnError(GDN_ERR_ARG, "state must be a contiguous fp32 tensor [B, nv, dk, dv]")
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
@@ -239,12 +256,9 @@ def backward(q, k, v, g, beta, h0, dout, dq, dk, dv, dg, dbeta, *, nk: int, nv: 
     import torch
 
     lib = load()
-    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
-                        ("g", g, torch.float32), ("beta", beta, torch.float32), ("dout", dout, torch.float32)):
-        if t.dtype != dt:
-            raise GdnError(GDN_ERR_ARG, f"{name} must be {dt}, got {t.dtype}")
-        if not t.is_cuda:
-            raise GdnError(GDN_ERR_ARG, f"{name} must be a CUDA tensor")
+    _check_rows(torch, _io_rows(torch, q, k, v, g, beta, ("dout", dout, torch.float32)))
+    _check_state(torch, h0, state_is_table, name="h0")
+    _check_aux(torch, cu_seqlens, workspace)
     for name, t in (("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg), ("dbeta", dbeta),
                     ("dST", dST), ("dh0", dh0)):
         if t is not None and (t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda):

@@ -215,3 +215,35 @@ def test_decode_host_checks(lib):
     assert rc == gdn.GDN_ERR_ARG and "q row stride" in msg
     assert _dec(lib, B=0, ptr=0)[0] == gdn.GDN_OK
     assert lib.gdn_last_launch_count() == 0
+
+
+def test_binding_rejects_host_tensors_and_wrong_types(lib):
+    # every entry point of the binding checks element types and device placement before
+    # the library sees an address (a host pointer would otherwise reach a kernel)
+    import torch
+
+    import gated_delta_rule_17_gb300 as gdn
+
+    rows, nk, nv = 64, 1, 1
+    bf = dict(dtype=torch.bfloat16)
+    f32 = dict(dtype=torch.float32)
+    q, k, v, out = (torch.zeros((rows, 128), **bf) for _ in range(4))
+    g, beta = torch.zeros((rows, nv), **f32), torch.zeros((rows, nv), **f32)
+    state = torch.zeros((1, nv, 128, 128), **f32)
+    calls = {
+        "prefill": lambda **kw: gdn.prefill(q, k, v, g, beta, state, out, nk=nk, nv=nv, B=1, T=rows, **kw),
+        "prefill_noalloc": lambda **kw: gdn.prefill_noalloc(q, k, v, g, beta, state, out, nk=nk, nv=nv, B=1,
+                                                            T=rows, **kw),
+        "decode": lambda **kw: gdn.decode(q, k, v, g, beta, state, out, nk=nk, nv=nv, **kw),
+        "backward": lambda **kw: gdn.backward(q, k, v, g, beta, state, torch.zeros((rows, 128), **f32),
+                                              *(torch.zeros((rows, 128), **f32) for _ in range(3)),
+                                              torch.zeros((rows, nv), **f32), torch.zeros((rows, nv), **f32),
+                                              nk=nk, nv=nv, B=1, T=rows, **kw),
+    }
+    for name, call in calls.items():
+        with pytest.raises(gdn.GdnError, match="CUDA tensor"):
+            call()
+    with pytest.raises(gdn.GdnError, match="must be torch.bfloat16"):
+        gdn.prefill(q.float(), k, v, g, beta, state, out, nk=nk, nv=nv, B=1, T=rows)
+    with pytest.raises(gdn.GdnError, match="got torch.float16"):
+        gdn.prefill_noalloc(q.half(), k, v, g, beta, state, out, nk=nk, nv=nv, B=1, T=rows)
