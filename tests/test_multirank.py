@@ -1,4 +1,4 @@
-"""bench.py's multi-rank plumbing on CPU (gloo, world size 2): the barrier and the
+"""bench.py's rank plumbing on CPU (gloo, world size 2): the barrier and the
 max-over-ranks timing reduction every rank runs, and the launch under
 torch.distributed.run that the multi-GPU benchmark uses, with the CPU reference arm
 (rank 0 alone prints the one JSON line, every rank exits 0)."""
@@ -57,3 +57,20 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["steps"] == 1
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_single_process_json_line():
+    # the default (N=1) reference arm: one JSON line carrying the contract's keys
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-seconds", "1"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    res = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [json.loads(x) for x in res.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = lines[0]
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["n_gpus"] == 1 and line["higher_is_better"] is True and line["value"] > 0
+    assert line["cpu_baseline"]["cores"] >= 1 and line["cpu_baseline"]["sample"]
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["d2h_bytes_per_step"] == 0
