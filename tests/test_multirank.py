@@ -1,7 +1,8 @@
 """bench.py's rank plumbing on CPU (gloo, world size 2): the barrier and the
 max-over-ranks timing reduction every rank runs, and the launch under
 torch.distributed.run that the multi-GPU benchmark uses, with the CPU reference arm
-(rank 0 alone prints the one JSON line, every rank exits 0)."""
+(rank 0 alone prints the one JSON line, every rank exits 0); and the single-process
+reference arm's JSON line."""
 import json
 import os
 import socket
