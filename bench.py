@@ -241,7 +241,7 @@ def run_gpu(args, world, rank, local):
         workload = gdn_synth.CONFIG_NAMES[args.config]
     if args.qk_l2norm:
         workload += ", raw q/k rows normalised in the kernels (fused prologue)"
-    from tests.gpu_helpers import DeviceProblem
+    from gdn_synth.device import DeviceProblem
 
     dp = DeviceProblem(p, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -384,7 +384,7 @@ def run_decode(args, world, rank, local):
     torch.cuda.set_device(dev)
     B = args.decode_batch
     p = gdn_synth.make_problem(seed=6100, B=B, T=args.steps + args.warmup, nk=16, nv=32, h0_std=0.02)
-    from tests.gpu_helpers import DeviceProblem
+    from gdn_synth.device import DeviceProblem
 
     dp = DeviceProblem(p, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -439,7 +439,7 @@ def run_backward(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     p = gdn_synth.config_problem(args.config)
-    from tests.gpu_helpers import DeviceProblem
+    from gdn_synth.device import DeviceProblem
 
     dp = DeviceProblem(p, device=dev)
     rng = torch.Generator(device=dev).manual_seed(7)

@@ -13,11 +13,12 @@ import threading
 
 __all__ = ["prefill", "prefill_noalloc", "NOALLOC_MAX_SEQS", "workspace_bytes", "check", "last_launch_count",
            "backward", "backward_workspace_bytes",
-           "set_timing_events", "decode", "lib_path", "load", "GdnError",
+           "set_timing_events", "set_test_hooks", "decode", "lib_path", "load", "GdnError",
            "Strides", "GDN_OK", "GDN_ERR_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
-           "GDN_ERR_DEVICE_STATUS", "GDN_ERR_TIMEOUT"]
+           "GDN_ERR_DEVICE_STATUS", "GDN_ERR_TIMEOUT", "GDN_ERR_RANGE"]
 
-GDN_OK, GDN_ERR_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_STATUS, GDN_ERR_TIMEOUT = range(6)
+(GDN_OK, GDN_ERR_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE_STATUS, GDN_ERR_TIMEOUT,
+ GDN_ERR_RANGE) = range(7)
 NOALLOC_MAX_SEQS = 16384  # GDN_NOALLOC_MAX_SEQS in include/gdn_prefill.h
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -75,7 +76,8 @@ def load():
             lib.gdn_prefill_backward.restype = i
             lib.gdn_set_timing_events.argtypes = [vp, vp, vp]
             lib.gdn_set_timing_events.restype = None
-            del i64
+            lib.gdn_set_test_hooks.argtypes = [i64, i64, i]
+            lib.gdn_set_test_hooks.restype = i
             _lib = lib
     return _lib
 
@@ -313,3 +315,12 @@ def set_timing_events(before_wy=None, before_spine=None, after_spine=None) -> No
     def handle(e):
         return None if e is None else e.cuda_event
     load().gdn_set_timing_events(handle(before_wy), handle(before_spine), handle(after_spine))
+
+
+def set_test_hooks(wait_limit_ns: int = 0, consumer_delay_ns: int = 0, skip_hand_off_chunk: int = -1) -> None:
+    """Test hooks (``gdn_set_test_hooks``) for later prefill calls on this thread: a
+    short wait limit, a consumer delay before the hand-off wait of odd chunks, and a
+    skipped hand-off arrival. All defaults switch them off."""
+    rc = load().gdn_set_test_hooks(int(wait_limit_ns), int(consumer_delay_ns), int(skip_hand_off_chunk))
+    if rc != GDN_OK:
+        _raise(rc)

@@ -29,6 +29,13 @@ namespace {
 thread_local char g_err[512] = "";
 thread_local int g_launches = 0;
 thread_local cudaEvent_t g_timing[3] = {nullptr, nullptr, nullptr};  // gdn_set_timing_events
+// gdn_set_test_hooks: wait limit (ns), consumer delay (ns), skipped hand-off chunk
+struct TestHooks {
+  int64_t wait_ns = 0, delay_ns = 0;
+  int skip_chunk = -1;
+  bool active() const { return wait_ns > 0 || delay_ns > 0 || skip_chunk >= 0; }
+};
+thread_local TestHooks g_hooks;
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -80,6 +87,7 @@ int device_info(DeviceInfo** out) {
       return fail(GDN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     for (const void* f : {reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<true, false>),
+                          reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<true, false, true>),
                           reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<true, true>),
                           reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<false, false>),
                           reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<false, true>)}) {
@@ -375,13 +383,15 @@ int wy_geometry(const DeviceInfo& d, int B, int T, int nv, bool varlen, int* ite
   return GDN_OK;
 }
 
-// One spine launch: the instantiation for output rows (or not) and the fused q/k norms (or not).
+// One spine launch: the instantiation for output rows (or not) and the fused q/k norms (or
+// not); the test instantiation when test hooks are set (output rows, no fused norms).
 void launch_spine(bool out_rows, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                   const CUtensorMap& mt, const gdn::ChunkParams& p, int64_t grid, cudaStream_t stream) {
   const dim3 g(static_cast<unsigned>(grid)), blk(gdn::kThreads);
   const size_t sm = gdn::Plan::DYN_SMEM;
   if (out_rows) {
-    if (p.qk_l2norm) gdn::gdn_prefill_kernel<true, true><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
+    if (g_hooks.active() && !p.qk_l2norm) gdn::gdn_prefill_kernel<true, false, true><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
+    else if (p.qk_l2norm) gdn::gdn_prefill_kernel<true, true><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
     else gdn::gdn_prefill_kernel<true, false><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
   } else {
     if (p.qk_l2norm) gdn::gdn_prefill_kernel<false, true><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
@@ -441,6 +451,9 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   p.state_is_table = r.table;
   p.qk_l2norm = r.l2norm;
   p.seg = nullptr;
+  p.test_wait_ns = g_hooks.wait_ns > 0 ? g_hooks.wait_ns : static_cast<int64_t>(gdn::kWaitLimitNs);
+  p.test_delay_ns = g_hooks.delay_ns;
+  p.test_skip_chunk = g_hooks.skip_chunk;
   int launches = 0;
   if (cu) {
     gdn_schedule_kernel<<<(B + 255) / 256, 256, 0, stream>>>(cu, B, T, order, cu_chunks, d->status);
@@ -662,6 +675,10 @@ int gdn_prefill_check(void* stream) {
   if (st & gdn::kStatusTimeout) return fail(GDN_ERR_TIMEOUT, "a bounded on-device wait expired (status 0x%x)", st);
   if (st & gdn::kStatusBadSeqlens)
     return fail(GDN_ERR_DEVICE_STATUS, "cu_seqlens is malformed: not non-decreasing from 0 to T (status 0x%x)", st);
+  if (st & gdn::kStatusRange)
+    return fail(GDN_ERR_RANGE,
+                "an output or final state is not finite: v, the state or an intermediate left the fp16 operand "
+                "range (|x| < 65504) (status 0x%x)", st);
   return GDN_OK;
 }
 
@@ -842,6 +859,18 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
 const char* gdn_last_error(void) { return g_err; }
 
 int gdn_last_launch_count(void) { return g_launches; }
+
+int gdn_set_test_hooks(int64_t wait_limit_ns, int64_t consumer_delay_ns, int skip_hand_off_chunk) {
+  g_err[0] = 0;
+  if (wait_limit_ns < 0 || consumer_delay_ns < 0 || skip_hand_off_chunk < -1)
+    return fail(GDN_ERR_ARG, "test hooks: limits must be >= 0 and the skipped chunk >= -1");
+  if (consumer_delay_ns > 100000000)
+    return fail(GDN_ERR_ARG, "test hooks: a consumer delay above 100 ms per chunk is refused");
+  g_hooks.wait_ns = wait_limit_ns;
+  g_hooks.delay_ns = consumer_delay_ns;
+  g_hooks.skip_chunk = skip_hand_off_chunk;
+  return GDN_OK;
+}
 
 void gdn_set_timing_events(void* before_wy, void* before_spine, void* after_spine) {
   g_timing[0] = static_cast<cudaEvent_t>(before_wy);

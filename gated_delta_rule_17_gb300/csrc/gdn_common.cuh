@@ -16,6 +16,9 @@ constexpr int kChunk = 64;  // tokens per chunk
 // Status bits written to the per-device status word.
 constexpr unsigned kStatusBadSeqlens = 1u;
 constexpr unsigned kStatusTimeout = 2u;
+// An output or the final state came out non-finite: an operand left the range of the
+// 16-bit tensor-core types (|v|, |S| and the intermediates must stay below ~6.5e4).
+constexpr unsigned kStatusRange = 4u;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 constexpr float kInvSqrtD = 0.08838834764831845f;  // 1 / sqrt(128)

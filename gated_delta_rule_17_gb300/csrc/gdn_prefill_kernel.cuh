@@ -37,7 +37,16 @@
 // treated as k = v = 0, g = 0: their T diag(beta) rows, which belong to other
 // tokens, only reach columns of u^T that are zeroed before use, and their
 // outputs are not stored. Every wait on an mbarrier is bounded; on expiry the
-// CTA records a status bit and unwinds.
+// CTA records a status bit and unwinds. A non-finite output or final state
+// (an operand outside the fp16 range) sets another status bit.
+//
+// Ordering. Every barrier is waited on by parity, so no barrier may complete
+// twice before each of its waiters has seen the earlier phase. A barrier that
+// completes once per chunk is either single (when its next completion is
+// caused, through some chain of waits, by each of its waiters having passed
+// the wait for the current chunk) or doubled by chunk parity (when only its
+// completion two chunks later is caused that way). The per-barrier argument
+// sits next to each barrier's declaration in Ctx.
 #pragma once
 #include "gdn_common.cuh"
 
@@ -69,6 +78,12 @@ struct ChunkParams {
   // skips the output rows (the range's T diag(beta) rows stay in place for a later run),
   // bit 1 runs it with v = 0 (the state map's linear part).
   const int32_t* seg;
+  // Test hooks, read only by the test instantiation (kTest = true): a wait limit in
+  // nanoseconds in place of kWaitLimitNs, a consumer delay in nanoseconds before the
+  // hand-off wait of every odd chunk (so the producer runs ahead), and a chunk whose
+  // hand-off arrival the producer skips (-1: none), so that bounded waits expire.
+  int64_t test_wait_ns, test_delay_ns;
+  int test_skip_chunk;
 };
 constexpr int kSegNoOutput = 1;
 constexpr int kSegZeroValues = 2;
@@ -120,17 +135,44 @@ struct Ctx {
   float* s_gstage;      // [2][64] g of a chunk, staged by cp.async
   float* s_elast;       // [3] e^{gc_last} by chunk index mod 3 (read by the consumer)
   volatile int* s_abort;
-  uint32_t mb_kq0, mb_kq1, mb_v0, mb_v1, mb_t, mb_g, mb_uw, mb_c1, mb_c20, mb_c21, mb_hand, mb_cu0, mb_cu1;
+  // Barriers and why none can complete twice ahead of a waiter (chunk c; "->" is
+  // "happens before, through waits"):
+  //   kq[b], v[b]  copies of chunk c+2 are issued after qrdy[b](c), which every
+  //                waiting producer warp signals after its own wait.
+  //   t            waited on by the producer-side issuer only, in program order.
+  //   g            Gram(c+1) is issued after wrd(c), signalled after both producer waits.
+  //   uw           U/W(c+1) need krdy(c+1), signalled after the producer's uw(c) wait.
+  //   c1           spine1(c+1) needs hand(c+1) (producer, after its c1(c) wait) and
+  //                strdy(c+1) (consumer, after its c1(c) wait).
+  //   c2[b]        spine2(c+2) needs usp(c+2) (consumer, after its c2(c) wait) and
+  //                hand(c+2) (producer, after its c2[b](c) wait at the top of c+2).
+  //   hand[b]      doubled: hand(c+1) may arrive while the consumer still finishes
+  //                chunk c-1 (it needs only c1(c) and c2(c-1)); hand(c+2) needs
+  //                c2[b](c), which needs the consumer's usp(c) and the spine
+  //                issuer's spine2(c), both after their hand(c) waits.
+  //   cu[b]        consumer cu(c) -> needs spine1(c) -> hand(c) -> uw(c) -> U(c) MMAs,
+  //                issued after the issuer's cu[b](c-2) wait.
+  //   vrdy, krdy   the producer's chunk c+1 starts after uw(c), committed after the
+  //                issuer's vrdy(c) and krdy(c) waits.
+  //   qrdy[b]      doubled: without outputs nothing orders qrdy(c+1) after the
+  //                issuer's qrdy(c) wait; qrdy(c+2) follows the producer's uw(c+1)
+  //                wait, and uw(c+1) is committed after the issuer's qrdy(c) wait.
+  //   wrd          wrd(c+1) follows uw(c+1) -> W(c+1) MMAs, issued after wrd(c).
+  //   strdy        strdy(c+1) follows the consumer's c2(c) wait -> spine2(c), issued
+  //                after the spine issuer's strdy(c) wait.
+  //   usp          usp(c+1) follows c1(c+1) -> spine1(c+1), issued after usp(c).
+  uint32_t mb_kq0, mb_kq1, mb_v0, mb_v1, mb_t, mb_g, mb_uw, mb_c1, mb_c20, mb_c21, mb_hand0, mb_hand1, mb_cu0, mb_cu1;
   // readiness for the issuer (one arrival per warp): V is fp16 (4), e^gc K is done and
-  // Q K^T read (8), Q~ is done (8), W read (8), S^T ready and O^T read (4), u split (4)
-  uint32_t mb_vrdy, mb_krdy, mb_qrdy, mb_wrd, mb_strdy, mb_usp;
+  // Q K^T read (8), Q~ is done (8, by chunk parity), W read (8), S^T ready and O^T
+  // read (4), u split (4)
+  uint32_t mb_vrdy, mb_krdy, mb_qrdy0, mb_qrdy1, mb_wrd, mb_strdy, mb_usp;
 };
 
 // All threads of a group wait on one mbarrier phase; the outcome is made
 // uniform across the group so that it can leave its loop together.
 __device__ __forceinline__ bool group_wait(const Ctx& x, const ChunkParams& p, uint32_t mbar, uint32_t parity,
-                                           uint32_t bar_id, uint32_t nthreads, bool leader) {
-  bool ok = (*x.s_abort == 0) && tc::mbar_wait_timed(mbar, parity, kWaitLimitNs);
+                                           uint32_t bar_id, uint32_t nthreads, bool leader, uint64_t lim) {
+  bool ok = (*x.s_abort == 0) && tc::mbar_wait_timed(mbar, parity, lim);
   ok = tc::barrier_all(bar_id, nthreads, ok);
   if (!ok) {
     if (leader) {
@@ -143,14 +185,22 @@ __device__ __forceinline__ bool group_wait(const Ctx& x, const ChunkParams& p, u
   return true;
 }
 
+// Wait limit: the 2 s default, or the test instantiation's own.
+template <bool kTest>
+__device__ __forceinline__ uint64_t wait_limit(const ChunkParams& p) {
+  if constexpr (kTest) return static_cast<uint64_t>(p.test_wait_ns);
+  else return kWaitLimitNs;
+}
+
 // ---------------------------------------------------------------------------------
 // Producer: the operand tiles of each chunk, one chunk ahead of the consumer
 // (the issuer runs its MMAs). Warp 4 also scans the gates of the chunk after,
 // so every chunk starts with its gate set ready.
 // ---------------------------------------------------------------------------------
-template <bool kOut, bool kNorm>
+template <bool kOut, bool kNorm, bool kTest>
 __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p, int ptid) {
   using P = Plan;
+  const uint64_t lim = wait_limit<kTest>(p);
   const int pw = ptid >> 5, lane = ptid & 31;
   const int quad = pw & 3;   // tensor-memory lane quarter of this warp
   const int half = pw >> 2;  // which half of a 64-column accumulator it reads
@@ -235,11 +285,11 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     // ---- the Gram MMA of this chunk is issued by the issuer once its tile lands ------
     // this chunk's Kd and A buffers were last read by the spine of chunk c-2
     ok = true;
-    if (c >= 2) ok = (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_c21 : x.mb_c20, ((c - 2) >> 1) & 1, kWaitLimitNs);
+    if (c >= 2) ok = (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_c21 : x.mb_c20, ((c - 2) >> 1) & 1, lim);
 
     if (quad < 2) {
       // ---- V -> fp16 in place (rows t; tail rows zeroed), lane quarters 0, 1 -----------
-      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_v1 : x.mb_v0, use, kWaitLimitNs);
+      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_v1 : x.mb_v0, use, lim);
       if (ok) {
 #pragma unroll 1
         for (int r0 = 0; r0 < 8; r0 += 4) {
@@ -269,7 +319,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         // it in place. The inverse norms are folded into this chunk's per-token factors
         // (K: e^gc, e^{gc_last-gc}, F; Q: e^gc/sqrt(dk), E) and kept apart for the
         // direct-decay path
-        ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_kq1 : x.mb_kq0, use, kWaitLimitNs);
+        ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_kq1 : x.mb_kq0, use, lim);
         tc::fence_after_sync();
         const int row = half * 64 + (quad - 2) * 32 + lane, t = row & 63;
         const uint32_t base = kq_off + (row >> 6) * 8192;
@@ -292,7 +342,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         }
         tc::named_barrier(kBarNorm, kProducerThreads);
       }
-      if constexpr (kOut) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
+      if constexpr (kOut) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, lim);
       tc::fence_after_sync();
       if (kOut && ok) {
         const int i = (quad - 2) * 32 + lane;  // A_ij = e^{gc_i - gc_j} q_i.k_j / sqrt(dk), j <= i
@@ -336,9 +386,9 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     //      Kd = e^{gc_last-gc} K (KD[b]); tail rows zeroed
     // (without outputs there is no Gram MMA: the tile only has to have landed)
     if constexpr (kOut)
-      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, kWaitLimitNs);
+      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, lim);
     else
-      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_kq1 : x.mb_kq0, use, kWaitLimitNs);
+      ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_kq1 : x.mb_kq0, use, lim);
     tc::fence_after_sync();
     if (ok) {
 #pragma unroll 1
@@ -366,7 +416,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 
     // ---- meanwhile: Q -> Q~ = e^gc Q / sqrt(dk) (fp16, rows t, tail rows zeroed), once
     //      the spine of chunk c-1 has read Q~ (and -W^T) ------------------------------------
-    if (kOut && c > 0) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, kWaitLimitNs);
+    if (kOut && c > 0) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, lim);
     if (kOut && ok) {
 #pragma unroll 1
       for (int r0 = 0; r0 < 4; r0 += 2) {
@@ -386,7 +436,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         }
       }
     }
-    signal(x.mb_qrdy);  // the raw K/Q tile is consumed: it may be refilled
+    signal(b ? x.mb_qrdy1 : x.mb_qrdy0);  // the raw K/Q tile is consumed: it may be refilled
     // ---- and the gates of the next chunk, into the other gate set (their copy was
     //      started a chunk ago), and the copy of the gates of the chunk after -----------
     if (pw == 4 && c + 1 < x.nchunks) {
@@ -399,7 +449,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       if (leader) fail();
       break;
     }
-    if (!group_wait(x, p, x.mb_uw, b, kBarProducer, kProducerThreads, leader)) break;
+    if (!group_wait(x, p, x.mb_uw, b, kBarProducer, kProducerThreads, leader, lim)) break;
 
     // ---- -W^T as the spine's fp16 B operand (rows k, columns t) -----------------------
     {
@@ -408,12 +458,9 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       tc::tmem_ld_wait();
       signal(x.mb_wrd);  // the W columns are read: the next Gram MMA may go
       if constexpr (!kOut) {
-        // The single -W^T tile and the hand-off barrier need the consumer past chunk c - 1:
-        // its u split of c - 1 comes after the MMA that read the previous tile and after its
-        // wait for the previous hand-off, so the barrier cannot complete twice ahead of that
-        // wait (a parity wait would then miss its phase). Runs with outputs get this order
-        // from the producer's longer chunk (its Gram and A epilogue).
-        if (c > 0 && !group_wait(x, p, x.mb_usp, (c - 1) & 1, kBarProducer, kProducerThreads, leader)) break;
+        // The single -W^T tile was last read by the spine MMAs of chunk c - 1; runs with
+        // outputs waited for them before converting Q~
+        if (c > 0 && !group_wait(x, p, x.mb_c1, (c - 1) & 1, kBarProducer, kProducerThreads, leader, lim)) break;
       }
       const int k = quad * 32 + lane;
 #pragma unroll
@@ -429,7 +476,9 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     tc::fence_proxy_async();
     tc::fence_before_sync();
     tc::named_barrier(kBarProducer, kProducerThreads);
-    if (leader) tc::mbar_arrive(x.mb_hand);  // chunk c's operands are ready
+    bool arrive = leader;
+    if constexpr (kTest) arrive = arrive && c != p.test_skip_chunk;
+    if (arrive) tc::mbar_arrive(b ? x.mb_hand1 : x.mb_hand0);  // chunk c's operands are ready
   }
 }
 
@@ -437,9 +486,10 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 // Consumer: the state spine and the output of each chunk. Thread v owns value
 // column v: tensor-memory lane v holds S^T[v][:], u^T[v][:] and O^T[v][:].
 // ---------------------------------------------------------------------------------
-template <bool kOut>
+template <bool kOut, bool kTest>
 __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p, int ctid) {
   using P = Plan;
+  const uint64_t lim = wait_limit<kTest>(p);
   const int quad = ctid >> 5;
   const int v = ctid;
   const bool leader = ctid == 0;
@@ -491,17 +541,28 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     tc::tmem_st_wait();
   };
 
+  // sum of every output and final-state value this thread writes: non-finite exactly
+  // when one of them is (an operand outside the fp16 range turns into inf or NaN)
+  float chk = 0.f;
   for (int c = 0; c < x.nchunks; ++c) {
     const int b = c & 1;
     const int64_t rem = x.len - static_cast<int64_t>(c) * kChunk;
     const int clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
     const uint32_t col_u = P::COL_U + 64 * b;
 
-    if (!group_wait(x, p, x.mb_hand, b, kBarConsumer, kConsumerThreads, leader)) break;
+    if constexpr (kTest) {
+      // test hook: fall behind the producer before the hand-off wait of odd chunks
+      if ((c & 1) && p.test_delay_ns > 0) {
+        const uint64_t t0 = tc::globaltimer_ns();
+        while (tc::globaltimer_ns() - t0 < static_cast<uint64_t>(p.test_delay_ns)) __nanosleep(500);
+      }
+    }
+    if (!group_wait(x, p, b ? x.mb_hand1 : x.mb_hand0, (c >> 1) & 1, kBarConsumer, kConsumerThreads, leader, lim))
+      break;
     // (the issuer runs u^T = U^T - S^T W^T onto U^T and O^T = S^T Q~^T.) The decay of
     // chunk c > 0 was applied at the end of the previous iteration, while these ran.
     if (c == 0) decay_state(0);
-    if (!group_wait(x, p, x.mb_c1, b, kBarConsumer, kConsumerThreads, leader)) break;
+    if (!group_wait(x, p, x.mb_c1, b, kBarConsumer, kConsumerThreads, leader, lim)) break;
 
     // ---- u^T as an fp16 hi + lo pair in tensor memory (the A operand of the next MMAs) ---
     {
@@ -525,7 +586,8 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     }
     signal(x.mb_usp);                    // the issuer runs S^T += u^T Kd, O^T += u^T A^T
     signal(b ? x.mb_cu1 : x.mb_cu0);     // the U columns of this chunk parity are free again
-    if (!group_wait(x, p, b ? x.mb_c21 : x.mb_c20, (c >> 1) & 1, kBarConsumer, kConsumerThreads, leader)) break;
+    if (!group_wait(x, p, b ? x.mb_c21 : x.mb_c20, (c >> 1) & 1, kBarConsumer, kConsumerThreads, leader, lim))
+      break;
 
     // ---- next chunk's fp16 S^T operand; this chunk's O^T into registers ---------------
     uint32_t o[64];
@@ -560,7 +622,11 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
       const int64_t ostride = p.out_stride;
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
-        if (e < clen) *optr = __float2bfloat16_rn(__uint_as_float(o[e]));
+        if (e < clen) {
+          const float y = __uint_as_float(o[e]);
+          *optr = __float2bfloat16_rn(y);
+          chk += y;
+        }
         optr += ostride;
       }
     }
@@ -574,8 +640,12 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
       tc::tmem_ld32(lanes + P::COL_S + q4 * 32, s);
       tc::tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) x.state[(q4 * 32 + e) * kDim + v] = __uint_as_float(s[e]);
+      for (int e = 0; e < 32; ++e) {
+        x.state[(q4 * 32 + e) * kDim + v] = __uint_as_float(s[e]);
+        chk += __uint_as_float(s[e]);
+      }
     }
+    if (!isfinite(chk)) atomicOr(p.status, kStatusRange);
   }
 }
 
@@ -586,11 +656,12 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
 // consumer warps only convert operands and signal readiness, so no warp that
 // converts waits for an instruction queue.
 // ---------------------------------------------------------------------------------
-template <bool kOut>
+template <bool kOut, bool kTest>
 __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, const CUtensorMap* tmap_q,
                                             const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
                                             const CUtensorMap* tmap_t, bool spine_side) {
   using P = Plan;
+  const uint64_t lim = wait_limit<kTest>(p);
   auto issue_kq = [&](int c) {
     const uint32_t dst = x.sbase + ((c & 1) ? P::KQ1 : P::KQ0);
     const uint32_t mb = (c & 1) ? x.mb_kq1 : x.mb_kq0;
@@ -617,7 +688,7 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
   };
   auto wait = [&](uint32_t mbar, uint32_t parity) -> bool {
     if (*x.s_abort != 0) return false;
-    if (!tc::mbar_wait_timed(mbar, parity, kWaitLimitNs)) {
+    if (!tc::mbar_wait_timed(mbar, parity, lim)) {
       *x.s_abort = 1;
       atomicOr(p.status, kStatusTimeout);
       return false;
@@ -692,7 +763,7 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
   if (spine_side) {
     for (int c = 0; c < n; ++c) {
       // first half once the operands are handed over and S^T is ready (and O^T read)
-      if (!wait(x.mb_hand, c & 1) || !wait(x.mb_strdy, c & 1)) break;
+      if (!wait((c & 1) ? x.mb_hand1 : x.mb_hand0, (c >> 1) & 1) || !wait(x.mb_strdy, c & 1)) break;
       spine1(c);
       // second half once u is split
       if (!wait(x.mb_usp, c & 1)) break;
@@ -728,7 +799,7 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
     wy(c, false);
     tc::mma_commit(x.mb_uw);
     // refill what chunk c has consumed
-    if (!wait(x.mb_uw, c & 1) || !wait(x.mb_qrdy, c & 1)) break;
+    if (!wait(x.mb_uw, c & 1) || !wait(b ? x.mb_qrdy1 : x.mb_qrdy0, (c >> 1) & 1)) break;
     if (c + 2 < n) {
       issue_kq(c + 2);
       issue_v(c + 2);
@@ -740,8 +811,10 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
 // kOut = false: runs that only carry the state (the segment schedule's state maps):
 // no Gram, A, Q~, output MMAs or output rows. kNorm: the fused q/k normalisation
 // (ChunkParams::qk_l2norm), a separate instantiation so that the common path carries
-// none of its code.
-template <bool kOut = true, bool kNorm = false>
+// none of its code. kTest: the test hooks of ChunkParams (wait limit, consumer delay,
+// skipped hand-off), likewise an instantiation of its own.
+constexpr int kNumMbar = 21;
+template <bool kOut = true, bool kNorm = false, bool kTest = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_t,
@@ -752,7 +825,7 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   __shared__ __align__(16) float s_rq[kChunk], s_rk[kChunk];
   __shared__ float s_elast[3];
   __shared__ int s_fast[2];
-  __shared__ __align__(8) uint64_t s_mb[19];
+  __shared__ __align__(8) uint64_t s_mb[kNumMbar];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -817,23 +890,25 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.mb_c1 = tc::smem_u32(&s_mb[7]);
   x.mb_c20 = tc::smem_u32(&s_mb[8]);
   x.mb_c21 = tc::smem_u32(&s_mb[9]);
-  x.mb_hand = tc::smem_u32(&s_mb[10]);
+  x.mb_hand0 = tc::smem_u32(&s_mb[10]);
   x.mb_cu0 = tc::smem_u32(&s_mb[11]);
   x.mb_cu1 = tc::smem_u32(&s_mb[12]);
   x.mb_vrdy = tc::smem_u32(&s_mb[13]);
   x.mb_krdy = tc::smem_u32(&s_mb[14]);
-  x.mb_qrdy = tc::smem_u32(&s_mb[15]);
+  x.mb_qrdy0 = tc::smem_u32(&s_mb[15]);
   x.mb_wrd = tc::smem_u32(&s_mb[16]);
   x.mb_strdy = tc::smem_u32(&s_mb[17]);
   x.mb_usp = tc::smem_u32(&s_mb[18]);
+  x.mb_hand1 = tc::smem_u32(&s_mb[19]);
+  x.mb_qrdy1 = tc::smem_u32(&s_mb[20]);
 
   if (warp == 0) tc::tmem_alloc(tc::smem_u32(&s_tmem), Plan::TMEM_COLS);
   if (tid == 0) {
     s_abort = 0;
     // arrival counts: copies and MMA commits 1, per-warp readiness 4 or 8
-    constexpr uint32_t kCount[19] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 8, 8, 8, 4, 4};
+    constexpr uint32_t kCount[kNumMbar] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 8, 8, 8, 4, 4, 1, 8};
 #pragma unroll
-    for (int i = 0; i < 19; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), kCount[i]);
+    for (int i = 0; i < kNumMbar; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), kCount[i]);
     tc::mbar_fence_init();
   }
   tc::fence_before_sync();
@@ -842,11 +917,11 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.tmem = s_tmem;
 
   if (warp < kConsumerWarps)
-    consumer_role<kOut>(x, p, tid);
+    consumer_role<kOut, kTest>(x, p, tid);
   else if (warp < kConsumerWarps + kProducerWarps)
-    producer_role<kOut, kNorm>(x, p, tid - kConsumerThreads);
+    producer_role<kOut, kNorm, kTest>(x, p, tid - kConsumerThreads);
   else if ((tid & 31) == 0)
-    issuer_role<kOut>(x, p, &tmap_q, &tmap_k, &tmap_v, &tmap_t, warp == kConsumerWarps + kProducerWarps + 1);
+    issuer_role<kOut, kTest>(x, p, &tmap_q, &tmap_k, &tmap_v, &tmap_t, warp == kConsumerWarps + kProducerWarps + 1);
 
   tc::fence_before_sync();
   __syncthreads();

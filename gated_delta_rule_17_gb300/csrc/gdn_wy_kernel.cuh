@@ -25,7 +25,7 @@
 // it with that token's output. The op therefore needs no scratch buffer, and
 // no row outside the batch's own output is touched.
 //
-// The kernel is persistent: four CTAs per SM each walk a strided list of
+// The kernel is persistent: five CTAs per SM each walk a strided list of
 // items; the copies of one CTA's item overlap the other CTAs' arithmetic. Items
 // are ordered head-fastest, so the v-heads that share a key head read its K tile
 // close together in time (the second read hits L2).

@@ -40,7 +40,9 @@ enum {
   GDN_ERR_UNSUPPORTED = 2,   /* dk/dv other than 128, nv not a multiple of nk, no sm_103 device */
   GDN_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (message names it) */
   GDN_ERR_DEVICE_STATUS = 4, /* a kernel found malformed cu_seqlens (reported by gdn_prefill_check) */
-  GDN_ERR_TIMEOUT = 5        /* a bounded on-device wait expired (reported by gdn_prefill_check) */
+  GDN_ERR_TIMEOUT = 5,       /* a bounded on-device wait expired (reported by gdn_prefill_check) */
+  GDN_ERR_RANGE = 6          /* an output or final state came out non-finite: an operand left the
+                                fp16 range (reported by gdn_prefill_check) */
 };
 
 /*
@@ -104,7 +106,12 @@ typedef struct {
  * Numerics: products run on the tensor cores with fp16 operands (split into
  * hi + lo pairs where the output needs it) and fp32 accumulation; the
  * triangular solve and the state are carried in fp32. Inputs must keep |v|,
- * |S| and intermediate values inside the fp16 range (about 6.5e4).
+ * |S| and intermediate values inside the fp16 range (|x| < 65504). This is
+ * narrower than bf16's range, so it is checked: an operand outside it turns
+ * into inf or NaN on conversion, which reaches the outputs or the final state,
+ * and any non-finite value there sets the device status bit that
+ * gdn_prefill_check reports as GDN_ERR_RANGE (the state and outputs of that
+ * call are then not usable).
  * Allocation: needs gdn_prefill_workspace_bytes() of device scratch, which
  * this call allocates and frees stream-ordered (cudaMallocAsync /
  * cudaFreeAsync); use gdn_prefill_ex to supply it instead.
@@ -130,7 +137,9 @@ int gdn_prefill(const void* q, const void* k, const void* v, const float* g, con
  * or 152 when no device is visible. */
 size_t gdn_prefill_workspace_bytes(int B, int T, int nv, int dk, int dv, int varlen);
 
-/* gdn_prefill with caller-provided scratch: `workspace` is a device buffer
+/* gdn_prefill with caller-provided scratch (the GDN prefill op likewise takes
+ * its scratch from the caller: ssm_gdn_a3.rs, `gdn_prefill_fla` arguments, the
+ * caller-owned `gdn_fla_scratch` buffer arena): `workspace` is a device buffer
  * of at least gdn_prefill_workspace_bytes(...) bytes (may be NULL when that
  * is 0), 256-byte aligned, not used by other work until the stream passes
  * this call. Allocates nothing. Varlen batches require the full size (else
@@ -215,17 +224,43 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
                          size_t workspace_bytes, void* stream);
 
 /* Synchronise `stream`, then read and clear the current device's status word
- * that kernels set on malformed cu_seqlens (GDN_ERR_DEVICE_STATUS) or on an
- * expired bounded wait (GDN_ERR_TIMEOUT). The word is shared by all calls on
- * the device since the last check. */
+ * that kernels set on malformed cu_seqlens (GDN_ERR_DEVICE_STATUS), on an
+ * expired bounded wait (GDN_ERR_TIMEOUT) or on a non-finite output or final
+ * state (GDN_ERR_RANGE). The word is shared by all calls on the device since
+ * the last check. The device-side counterpart of the op's host guards
+ * (ssm_gdn_a3.rs, the named-reject guards around `gdn_tc_spine_reject`):
+ * what only the kernels can see is reported here instead of silently. After
+ * GDN_ERR_TIMEOUT the call's output rows and state are incomplete (output rows
+ * may still hold the WY hand-off words); the next call is unaffected. */
 int gdn_prefill_check(void* stream);
 
 /* Message for the last error returned on the calling thread, naming the
- * argument or guard that rejected the call ("" after success). */
+ * argument or guard that rejected the call ("" after success); the op's
+ * named-reject guards (ssm_gdn_a3.rs, `gdn_tc_spine_reject` and the reasons it
+ * logs) likewise name what rejected a launch. Thread-local; valid until the
+ * next call on the same thread. */
 const char* gdn_last_error(void);
 
-/* Number of kernel launches the last successful call on this thread enqueued. */
+/* Number of kernel launches the last successful call on this thread enqueued
+ * (the op's dispatch in ssm_gdn_a3.rs, `gdn_prefill_fla`, is a fixed sequence
+ * of stage launches; here 2 for a dense batch, 3 with cu_seqlens, more on the
+ * segment-parallel schedule). A measurement aid: bench harnesses count the
+ * kernels they time with it. */
 int gdn_last_launch_count(void);
+
+/* Test hooks, for the library's own tests only (no counterpart in the op):
+ * later gdn_prefill* calls on this host thread run a separate test build of
+ * the spine kernel (dense or varlen, without the fused q/k norms) that
+ *   - uses wait_limit_ns (> 0) instead of the 2 s limit of every bounded wait,
+ *   - makes its consumer warps sleep consumer_delay_ns before the hand-off
+ *     wait of every odd chunk (the producer warps then run ahead), and
+ *   - skips the producer's hand-off arrival of chunk skip_hand_off_chunk
+ *     (>= 0), so that the waits on it expire and the call reports
+ *     GDN_ERR_TIMEOUT through gdn_prefill_check.
+ * All three off (0, 0, -1) returns to the normal kernel. Delays above 100 ms
+ * per chunk are refused (GDN_ERR_ARG). Nothing faults or hangs: expired waits
+ * unwind the kernel, which frees its tensor memory and returns. */
+int gdn_set_test_hooks(int64_t wait_limit_ns, int64_t consumer_delay_ns, int skip_hand_off_chunk);
 
 #ifdef __cplusplus
 }
