@@ -503,26 +503,27 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     __syncthreads();
 
     // ---- T diag(beta) as fp16 hi + lo over the output rows of the chunk ------------------
-    // Thread pair (2t, 2t+1) writes row t: 32 columns each, hi at [0, 64), lo at [64, 128).
+    // Warp w writes rows 16w..16w+15, four rows per step: lanes 8r..8r+7 take row
+    // 16w + 4i + r, 8 columns each, so one store instruction writes the hi halves of
+    // four rows (four whole 128-byte segments) and the next their lo halves.
     {
-      const int t = tid >> 1, j0 = (tid & 1) * 32;
-      if (t < clen) {
-        uint16_t* dst = p.tb + (cur.row0 + t) * p.out_stride + static_cast<int64_t>(cur.h) * kDim;
+      const int c8 = (lane & 7) * 8;
+      const float4 b0 = p.t_only ? make_float4(1.f, 1.f, 1.f, 1.f) : *reinterpret_cast<const float4*>(s_beta + c8);
+      const float4 b1 = p.t_only ? make_float4(1.f, 1.f, 1.f, 1.f) : *reinterpret_cast<const float4*>(s_beta + c8 + 4);
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          const int jb = j0 + q8 * 8;
-          const float4 ta = *reinterpret_cast<const float4*>(lf + lf_idx(t, jb));
-          const float4 tb = *reinterpret_cast<const float4*>(lf + lf_idx(t, jb + 4));
-          float4 ba = *reinterpret_cast<const float4*>(s_beta + jb);
-          float4 bb = *reinterpret_cast<const float4*>(s_beta + jb + 4);
-          if (p.t_only) ba = bb = make_float4(1.f, 1.f, 1.f, 1.f);
+      for (int i = 0; i < 4; ++i) {
+        const int t = 16 * warp + 4 * i + (lane >> 3);
+        if (t < clen) {
+          uint16_t* dst = p.tb + (cur.row0 + t) * p.out_stride + static_cast<int64_t>(cur.h) * kDim + c8;
+          const float4 ta = *reinterpret_cast<const float4*>(lf + lf_idx(t, c8));
+          const float4 tb = *reinterpret_cast<const float4*>(lf + lf_idx(t, c8 + 4));
           uint32_t hi[4], lo[4];
-          split_half2(ta.x * ba.x, ta.y * ba.y, hi[0], lo[0]);
-          split_half2(ta.z * ba.z, ta.w * ba.w, hi[1], lo[1]);
-          split_half2(tb.x * bb.x, tb.y * bb.y, hi[2], lo[2]);
-          split_half2(tb.z * bb.z, tb.w * bb.w, hi[3], lo[3]);
-          *reinterpret_cast<uint4*>(dst + jb) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(dst + 64 + jb) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          split_half2(ta.x * b0.x, ta.y * b0.y, hi[0], lo[0]);
+          split_half2(ta.z * b0.z, ta.w * b0.w, hi[1], lo[1]);
+          split_half2(tb.x * b1.x, tb.y * b1.y, hi[2], lo[2]);
+          split_half2(tb.z * b1.z, tb.w * b1.w, hi[3], lo[3]);
+          *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(dst + 64) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
     }
