@@ -90,6 +90,7 @@ int device_info(DeviceInfo** out) {
                           reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<true, false, true>),
                           reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<true, true>),
                           reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<false, false>),
+                          reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<false, false, false, true>),
                           reinterpret_cast<const void*>(gdn::gdn_prefill_kernel<false, true>)}) {
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, gdn::Plan::DYN_SMEM);
       if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -97,7 +98,6 @@ int device_info(DeviceInfo** out) {
     e = cudaFuncSetAttribute(gdn::gdn_wy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gdn::WyPlan::DYN_SMEM);
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     const std::pair<const void*, int> bwd[] = {
-        {reinterpret_cast<const void*>(gdn::gdn_bwd_states_kernel), gdn::kStatesSmem},
         {reinterpret_cast<const void*>(gdn::gdn_bwd_dstates_tc_kernel), gdn::DsPlan::DYN_SMEM},
         {reinterpret_cast<const void*>(gdn::gdn_bwd_grads_kernel), gdn::kGradsSmem}};
     for (const auto& f : bwd) {
@@ -759,9 +759,10 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   if (rows > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "%lld token rows exceed the 2^31 TMA coordinate range", (long long)rows);
   const BwdLayout l = bwd_layout(B, T, nv, cu_seqlens != nullptr);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  CUtensorMap mq, mk;
+  CUtensorMap mq, mk, mv;
   if (int rc = make_map(&mq, q, static_cast<int64_t>(nk) * gdn::kDim, rows, r.q, "q")) return rc;
   if (int rc = make_map(&mk, k, static_cast<int64_t>(nk) * gdn::kDim, rows, r.k, "k")) return rc;
+  if (int rc = make_map(&mv, v, static_cast<int64_t>(nv) * gdn::kDim, rows, r.v, "v")) return rc;
   gdn::WyParams w;
   int64_t wy_grid = 0;
   if (int rc = wy_geometry(*d, B, T, nv, cu_seqlens != nullptr, &w.items, &wy_grid)) return rc;
@@ -778,6 +779,13 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaMallocAsync(%zu): %s", l.total, cudaGetErrorString(e));
   }
   char* w8 = static_cast<char*>(ws);
+  // the WY kernel's T rows (16-bit), read back by the forward chain's copies
+  CUtensorMap mt;
+  if (int rc = make_map(&mt, w8 + l.tm, static_cast<int64_t>(nv) * gdn::kDim, rows, static_cast<int64_t>(nv) * gdn::kDim,
+                        "T")) {
+    if (!workspace) cudaFreeAsync(ws, s);
+    return rc;
+  }
   int32_t* sched = cu_seqlens ? reinterpret_cast<int32_t*>(w8 + l.sched) : nullptr;
   int32_t* order = sched;
   int32_t* cu_chunks = sched ? sched + B : nullptr;
@@ -841,7 +849,31 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   }
   gdn::gdn_wy_kernel<<<static_cast<unsigned>(wy_grid), gdn::kWyThreads, gdn::WyPlan::DYN_SMEM, s>>>(mk, w);
   const unsigned chains = static_cast<unsigned>(static_cast<int64_t>(B) * nv);
-  gdn::gdn_bwd_states_kernel<<<chains, gdn::kBcThreads, gdn::kStatesSmem, s>>>(p);
+  // the forward chain: the output-free spine, storing each chunk's entry state and u
+  gdn::ChunkParams fc{};
+  fc.g = g;
+  fc.state = const_cast<void*>(h0);
+  fc.out = nullptr;
+  fc.cu_seqlens = cu_seqlens;
+  fc.order = order;
+  fc.status = d->status;
+  fc.g_stride = r.g;
+  fc.out_stride = 0;
+  fc.B = B;
+  fc.T = T;
+  fc.nk = nk;
+  fc.nv = nv;
+  fc.state_is_table = r.table;
+  fc.qk_l2norm = 0;
+  fc.seg = nullptr;
+  fc.test_wait_ns = static_cast<int64_t>(gdn::kWaitLimitNs);
+  fc.test_delay_ns = 0;
+  fc.test_skip_chunk = -1;
+  fc.beta = beta;
+  fc.beta_stride = r.beta;
+  fc.s0buf = p.s0buf;
+  fc.ubuf = p.ubuf;
+  gdn::gdn_prefill_kernel<false, false, false, true><<<chains, gdn::kThreads, gdn::Plan::DYN_SMEM, s>>>(mq, mk, mv, mt, fc);
   gdn::gdn_bwd_dstates_tc_kernel<<<chains, gdn::kDsThreads, gdn::DsPlan::DYN_SMEM, s>>>(mq, mk, p);
   gdn::gdn_bwd_grads_kernel<<<static_cast<unsigned>(grad_items), gdn::kBcThreads, gdn::kGradsSmem, s>>>(p);
   launches += 4;

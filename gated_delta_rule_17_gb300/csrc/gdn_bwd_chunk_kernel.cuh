@@ -31,17 +31,15 @@
 //               plus gamma <dS_end, S0> + sum_t w_t on the last token
 //     dg_t = sum of d b over the chunk's tokens t .. 63
 //
-// Three kernels: gdn_bwd_states_kernel runs the forward chain once per (sequence,
-// v-head), storing every chunk's entry state S0 and u; gdn_bwd_dstates_tc_kernel
-// (gdn_bwd_dstates_tc.cuh, on tcgen05) runs the reverse chain, storing every chunk's
-// dS_end and du' and writing dV;
-// gdn_bwd_grads_kernel takes one (chunk, key head) each and writes dQ, dK (summed
-// over the key head's GQA group of value heads), and dbeta and dg of every value head.
-// T comes from the forward's WY kernel (unscaled by beta). In the two kernels here
-// every contraction is an fp16 tensor-core product with fp32 accumulation
-// (gdn_mma.cuh); the forward chain carries its state in fp32 registers and feeds it
-// to the tensor cores as an fp16 hi + lo pair, as it does the operands that enter
-// the chain (T, beta X, u).
+// Three chain and gradient kernels: the forward chain is the output-free spine of
+// gdn_prefill_kernel.cuh (tcgen05, state in tensor memory; its backward instantiation
+// scales the WY kernel's T by beta and stores every chunk's entry state S0 and u);
+// gdn_bwd_dstates_tc_kernel (gdn_bwd_dstates_tc.cuh, on tcgen05) runs the reverse
+// chain, storing every chunk's dS_end and du' and writing dV; gdn_bwd_grads_kernel
+// (here) takes one (chunk, key head) each and writes dQ, dK (summed over the key
+// head's GQA group of value heads), and dbeta and dg of every value head. T comes
+// from the forward's WY kernel (unscaled by beta). In the gradient kernel every
+// contraction is an fp16 tensor-core product with fp32 accumulation (gdn_mma.cuh).
 //
 // Padding tokens of a ragged last chunk are loaded as q = k = v = dO = 0,
 // g = beta = 0, and T's rows past the chunk's end as 0: every product then
@@ -160,25 +158,6 @@ __device__ __forceinline__ void bc_put_bf16_as_f16(__half* dst, const BcRows16& 
   }
 }
 
-// 16-bit rows -> tile, unconverted
-__device__ __forceinline__ void bc_put16(void* dst, const BcRows16& r) {
-  uint16_t* d16 = static_cast<uint16_t*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
-    *reinterpret_cast<uint4*>(d16 + row * kLd + 8 * c8) = r.x[i];
-  }
-}
-
-// T rows (64 fp16 hi then 64 lo) -> the hi and lo 64 x 64 tiles
-__device__ __forceinline__ void bc_put_t(__half* th, __half* tl, const BcRows16& r) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
-    *reinterpret_cast<uint4*>((c8 < 8 ? th : tl) + row * kLd64 + 8 * (c8 & 7)) = r.x[i];
-  }
-}
-
 // fp32 rows -> fp16 tile; row `row` (= warp + 8 i for this thread) scaled by scale_of(row)
 template <typename Scale>
 __device__ __forceinline__ void bc_put_f32(__half* dst, const BcRows32& r, Scale scale_of) {
@@ -207,189 +186,10 @@ __device__ __forceinline__ GatePrefix bc_put_gates(const BcGates& x, float* s_b,
 }
 
 
-// fp32 accumulator fragment -> fp16 hi and lo tiles (row-major, leading dimension ld).
-template <int NT>
-__device__ __forceinline__ void bc_store_split(const float (&c)[NT][4], __half* hi, __half* lo, int ld, int m0,
-                                               int n0) {
-  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
-#pragma unroll
-  for (int j = 0; j < NT; ++j)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int row = m0 + gq + 8 * e, col = n0 + 8 * j + 2 * tq;
-      __half2 h, l;
-      mm::split2(c[j][2 * e], c[j][2 * e + 1], h, l);
-      *reinterpret_cast<__half2*>(hi + row * ld + col) = h;
-      *reinterpret_cast<__half2*>(lo + row * ld + col) = l;
-    }
-}
-
-template <int NT>
-__device__ __forceinline__ void bc_store_split2(const float (&c)[2][NT][4], __half* hi, __half* lo, int ld, int m0,
-                                                int n0) {
-  bc_store_split<NT>(c[0], hi, lo, ld, m0, n0);
-  bc_store_split<NT>(c[1], hi, lo, ld, m0 + 16, n0);
-}
-
 // Warp tiles. A 64 x 128 product gives warp w the 32 x 32 block at rows 32 (w % 2),
-// columns 32 (w / 2); a 128 x 128 product (a chain's state) the 32 x 64 block at rows
-// 32 (w % 4), columns 64 (w / 4); a 64 x 64 product the 16 x 32 block at rows
-// 16 (w % 4), columns 32 (w / 4). Element (mt, j, x) of a thread's two-row-tile
+// columns 32 (w / 2); a 64 x 64 product the 16 x 32 block at rows 16 (w % 4),
+// columns 32 (w / 4). Element (mt, j, x) of a thread's two-row-tile
 // accumulator sits at row m0 + 16 mt + g + 8 (x / 2), column n0 + 8 j + 2 t + x % 2.
-
-// 128 x 128 fp16 tile (leading dimension kLd) -> global [128][128].
-__device__ __forceinline__ void bc_store_state(__half* dst, const __half* src) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int idx = threadIdx.x + kBcThreads * i, row = idx >> 4, c8 = idx & 15;
-    reinterpret_cast<uint4*>(dst + row * kDim)[c8] = *reinterpret_cast<const uint4*>(src + row * kLd + 8 * c8);
-  }
-}
-
-__device__ __forceinline__ const float* bc_h0(const BwdChunkParams& p, int s, int h) {
-  const float* h0 = p.state_is_table ? reinterpret_cast<const float* const*>(p.h0)[s]
-                                     : reinterpret_cast<const float*>(p.h0) + static_cast<int64_t>(s) * p.nv * kDim * kDim;
-  return h0 + static_cast<int64_t>(h) * kDim * kDim;
-}
-
-// ---- forward chain: every chunk's entry state S0 and u ------------------------------
-// One CTA per (sequence, v-head). The state lives in fp32 registers (warp tiles of
-// the 128 x 128 state, k by v).
-constexpr int kStatesSmem = 2 * kTile128 + 2 * kTile64 + 2 * kTileState + 4 * kTile128;
-
-__global__ void __launch_bounds__(kBcThreads, 1) gdn_bwd_states_kernel(const BwdChunkParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  __half* sK = reinterpret_cast<__half*>(smem);
-  __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(smem + kTile128);
-  __half* sTh = reinterpret_cast<__half*>(smem + 2 * kTile128);
-  __half* sTl = sTh + kChunk * kLd64;
-  __half* sSh = reinterpret_cast<__half*>(smem + 2 * kTile128 + 2 * kTile64);
-  __half* sSl = sSh + kDim * kLd;
-  __half* sXh = sSl + kDim * kLd;
-  __half* sXl = sXh + kChunk * kLd;
-  __half* sUh = sXl + kChunk * kLd;
-  __half* sUl = sUh + kChunk * kLd;
-  __shared__ float s_b[kChunk], s_beta[kChunk];
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, tq = lane & 3;
-  const int si = blockIdx.x / p.nv, h = blockIdx.x % p.nv, kh = h / (p.nv / p.nk);
-  const int s = p.order ? p.order[si] : si;
-  int64_t row0, len;
-  if (!bc_sequence(p, s, row0, len)) return;
-  const int64_t nch = (len + kChunk - 1) / kChunk;
-  if (nch == 0) return;
-  const int64_t hrow = static_cast<int64_t>(p.nv) * kDim;  // row stride of the [rows][nv][128] buffers
-  const int sm0 = 32 * (warp & 3), sn0 = 64 * (warp >> 2);  // state tile
-  const int m0 = 32 * (warp & 1), n0 = 32 * (warp >> 1);    // 64 x 128 products
-  const uint32_t aK = mm::saddr(sK), aTh = mm::saddr(sTh), aTl = mm::saddr(sTl), aSh = mm::saddr(sSh),
-                 aSl = mm::saddr(sSl), aXh = mm::saddr(sXh), aXl = mm::saddr(sXl), aUh = mm::saddr(sUh),
-                 aUl = mm::saddr(sUl);
-
-  float S[2][8][4];
-  {
-    const float* h0 = bc_h0(p, s, h);
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float2 x =
-              *reinterpret_cast<const float2*>(h0 + (sm0 + 16 * mt + gq + 8 * e) * kDim + sn0 + 8 * j + 2 * tq);
-          S[mt][j][2 * e] = x.x;
-          S[mt][j][2 * e + 1] = x.y;
-        }
-  }
-  bc_store_split2<8>(S, sSh, sSl, kLd, sm0, sn0);
-
-  BcRows16 fk, fv, ft;
-  BcGates fg;
-  auto fetch = [&](int64_t c) {
-    const int64_t r0 = row0 + c * kChunk;
-    const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
-    bc_fetch16(fk, p.k + r0 * p.k_stride + kh * kDim, p.k_stride, n);
-    bc_fetch16(fv, p.v + r0 * p.v_stride + h * kDim, p.v_stride, n);
-    bc_fetch16(ft, p.tm + r0 * hrow + h * kDim, hrow, n);
-    bc_fetch_gates(fg, p, r0, n, h);
-  };
-  fetch(0);
-  __syncthreads();
-
-  for (int64_t c = 0; c < nch; ++c) {
-    const int64_t r0 = row0 + c * kChunk;
-    const int n = static_cast<int>(len - c * kChunk < kChunk ? len - c * kChunk : kChunk);
-    bc_store_state(p.s0buf + (bc_slot(row0, s, c) * p.nv + h) * kDim * kDim, sSh);
-    bc_put_gates(fg, s_b, s_beta);
-    bc_put_bf16_as_f16(sK, fk);
-    bc_put16(sV, fv);
-    bc_put_t(sTh, sTl, ft);
-    __syncthreads();
-    if (c + 1 < nch) fetch(c + 1);  // in flight while this chunk computes
-
-    // K S0, then beta X = beta (V - Gamma K S0) as fp16 hi + lo
-    {
-      float acc[2][4][4];
-      mm::zero(acc);
-      mm::warp_mma2_sum<false, false, 4>(acc, aK, kLd, aSh, aSl, kLd, m0, n0, kDim);
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = m0 + 16 * mt + gq + 8 * e;
-          const float G = __expf(s_b[t]), bt = s_beta[t];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 vv =
-                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sV + t * kLd + n0 + 8 * j + 2 * tq));
-            acc[mt][j][2 * e] = bt * (vv.x - G * acc[mt][j][2 * e]);
-            acc[mt][j][2 * e + 1] = bt * (vv.y - G * acc[mt][j][2 * e + 1]);
-          }
-        }
-      bc_store_split2<4>(acc, sXh, sXl, kLd, m0, n0);
-    }
-    __syncthreads();
-
-    // u = T (beta X): stored for the gradient kernel; (gamma / Gamma) u as fp16 hi + lo
-    {
-      float acc[2][4][4];
-      mm::zero(acc);
-      mm::warp_mma2_sum<false, false, 4>(acc, aTh, kLd64, aXh, aXl, kLd, m0, n0, kChunk);
-      mm::warp_mma2<false, false, 4>(acc, aTl, kLd64, aXh, kLd, m0, n0, kChunk);
-      const float blast = s_b[kChunk - 1];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = m0 + 16 * mt + gq + 8 * e;
-          const float sc = __expf(blast - s_b[t]);
-          __half* urow = p.ubuf + (r0 + t) * hrow + h * kDim + n0 + 2 * tq;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (t < n)
-              *reinterpret_cast<__half2*>(urow + 8 * j) = __floats2half2_rn(acc[mt][j][2 * e], acc[mt][j][2 * e + 1]);
-            acc[mt][j][2 * e] *= sc;
-            acc[mt][j][2 * e + 1] *= sc;
-          }
-        }
-      bc_store_split2<4>(acc, sUh, sUl, kLd, m0, n0);
-    }
-    __syncthreads();
-
-    // S = gamma S + K^T ((gamma / Gamma) u)
-    {
-      const float gam = __expf(s_b[kChunk - 1]);
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int x = 0; x < 4; ++x) S[mt][j][x] *= gam;
-      mm::warp_mma2_sum<true, false, 8>(S, aK, kLd, aUh, aUl, kLd, sm0, sn0, kChunk);
-      bc_store_split2<8>(S, sSh, sSl, kLd, sm0, sn0);
-    }
-    __syncthreads();
-  }
-}
 
 // ---- per-chunk gradients ----------------------------------------------------------
 // One CTA per (chunk, key head): it walks the value heads of the key head's GQA group,

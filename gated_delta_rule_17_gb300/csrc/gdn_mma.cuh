@@ -259,69 +259,6 @@ __device__ __forceinline__ void warp_mma2_pair(float (&c)[2][NT][4], float (&d)[
   }
 }
 
-// warp_mma2 of one A against the sum of two B tiles, c += A B + A B2 (the hi and lo
-// halves of a split operand), with each A fragment loaded once for both. B2 has B's
-// orientation and leading dimension (shared address b2). Per K step the two products
-// are accumulated in turn, so the rounding order differs from two separate calls.
-template <bool kAT, bool kBT, int NT, int kUnroll = 2>
-__device__ __forceinline__ void warp_mma2_sum(float (&c)[2][NT][4], uint32_t a, int lda, uint32_t b, uint32_t b2,
-                                              int ldb, int m0, int n0, int K) {
-  static_assert(NT % 2 == 0, "B operands are loaded two n8 tiles at a time");
-  const int lane = threadIdx.x & 31;
-  uint32_t a_lane, b_lane;
-  int a_step, b_step;
-  uint32_t a_next;
-  if (!kAT) {
-    a_lane = a + 2u * static_cast<uint32_t>((m0 + (lane & 15)) * lda + (lane >> 4) * 8);
-    a_step = 32;
-    a_next = 32u * lda;
-  } else {
-    a_lane = a + 2u * static_cast<uint32_t>(((lane & 7) + ((lane >> 4) << 3)) * lda + m0 + ((lane >> 3) & 1) * 8);
-    a_step = 32 * lda;
-    a_next = 32u;
-  }
-  if (kBT) {
-    b_lane = b + 2u * static_cast<uint32_t>((n0 + (lane & 7) + ((lane >> 4) << 3)) * ldb + ((lane >> 3) & 1) * 8);
-    b_step = 32;
-  } else {
-    b_lane = b + 2u * static_cast<uint32_t>((lane & 15) * ldb + n0 + (lane >> 4) * 8);
-    b_step = 32 * ldb;
-  }
-  const uint32_t b_other = b2 - b;  // bytes from B's tile to B2's
-  const uint32_t b_pair = kBT ? 32u * ldb : 32u;
-#pragma unroll kUnroll
-  for (int k0 = 0; k0 < K; k0 += 16) {
-    uint32_t af0[4], af1[4];
-    if (!kAT) {
-      ldsm_x4(a_lane, af0);
-      ldsm_x4(a_lane + a_next, af1);
-    } else {
-      ldsm_x4_t(a_lane, af0);
-      ldsm_x4_t(a_lane + a_next, af1);
-    }
-#pragma unroll
-    for (int j = 0; j < NT / 2; ++j) {
-      uint32_t bf[4], bg[4];
-      if (kBT) {
-        ldsm_x4(b_lane + j * b_pair, bf);
-        ldsm_x4(b_lane + b_other + j * b_pair, bg);
-      } else {
-        ldsm_x4_t(b_lane + j * b_pair, bf);
-        ldsm_x4_t(b_lane + b_other + j * b_pair, bg);
-      }
-      mma16816(c[0][2 * j], af0, bf[0], bf[1]);
-      mma16816(c[0][2 * j + 1], af0, bf[2], bf[3]);
-      mma16816(c[1][2 * j], af1, bf[0], bf[1]);
-      mma16816(c[1][2 * j + 1], af1, bf[2], bf[3]);
-      mma16816(c[0][2 * j], af0, bg[0], bg[1]);
-      mma16816(c[0][2 * j + 1], af0, bg[2], bg[3]);
-      mma16816(c[1][2 * j], af1, bg[0], bg[1]);
-      mma16816(c[1][2 * j + 1], af1, bg[2], bg[3]);
-    }
-    a_lane += a_step;
-    b_lane += b_step;
-  }
-}
 
 template <int NT>
 __device__ __forceinline__ void zero(float (&c)[NT][4]) {
@@ -343,13 +280,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
-
-// fp16 hi + lo of a pair: hi = fp16(x), lo = fp16(x - hi)
-__device__ __forceinline__ void split2(float x, float y, __half2& hi, __half2& lo) {
-  hi = __floats2half2_rn(x, y);
-  const float2 f = __half22float2(hi);
-  lo = __floats2half2_rn(x - f.x, y - f.y);
-}
 
 }  // namespace mm
 }  // namespace gdn

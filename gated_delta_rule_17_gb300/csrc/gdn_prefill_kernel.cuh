@@ -84,6 +84,14 @@ struct ChunkParams {
   // hand-off arrival the producer skips (-1: none), so that bounded waits expire.
   int64_t test_wait_ns, test_delay_ns;
   int test_skip_chunk;
+  // The backward's forward chain (kBwd = true): the WY kernel hands over T itself (not
+  // T diag(beta)), so the producer scales the tile's columns by beta in place; each
+  // chunk's entry state S0 and u are stored as fp16 for the gradient kernels; the
+  // carried-in state is only read.
+  const float* beta;
+  int64_t beta_stride;
+  __half* s0buf;  // [slots][nv][128][128]: S0 of chunk c in slot row0 / 64 + s + c, [k][v]
+  __half* ubuf;   // [rows][nv][128]: u
 };
 constexpr int kSegNoOutput = 1;
 constexpr int kSegZeroValues = 2;
@@ -133,6 +141,7 @@ struct Ctx {
   float *s_rq, *s_rk;   // fused prologue: 1 / |q_t|, 1 / |k_t| of the current chunk
   int* s_fast;          // [2] 1 when the chunk's gate range allows the factorised decays
   float* s_gstage;      // [2][64] g of a chunk, staged by cp.async
+  float *s_bstage, *s_bv;  // backward's forward chain: beta staged, and beta of a gate set
   float* s_elast;       // [3] e^{gc_last} by chunk index mod 3 (read by the consumer)
   volatile int* s_abort;
   // Barriers and why none can complete twice ahead of a waiter (chunk c; "->" is
@@ -197,7 +206,7 @@ __device__ __forceinline__ uint64_t wait_limit(const ChunkParams& p) {
 // (the issuer runs its MMAs). Warp 4 also scans the gates of the chunk after,
 // so every chunk starts with its gate set ready.
 // ---------------------------------------------------------------------------------
-template <bool kOut, bool kNorm, bool kTest>
+template <bool kOut, bool kNorm, bool kTest, bool kBwd>
 __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p, int ptid) {
   using P = Plan;
   const uint64_t lim = wait_limit<kTest>(p);
@@ -213,14 +222,18 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
   // into gate set c & 1 one chunk ahead
   auto load_gates = [&](int c) {
     float* st = x.s_gstage + (c & 1) * kChunk;
+    float* sb = x.s_bstage + (c & 1) * kChunk;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int tt = 2 * lane + e;
       const int64_t t = static_cast<int64_t>(c) * kChunk + tt;
-      if (t < x.len)
+      if (t < x.len) {
         tc::cp_async_4(tc::smem_u32(st + tt), p.g + (x.row0 + t) * p.g_stride + x.h);
-      else
+        if constexpr (kBwd) tc::cp_async_4(tc::smem_u32(sb + tt), p.beta + (x.row0 + t) * p.beta_stride + x.h);
+      } else {
         st[tt] = 0.f;
+        if constexpr (kBwd) sb[tt] = 0.f;
+      }
     }
     tc::cp_async_commit();
   };
@@ -244,6 +257,10 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     x.s_E[gs + 2 * lane + 1] = __expf(gp.gcb - mid);
     x.s_F[gs + 2 * lane] = __expf(mid - gp.gca);
     x.s_F[gs + 2 * lane + 1] = __expf(mid - gp.gcb);
+    if constexpr (kBwd) {  // beta of the gate set, for the T diag(beta) pass
+      x.s_bv[gs + 2 * lane] = x.s_bstage[gs + 2 * lane];
+      x.s_bv[gs + 2 * lane + 1] = x.s_bstage[gs + 2 * lane + 1];
+    }
     if (lane == 0) {
       x.s_elast[c % 3] = __expf(gp.last);
       x.s_fast[c & 1] = (gp.first - gp.last) <= kFactorisedRange;
@@ -312,6 +329,33 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       signal(x.mb_vrdy);  // V is fp16: the U MMAs may go
       if constexpr (kNorm) tc::named_barrier(kBarNorm, kProducerThreads);
     } else {
+      if constexpr (kBwd) {
+        // lane quarters 2-3 (no A epilogue without outputs): T -> T diag(beta) in place
+        // (fp16 hi + lo, 22 significant bits), once the tile has landed: column j scaled
+        // by beta_j; columns past the chunk's end get 0. Then the U MMAs may go.
+        ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_t, c & 1, lim);
+        tc::fence_after_sync();
+        if (ok) {
+#pragma unroll 1
+          for (int r = 0; r < 8; ++r) {  // 4 columns (8 bytes of hi, 8 of lo) per step
+            const int it = hq + r * 128, t = it >> 4, j4 = (it & 15) * 4;
+            const uint32_t o = P::TB + tc::sw128(t, j4 * 2);
+            const uint2 h = *reinterpret_cast<const uint2*>(sm + o);
+            const uint2 l = *reinterpret_cast<const uint2*>(sm + o + 8192);
+            const float2 h0 = __half22float2(*reinterpret_cast<const __half2*>(&h.x));
+            const float2 h1 = __half22float2(*reinterpret_cast<const __half2*>(&h.y));
+            const float2 l0 = __half22float2(*reinterpret_cast<const __half2*>(&l.x));
+            const float2 l1 = __half22float2(*reinterpret_cast<const __half2*>(&l.y));
+            const float4 bj = *reinterpret_cast<const float4*>(x.s_bv + gs + j4);
+            uint2 nh, nl;
+            split_half2((h0.x + l0.x) * bj.x, (h0.y + l0.y) * bj.y, nh.x, nl.x);
+            split_half2((h1.x + l1.x) * bj.z, (h1.y + l1.y) * bj.w, nh.y, nl.y);
+            *reinterpret_cast<uint2*>(sm + o) = nh;
+            *reinterpret_cast<uint2*>(sm + o + 8192) = nl;
+          }
+        }
+        signal(x.mb_vrdy);
+      }
       // ---- A (fp16 hi + lo) from Q K^T, lanes 64-127 ------------------------------------
       if constexpr (kNorm) {
         // fused prologue, while the Gram MMA runs: one raw row per thread, K rows 0-63
@@ -486,8 +530,8 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 // Consumer: the state spine and the output of each chunk. Thread v owns value
 // column v: tensor-memory lane v holds S^T[v][:], u^T[v][:] and O^T[v][:].
 // ---------------------------------------------------------------------------------
-template <bool kOut, bool kTest>
-__device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p, int ctid) {
+template <bool kOut, bool kTest, bool kBwd>
+__device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p, int ctid, int seq) {
   using P = Plan;
   const uint64_t lim = wait_limit<kTest>(p);
   const int quad = ctid >> 5;
@@ -503,6 +547,14 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     if (lane == 0) tc::mbar_arrive(mbar);
   };
 
+  // backward's forward chain: this thread's value column of a chunk's entry state, as
+  // fp16 into its slot ([k][v]: the 32 lanes of a warp write 64 consecutive bytes)
+  auto store_s0 = [&](int c, int q4, const uint32_t (&s)[32]) {
+    __half* dst = p.s0buf + ((x.row0 / kChunk + seq + c) * p.nv + x.h) * kDim * kDim + (q4 * 32) * kDim + v;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) dst[e * kDim] = __float2half_rn(__uint_as_float(s[e]));
+  };
+
   // carried-in state: fp32 S^T into tensor memory, plus its fp16 operand copy
   {
     uint32_t s[32], st[32];
@@ -510,6 +562,7 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     for (int q4 = 0; q4 < 4; ++q4) {
 #pragma unroll
       for (int e = 0; e < 32; ++e) s[e] = __float_as_uint(x.state[(q4 * 32 + e) * kDim + v]);
+      if constexpr (kBwd) store_s0(0, q4, s);
       tc::tmem_st32(lanes + P::COL_S + q4 * 32, s);
 #pragma unroll
       for (int e = 0; e < 16; ++e)
@@ -571,6 +624,12 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
         uint32_t u[32], hi[16], lo[16];
         tc::tmem_ld32(lanes + col_u + h2 * 32, u);
         tc::tmem_ld_wait();
+        if constexpr (kBwd) {  // u rows for the gradient kernels (rows of the chunk only)
+          __half* dst = p.ubuf + (x.row0 + static_cast<int64_t>(c) * kChunk + h2 * 32) * (p.nv * kDim) + x.h * kDim + v;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (h2 * 32 + e < clen) dst[static_cast<int64_t>(e) * p.nv * kDim] = __float2half_rn(__uint_as_float(u[e]));
+        }
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           // columns past the end of the sequence are zeroed: their U and W rows came
@@ -597,6 +656,9 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
         uint32_t s[32], st[16];
         tc::tmem_ld32(lanes + P::COL_S + q4 * 32, s);
         tc::tmem_ld_wait();
+        if constexpr (kBwd) {
+          if (c + 1 < x.nchunks) store_s0(c + 1, q4, s);
+        }
 #pragma unroll
         for (int e = 0; e < 16; ++e) st[e] = pack_half2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1]));
         tc::tmem_st16u(lanes + P::COL_ST + q4 * 16, st);
@@ -633,7 +695,7 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     if (c + 1 < x.nchunks) decay_state(c + 1);
   }
 
-  if (*x.s_abort == 0) {  // carried-out state S_T, k-major
+  if (!kBwd && *x.s_abort == 0) {  // carried-out state S_T, k-major
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
       uint32_t s[32];
@@ -814,7 +876,7 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
 // none of its code. kTest: the test hooks of ChunkParams (wait limit, consumer delay,
 // skipped hand-off), likewise an instantiation of its own.
 constexpr int kNumMbar = 21;
-template <bool kOut = true, bool kNorm = false, bool kTest = false>
+template <bool kOut = true, bool kNorm = false, bool kTest = false, bool kBwd = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_t,
@@ -822,6 +884,7 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(16) float s_gc[2 * kChunk], s_eg[2 * kChunk], s_egq[2 * kChunk], s_edec[2 * kChunk];
   __shared__ __align__(16) float s_E[2 * kChunk], s_F[2 * kChunk], s_gstage[2 * kChunk];
+  __shared__ __align__(16) float s_bstage[kBwd ? 2 * kChunk : 1], s_bv[kBwd ? 2 * kChunk : 1];
   __shared__ __align__(16) float s_rq[kChunk], s_rk[kChunk];
   __shared__ float s_elast[3];
   __shared__ int s_fast[2];
@@ -879,6 +942,8 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.s_rk = s_rk;
   x.s_fast = s_fast;
   x.s_gstage = s_gstage;
+  x.s_bstage = s_bstage;
+  x.s_bv = s_bv;
   x.s_abort = &s_abort;
   x.mb_kq0 = tc::smem_u32(&s_mb[0]);
   x.mb_kq1 = tc::smem_u32(&s_mb[1]);
@@ -906,7 +971,8 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   if (tid == 0) {
     s_abort = 0;
     // arrival counts: copies and MMA commits 1, per-warp readiness 4 or 8
-    constexpr uint32_t kCount[kNumMbar] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 4, 8, 8, 8, 4, 4, 1, 8};
+    // (V ready: 4 arrivals, or 8 when lane quarters 2-3 also scale T by beta)
+    constexpr uint32_t kCount[kNumMbar] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, kBwd ? 8u : 4u, 8, 8, 8, 4, 4, 1, 8};
 #pragma unroll
     for (int i = 0; i < kNumMbar; ++i) tc::mbar_init(tc::smem_u32(&s_mb[i]), kCount[i]);
     tc::mbar_fence_init();
@@ -917,9 +983,9 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.tmem = s_tmem;
 
   if (warp < kConsumerWarps)
-    consumer_role<kOut, kTest>(x, p, tid);
+    consumer_role<kOut, kTest, kBwd>(x, p, tid, s);
   else if (warp < kConsumerWarps + kProducerWarps)
-    producer_role<kOut, kNorm, kTest>(x, p, tid - kConsumerThreads);
+    producer_role<kOut, kNorm, kTest, kBwd>(x, p, tid - kConsumerThreads);
   else if ((tid & 31) == 0)
     issuer_role<kOut, kTest>(x, p, &tmap_q, &tmap_k, &tmap_v, &tmap_t, warp == kConsumerWarps + kProducerWarps + 1);
 
