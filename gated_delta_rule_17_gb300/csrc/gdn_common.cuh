@@ -29,9 +29,11 @@ constexpr float kInvSqrtD = 0.08838834764831845f;  // 1 / sqrt(128)
 constexpr float kFactorisedRange = 120.f;
 
 // fp32 64 x 64 work matrix with 16-byte chunks XOR-swizzled by row, so that
-// float4 accesses by threads on different rows hit different banks.
+// float4 accesses by threads on different rows hit different banks; chunk k of a row
+// is also XORed with k / 8, so that chunks k and k + 8 of one row (256 bytes apart,
+// the same banks otherwise) land in different bank groups.
 __device__ __forceinline__ int lf_idx(int r, int c) {
-  return r * 64 + ((((c >> 2) ^ r) & 15) << 2) + (c & 3);
+  return r * 64 + ((((c >> 2) ^ r ^ (c >> 5)) & 15) << 2) + (c & 3);
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 raw, float (&f)[8]) {

@@ -36,6 +36,10 @@ namespace gdn {
 
 constexpr int kWyThreads = 128;
 constexpr int kWyCtasPerSm = 5;
+// X blocks of the 16 -> 32 merges: rows of 20 floats, so that rows four apart (read by
+// one quarter warp) fall in different bank groups
+constexpr int kX16Ld = 20;
+constexpr int kX16Blk = 16 * kX16Ld;
 
 struct WyParams {
   const float* g;
@@ -69,7 +73,7 @@ struct WyPlan {
   static constexpr int S_LT = 0;       // fp32 4 x 16 x 16 diagonal blocks of L, transposed
   static constexpr int S_AL = 4096;    // bf16 hi of L[32:64, 0:32] (A rows 32-63 of the tile at 0),
                                        //   lo 8 KB on (the tile at 8 KB); later T[32:64, 32:64]
-  static constexpr int S_X16 = 8192;   // fp32 2 x 16 x 16 partial products
+  static constexpr int S_X16 = 8192;   // fp32 2 x 16 x 16 partial products (rows padded to 20)
   static constexpr int BT_HI = 0;      // bf16 hi of T[0:32, 0:32] (B rows m), later of X (over S_LT)
   static constexpr int BT_LO = 8192;   // ... lo (over S_X16)
   static constexpr uint32_t TMEM_COLS = 64;  // K K^T (M = 64), then X and T22 X (32 columns each)
@@ -356,44 +360,59 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
     }
     __syncthreads();
     // (b) the 16 x 16 blocks (1,0) and (3,2) of T: X = L_{i,i-1} T_{i-1,i-1}, then
-    //     T_{i,i-1} = -T_ii X; threads 0-63 take block (1,0), 64-127 block (3,2),
-    //     1 x 4 outputs each.
-    {
-      const int blk = tid >> 6, r = (tid >> 2) & 15, c0 = (tid & 3) * 4;
-      const int rr = 32 * blk + 16 + r, cb = 32 * blk;
-      float lrow[16];
+    //     T_{i,i-1} = -T_ii X. Warp 0 takes block (1,0), warp 1 block (3,2), 2 x 4
+    //     outputs per lane. (A 16-byte shared load costs one pass per quarter warp even
+    //     when its lanes read one address, so the row of T or X that every output of a
+    //     row block needs is best read by fewer threads; one warp for both blocks read
+    //     least but ran longer.)
+    if (warp < 2) {
+      const int blk = warp, r0 = 2 * (lane >> 2), c0 = (lane & 3) * 4;
+      const int cb = 32 * blk;
+      float lr[2][16];
 #pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(rr, cb + 4 * i4));
-        lrow[4 * i4] = v4.x; lrow[4 * i4 + 1] = v4.y; lrow[4 * i4 + 2] = v4.z; lrow[4 * i4 + 3] = v4.w;
-      }
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+          const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(cb + 16 + r0 + i, cb + 4 * i4));
+          lr[i][4 * i4] = v4.x; lr[i][4 * i4 + 1] = v4.y; lr[i][4 * i4 + 2] = v4.z; lr[i][4 * i4 + 3] = v4.w;
+        }
+      float acc[2][4] = {};
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
         const float4 tv = *reinterpret_cast<const float4*>(lf + lf_idx(cb + m, cb + c0));
-        acc.x = fmaf(lrow[m], tv.x, acc.x); acc.y = fmaf(lrow[m], tv.y, acc.y);
-        acc.z = fmaf(lrow[m], tv.z, acc.z); acc.w = fmaf(lrow[m], tv.w, acc.w);
-      }
-      *reinterpret_cast<float4*>(x16 + blk * 256 + r * 16 + c0) = acc;
-    }
-    __syncthreads();
-    {
-      const int blk = tid >> 6, r = (tid >> 2) & 15, c0 = (tid & 3) * 4;
-      const int rr = 32 * blk + 16 + r, cb = 32 * blk + 16;
-      float trow[16];
 #pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(rr, cb + 4 * i4));
-        trow[4 * i4] = v4.x; trow[4 * i4 + 1] = v4.y; trow[4 * i4 + 2] = v4.z; trow[4 * i4 + 3] = v4.w;
+        for (int i = 0; i < 2; ++i) {
+          acc[i][0] = fmaf(lr[i][m], tv.x, acc[i][0]); acc[i][1] = fmaf(lr[i][m], tv.y, acc[i][1]);
+          acc[i][2] = fmaf(lr[i][m], tv.z, acc[i][2]); acc[i][3] = fmaf(lr[i][m], tv.w, acc[i][3]);
+        }
       }
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        *reinterpret_cast<float4*>(x16 + blk * kX16Blk + (r0 + i) * kX16Ld + c0) =
+            make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+          const float4 v4 = *reinterpret_cast<const float4*>(lf + lf_idx(cb + 16 + r0 + i, cb + 16 + 4 * i4));
+          lr[i][4 * i4] = v4.x; lr[i][4 * i4 + 1] = v4.y; lr[i][4 * i4 + 2] = v4.z; lr[i][4 * i4 + 3] = v4.w;
+        }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 #pragma unroll
       for (int m = 0; m < 16; ++m) {  // T_ii[r][m] = 0 for m > r
-        const float4 xv = *reinterpret_cast<const float4*>(x16 + blk * 256 + m * 16 + c0);
-        acc.x = fmaf(trow[m], xv.x, acc.x); acc.y = fmaf(trow[m], xv.y, acc.y);
-        acc.z = fmaf(trow[m], xv.z, acc.z); acc.w = fmaf(trow[m], xv.w, acc.w);
+        const float4 xv = *reinterpret_cast<const float4*>(x16 + blk * kX16Blk + m * kX16Ld + c0);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          acc[i][0] = fmaf(lr[i][m], xv.x, acc[i][0]); acc[i][1] = fmaf(lr[i][m], xv.y, acc[i][1]);
+          acc[i][2] = fmaf(lr[i][m], xv.z, acc[i][2]); acc[i][3] = fmaf(lr[i][m], xv.w, acc[i][3]);
+        }
       }
-      *reinterpret_cast<float4*>(lf + lf_idx(rr, cb - 16 + c0)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        *reinterpret_cast<float4*>(lf + lf_idx(cb + 16 + r0 + i, cb + c0)) =
+            make_float4(-acc[i][0], -acc[i][1], -acc[i][2], -acc[i][3]);
     }
     __syncthreads();
     // (c) the last merge on the tensor cores, with bf16 hi + lo operands. First
