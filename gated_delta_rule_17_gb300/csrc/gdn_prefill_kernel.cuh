@@ -139,6 +139,9 @@ struct Ctx {
   float *s_gc, *s_eg, *s_egq, *s_edec;  // gc, e^gc, e^gc / sqrt(dk), e^{gc_last - gc}
   float *s_E, *s_F;     // e^{gc - m}, e^{m - gc} about the chunk's mid gate m
   float *s_rq, *s_rk;   // fused prologue: 1 / |q_t|, 1 / |k_t| of the current chunk
+  float* s_qpart;       // fused prologue with outputs: [4][64] partial sums of q_t^2
+  float* s_rq3;         // ... and 1 / |q_t| by chunk index mod 3 ([3][64]), read at the store
+  float* s_rk3;         // ... and 1 / |k_t| by chunk index mod 3 ([3][64]), read by the u split
   int* s_fast;          // [2] 1 when the chunk's gate range allows the factorised decays
   float* s_gstage;      // [2][64] g of a chunk, staged by cp.async
   float *s_bstage, *s_bv;  // backward's forward chain: beta staged, and beta of a gate set
@@ -327,6 +330,27 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         }
       }
       signal(x.mb_vrdy);  // V is fp16: the U MMAs may go
+      if constexpr (kNorm && kOut) {
+        // fused prologue: |k_t|^2 is the diagonal of the Gram's K K^T half (tensor-memory
+        // lanes 0-63), read by the first warp of lane quarters 0 and 1. Only e^gc K (the
+        // W operand) takes 1 / |k_t| here; A and Kd are formed from the raw keys, and the
+        // consumer scales column t of u by 1 / |k_t| instead (S^T += u^T Kd and
+        // O^T += u^T A^T each have exactly one factor indexed by t)
+        ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, lim);
+        tc::fence_after_sync();
+        if (half == 0 && ok) {
+          uint32_t d[32];
+          tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + quad * 32, d);
+          tc::tmem_ld_wait();
+          float ss = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ss = (e == lane) ? __uint_as_float(d[e]) : ss;
+          const int t = quad * 32 + lane;
+          const float r = 1.f / sqrtf(ss + kL2Eps);
+          x.s_rk3[(c % 3) * kChunk + t] = r;
+          x.s_eg[gs + t] *= r;
+        }
+      }
       if constexpr (kNorm) tc::named_barrier(kBarNorm, kProducerThreads);
     } else {
       if constexpr (kBwd) {
@@ -357,12 +381,11 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         signal(x.mb_vrdy);
       }
       // ---- A (fp16 hi + lo) from Q K^T, lanes 64-127 ------------------------------------
-      if constexpr (kNorm) {
-        // fused prologue, while the Gram MMA runs: one raw row per thread, K rows 0-63
-        // then Q rows 0-63, read once the tile has landed and before any thread converts
-        // it in place. The inverse norms are folded into this chunk's per-token factors
-        // (K: e^gc, e^{gc_last-gc}, F; Q: e^gc/sqrt(dk), E) and kept apart for the
-        // direct-decay path
+      if constexpr (kNorm && !kOut) {
+        // fused prologue without outputs (no Gram to take |k|^2 from): one raw row per
+        // thread, K rows 0-63 then Q rows 0-63, read once the tile has landed and before
+        // any thread converts it in place. The inverse norms are folded into this chunk's
+        // per-token factors (K: e^gc, e^{gc_last-gc}, F; Q: e^gc/sqrt(dk), E)
         ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_kq1 : x.mb_kq0, use, lim);
         tc::fence_after_sync();
         const int row = half * 64 + (quad - 2) * 32 + lane, t = row & 63;
@@ -406,14 +429,13 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 #pragma unroll
             for (int e = 0; e < 8; ++e) a[e] = (j0 + e <= i) ? ei * f[e] * __uint_as_float(d[e]) : 0.f;
           } else {
-            constexpr bool norm = kNorm;
-            const float ri = (norm ? x.s_rq[i] : 1.f) * kInvSqrtD;
+            // (raw q and k: 1 / |q_i| is applied to the output row, 1 / |k_j| to u)
+            const float ri = kInvSqrtD;
             const float gi = x.s_gc[gs + i];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               const int j = j0 + e;
-              a[e] = (j <= i) ? __expf(gi - x.s_gc[gs + j]) * ri * (norm ? x.s_rk[j] : 1.f) * __uint_as_float(d[e])
-                              : 0.f;
+              a[e] = (j <= i) ? __expf(gi - x.s_gc[gs + j]) * ri * __uint_as_float(d[e]) : 0.f;
             }
           }
           uint32_t hi[4], lo[4];
@@ -424,6 +446,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
           *reinterpret_cast<uint4*>(sm + a_off + 8192 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
+      if constexpr (kNorm && kOut) tc::named_barrier(kBarNorm, kProducerThreads);
     }
 
     // ---- once the Gram MMA has read K: K -> e^gc K (fp16, in place, rows t) and --------
@@ -435,7 +458,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_kq1 : x.mb_kq0, use, lim);
     tc::fence_after_sync();
     if (ok) {
-#pragma unroll 1
+#pragma unroll
       for (int r0 = 0; r0 < 4; r0 += 2) {
       uint4 rk[2];
 #pragma unroll
@@ -462,6 +485,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     //      the spine of chunk c-1 has read Q~ (and -W^T) ------------------------------------
     if (kOut && c > 0) ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_c1, (c - 1) & 1, lim);
     if (kOut && ok) {
+      float qss = 0.f;  // fused prologue: this thread's part of |q_t|^2 (row t = ptid % 64)
 #pragma unroll 1
       for (int r0 = 0; r0 < 4; r0 += 2) {
         uint4 rq[2];
@@ -475,10 +499,15 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
           const int it = ptid + (r0 + r) * kProducerThreads, t = it & 63, cc = it >> 6;
           float f[8];
           unpack_bf16x8(rq[r], f);
+          if constexpr (kNorm) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qss = fmaf(f[e], f[e], qss);
+          }
           *reinterpret_cast<uint4*>(sm + P::QT + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
               t < clen ? pack_half8(f, x.s_egq[gs + t]) : make_uint4(0, 0, 0, 0);
         }
       }
+      if constexpr (kNorm) x.s_qpart[(ptid >> 6) * kChunk + (ptid & 63)] = qss;
     }
     signal(b ? x.mb_qrdy1 : x.mb_qrdy0);  // the raw K/Q tile is consumed: it may be refilled
     // ---- and the gates of the next chunk, into the other gate set (their copy was
@@ -492,6 +521,18 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     if (!tc::barrier_all(kBarProducer, kProducerThreads, ok && *x.s_abort == 0)) {
       if (leader) fail();
       break;
+    }
+    if constexpr (kNorm && kOut) {
+      // 1 / |q_t| of this chunk, for the consumer's output rows (the A and Q~ operands
+      // carry the raw q: both output terms are linear in q_t); published by the hand-off
+      if (pw == 2) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int t = h2 * 32 + lane;
+          const float ss = x.s_qpart[t] + x.s_qpart[kChunk + t] + x.s_qpart[2 * kChunk + t] + x.s_qpart[3 * kChunk + t];
+          x.s_rq3[(c % 3) * kChunk + t] = 1.f / sqrtf(ss + kL2Eps);
+        }
+      }
     }
     if (!group_wait(x, p, x.mb_uw, b, kBarProducer, kProducerThreads, leader, lim)) break;
 
@@ -530,7 +571,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
 // Consumer: the state spine and the output of each chunk. Thread v owns value
 // column v: tensor-memory lane v holds S^T[v][:], u^T[v][:] and O^T[v][:].
 // ---------------------------------------------------------------------------------
-template <bool kOut, bool kTest, bool kBwd>
+template <bool kOut, bool kNorm, bool kTest, bool kBwd>
 __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p, int ctid, int seq) {
   using P = Plan;
   const uint64_t lim = wait_limit<kTest>(p);
@@ -635,8 +676,12 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
           // columns past the end of the sequence are zeroed: their U and W rows came
           // from other tokens' T diag(beta) rows
           const int t = h2 * 32 + 2 * e;
-          split_half2(t < clen ? __uint_as_float(u[2 * e]) : 0.f, t + 1 < clen ? __uint_as_float(u[2 * e + 1]) : 0.f,
-                      hi[e], lo[e]);
+          float u0 = t < clen ? __uint_as_float(u[2 * e]) : 0.f, u1 = t + 1 < clen ? __uint_as_float(u[2 * e + 1]) : 0.f;
+          if constexpr (kNorm && kOut) {  // fused prologue: A and Kd carry the raw keys
+            u0 *= x.s_rk3[(c % 3) * kChunk + t];
+            u1 *= x.s_rk3[(c % 3) * kChunk + t + 1];
+          }
+          split_half2(u0, u1, hi[e], lo[e]);
         }
         tc::tmem_st16u(lanes + P::COL_UT + h2 * 16, hi);
         tc::tmem_st16u(lanes + P::COL_UT + 32 + h2 * 16, lo);
@@ -685,7 +730,8 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
 #pragma unroll
       for (int e = 0; e < 64; ++e) {
         if (e < clen) {
-          const float y = __uint_as_float(o[e]);
+          float y = __uint_as_float(o[e]);
+          if constexpr (kNorm) y *= x.s_rq3[(c % 3) * kChunk + e];  // fused prologue: 1 / |q_t|
           *optr = __float2bfloat16_rn(y);
           chk += y;
         }
@@ -886,6 +932,8 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   __shared__ __align__(16) float s_E[2 * kChunk], s_F[2 * kChunk], s_gstage[2 * kChunk];
   __shared__ __align__(16) float s_bstage[kBwd ? 2 * kChunk : 1], s_bv[kBwd ? 2 * kChunk : 1];
   __shared__ __align__(16) float s_rq[kChunk], s_rk[kChunk];
+  __shared__ __align__(16) float s_qpart[kNorm && kOut ? 4 * kChunk : 1], s_rq3[kNorm && kOut ? 3 * kChunk : 1];
+  __shared__ __align__(16) float s_rk3[kNorm && kOut ? 3 * kChunk : 1];
   __shared__ float s_elast[3];
   __shared__ int s_fast[2];
   __shared__ __align__(8) uint64_t s_mb[kNumMbar];
@@ -940,6 +988,9 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.s_F = s_F;
   x.s_rq = s_rq;
   x.s_rk = s_rk;
+  x.s_qpart = s_qpart;
+  x.s_rq3 = s_rq3;
+  x.s_rk3 = s_rk3;
   x.s_fast = s_fast;
   x.s_gstage = s_gstage;
   x.s_bstage = s_bstage;
@@ -983,7 +1034,7 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   x.tmem = s_tmem;
 
   if (warp < kConsumerWarps)
-    consumer_role<kOut, kTest, kBwd>(x, p, tid, s);
+    consumer_role<kOut, kNorm, kTest, kBwd>(x, p, tid, s);
   else if (warp < kConsumerWarps + kProducerWarps)
     producer_role<kOut, kNorm, kTest, kBwd>(x, p, tid - kConsumerThreads);
   else if ((tid & 31) == 0)
