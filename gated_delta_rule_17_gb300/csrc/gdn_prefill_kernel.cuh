@@ -140,8 +140,12 @@ struct Ctx {
   float *s_E, *s_F;     // e^{gc - m}, e^{m - gc} about the chunk's mid gate m
   float *s_rq, *s_rk;   // fused prologue: 1 / |q_t|, 1 / |k_t| of the current chunk
   float* s_qpart;       // fused prologue with outputs: [4][64] partial sums of q_t^2
-  float* s_rq3;         // ... and 1 / |q_t| by chunk index mod 3 ([3][64]), read at the store
-  float* s_rk3;         // ... and 1 / |k_t| by chunk index mod 3 ([3][64]), read by the u split
+  // ... and 1 / |q_t|, 1 / |k_t| by chunk index mod 3 ([3][64] each), read by the
+  // consumer's store and u split of that chunk. The producer writes chunk c+3's slot after
+  // its wait on c2(c+1) at the top of chunk c+3; spine2(c+1) is issued after the
+  // consumer's usp(c+1), which follows its store and u split of chunk c.
+  float* s_rq3;
+  float* s_rk3;
   int* s_fast;          // [2] 1 when the chunk's gate range allows the factorised decays
   float* s_gstage;      // [2][64] g of a chunk, staged by cp.async
   float *s_bstage, *s_bv;  // backward's forward chain: beta staged, and beta of a gate set
