@@ -12,7 +12,8 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "csrc", "gdn_api.cu")
 DEPS = [os.path.join(HERE, "csrc", f) for f in ("gdn_api.cu", "gdn_common.cuh", "gdn_prefill_kernel.cuh", "gdn_decode_kernel.cuh",
-                                                           "gdn_wy_kernel.cuh", "gdn_bwd_chunk_kernel.cuh", "gdn_bwd_dstates_tc.cuh", "gdn_mma.cuh", "tc.cuh")] + [
+                                                           "gdn_wy_kernel.cuh", "gdn_bwd_common.cuh", "gdn_bwd_dstates_tc.cuh", "gdn_bwd_grads_tc.cuh",
+                                                           "tc.cuh")] + [
     os.path.join(os.path.dirname(HERE), "include", "gdn_prefill.h")]
 OUT_DIR = os.path.join(HERE, "_lib")
 OUT = os.path.join(OUT_DIR, "libgdn_gb300.so")

@@ -21,8 +21,8 @@
 #include "gdn_prefill_kernel.cuh"
 #include "gdn_wy_kernel.cuh"
 #include "gdn_decode_kernel.cuh"
-#include "gdn_bwd_chunk_kernel.cuh"
 #include "gdn_bwd_dstates_tc.cuh"
+#include "gdn_bwd_grads_tc.cuh"
 
 namespace {
 
@@ -99,7 +99,7 @@ int device_info(DeviceInfo** out) {
     if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     const std::pair<const void*, int> bwd[] = {
         {reinterpret_cast<const void*>(gdn::gdn_bwd_dstates_tc_kernel), gdn::DsPlan::DYN_SMEM},
-        {reinterpret_cast<const void*>(gdn::gdn_bwd_grads_kernel), gdn::kGradsSmem}};
+        {reinterpret_cast<const void*>(gdn::gdn_bwd_grads_tc_kernel), gdn::GtPlan::DYN_SMEM}};
     for (const auto& f : bwd) {
       e = cudaFuncSetAttribute(f.first, cudaFuncAttributeMaxDynamicSharedMemorySize, f.second);
       if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -875,7 +875,7 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   fc.ubuf = p.ubuf;
   gdn::gdn_prefill_kernel<false, false, false, true><<<chains, gdn::kThreads, gdn::Plan::DYN_SMEM, s>>>(mq, mk, mv, mt, fc);
   gdn::gdn_bwd_dstates_tc_kernel<<<chains, gdn::kDsThreads, gdn::DsPlan::DYN_SMEM, s>>>(mq, mk, p);
-  gdn::gdn_bwd_grads_kernel<<<static_cast<unsigned>(grad_items), gdn::kBcThreads, gdn::kGradsSmem, s>>>(p);
+  gdn::gdn_bwd_grads_tc_kernel<<<static_cast<unsigned>(grad_items), gdn::kGtThreads, gdn::GtPlan::DYN_SMEM, s>>>(p);
   launches += 4;
   int rc = GDN_OK;
   cudaError_t e = cudaGetLastError();

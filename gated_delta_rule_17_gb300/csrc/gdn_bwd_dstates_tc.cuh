@@ -1,7 +1,7 @@
 // Reverse chain of the chunked backward on the 5th-generation tensor cores.
 //
 // The reverse chain of the chunk-level derivative (derived in the header of
-// gdn_bwd_chunk_kernel.cuh), per chunk c from the last:
+// gdn_bwd_common.cuh), per chunk c from the last:
 //
 //     du  = (Q K^T . M)^T dO / sqrt(dk) + (gamma / Gamma) K dS_end
 //     du' = T^T du,  dV = beta du'
@@ -25,7 +25,7 @@
 // (two buffers, one chunk ahead); dO and T by cp.async one chunk ahead. Every wait is
 // bounded; on expiry the CTA sets the status bit and stops.
 #pragma once
-#include "gdn_bwd_chunk_kernel.cuh"
+#include "gdn_bwd_common.cuh"
 
 namespace gdn {
 
@@ -123,16 +123,16 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
     for (int i = 0; i < 1024 / kDsThreads; ++i) {
       const int idx = tid + kDsThreads * i, row = idx >> 4, c8 = idx & 15;
       const int srow = row < n ? row : 0;
-      mm::cp_async16(tb + (c8 >> 3) * 8192 + tc::sw128(row, (c8 & 7) * 16), tsrc + srow * hrow + 8 * c8, row < n);
+      cp_async16(tb + (c8 >> 3) * 8192 + tc::sw128(row, (c8 & 7) * 16), tsrc + srow * hrow + 8 * c8, row < n);
     }
     const float* dsrc = p.dout + r0 * hrow + h * kDim;
 #pragma unroll
     for (int i = 0; i < 2048 / kDsThreads; ++i) {
       const int idx = tid + kDsThreads * i, row = idx >> 5, c4 = idx & 31;
       const int srow = row < n ? row : 0;
-      mm::cp_async16(sb + P::DOST + row * 512 + c4 * 16, dsrc + srow * hrow + 4 * c4, row < n);
+      cp_async16(sb + P::DOST + row * 512 + c4 * 16, dsrc + srow * hrow + 4 * c4, row < n);
     }
-    mm::cp_async_commit();
+    tc::cp_async_commit();
   };
 
   bool ok = true;
@@ -281,7 +281,7 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
       fetch_gates(nch - 1);
       gates();
     }
-    mm::cp_async_wait_all();
+    tc::cp_async_wait_all();
     __syncthreads();
     convert_do(nch - 1);
     const float* d0 = p.dst ? p.dst + (static_cast<int64_t>(s) * p.nv + h) * kDim * kDim : nullptr;
@@ -432,7 +432,7 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
     // meanwhile, the previous chunk's chain-free work: factors, dO operands (its own scaled
     // buffer; the fp16 dO tile's last reader, this chunk's P1, is done), A~ and P1
     if (c > 0) {
-      mm::cp_async_wait_all();
+      tc::cp_async_wait_all();
       if (warp == 0) gates();
       __syncthreads();
       convert_do(c - 1);
@@ -464,7 +464,7 @@ gdn_bwd_dstates_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gr
 #pragma unroll
     for (int e = 0; e < 32; ++e) d[(part * 32 + e) * kDim] = __uint_as_float(x[e]);
   }
-  mm::cp_async_wait_all();
+  tc::cp_async_wait_all();
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) {
