@@ -545,7 +545,9 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       uint32_t d[32];
       tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + half * 32, d);
       tc::tmem_ld_wait();
-      signal(x.mb_wrd);  // the W columns are read: the next Gram MMA may go
+      tc::fence_before_sync();  // the W columns are read (tensor memory only): the next Gram MMA may go
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(x.mb_wrd);
       if constexpr (!kOut) {
         // The single -W^T tile was last read by the spine MMAs of chunk c - 1; runs with
         // outputs waited for them before converting Q~
