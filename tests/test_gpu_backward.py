@@ -128,6 +128,15 @@ def test_backward_one_head_per_key():
     assert_grads(got, ref, "nk = nv")
 
 
+@pytest.mark.parametrize("group", [4, 8])
+def test_backward_wide_gqa_groups(group):
+    # 4 and 8 value heads per key head: the per-chunk gradient kernel walks the whole group
+    # in one CTA, accumulating dq and dk over it, with a ragged last chunk
+    p = gdn_synth.make_problem(seed=8550 + group, B=2, T=150, nk=2, nv=2 * group, h0_std=0.02)
+    got, ref = run_backward(p, 8550 + group)
+    assert_grads(got, ref, f"{group} value heads per key head")
+
+
 @pytest.mark.parametrize("B", [4, 5])
 def test_backward_many_chains(B):
     # 128 and 160 (sequence, head) chains (more than the SMs: a second wave) of 70 tokens

@@ -203,10 +203,17 @@ def test_ragged_tail_dense(T):
     run_and_check(p, label=f"dense T={T}")
 
 
-def test_wide_batch_uses_full_width_slices():
-    # B*nv above half the SM count selects the 128-column slice per CTA
+def test_wide_batch():
+    # 96 (sequence, head) chains of three sequences, one CTA each
     p = gdn_synth.make_problem(seed=3100, B=3, T=130, nk=16, nv=32, h0_std=0.02)
     run_and_check(p, heads=[0, 17, 31], label="wide batch")
+
+
+@pytest.mark.parametrize("group", [4, 8])
+def test_wide_gqa_groups(group):
+    # 4 and 8 value heads per key head read each key head's q/k tiles
+    p = gdn_synth.make_problem(seed=3450 + group, B=2, T=150, nk=2, nv=2 * group, h0_std=0.02)
+    run_and_check(p, label=f"{group} value heads per key head")
 
 
 def test_varlen_edge_lengths_packed_strides():
