@@ -385,18 +385,38 @@ int wy_geometry(const DeviceInfo& d, int B, int T, int nv, bool varlen, int* ite
 
 // One spine launch: the instantiation for output rows (or not) and the fused q/k norms (or
 // not); the test instantiation when test hooks are set (output rows, no fused norms).
-void launch_spine(bool out_rows, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                  const CUtensorMap& mt, const gdn::ChunkParams& p, int64_t grid, cudaStream_t stream) {
-  const dim3 g(static_cast<unsigned>(grid)), blk(gdn::kThreads);
-  const size_t sm = gdn::Plan::DYN_SMEM;
+// `after_wy`: the launch directly follows the WY kernel in the stream and may start while
+// that kernel still runs (programmatic stream serialisation). Its CTAs then take SMs as
+// the WY kernel's CTAs leave them, set up, load their first tiles and issue their first
+// Gram; every access to the T diag(beta) / output rows waits for the WY grid in the
+// kernel (tc::grid_dependency_wait).
+template <bool kOut, bool kNorm, bool kTest = false>
+cudaError_t launch_spine_as(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const CUtensorMap& mt, const gdn::ChunkParams& p, int64_t grid, bool after_wy,
+                            cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(gdn::kThreads);
+  cfg.dynamicSmemBytes = gdn::Plan::DYN_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_wy ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gdn::gdn_prefill_kernel<kOut, kNorm, kTest>, mq, mk, mv, mt, p);
+}
+
+cudaError_t launch_spine(bool out_rows, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mt, const gdn::ChunkParams& p, int64_t grid, cudaStream_t stream,
+                         bool after_wy = false) {
   if (out_rows) {
-    if (g_hooks.active() && !p.qk_l2norm) gdn::gdn_prefill_kernel<true, false, true><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
-    else if (p.qk_l2norm) gdn::gdn_prefill_kernel<true, true><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
-    else gdn::gdn_prefill_kernel<true, false><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
-  } else {
-    if (p.qk_l2norm) gdn::gdn_prefill_kernel<false, true><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
-    else gdn::gdn_prefill_kernel<false, false><<<g, blk, sm, stream>>>(mq, mk, mv, mt, p);
+    if (g_hooks.active() && !p.qk_l2norm) return launch_spine_as<true, false, true>(mq, mk, mv, mt, p, grid, after_wy, stream);
+    if (p.qk_l2norm) return launch_spine_as<true, true>(mq, mk, mv, mt, p, grid, after_wy, stream);
+    return launch_spine_as<true, false>(mq, mk, mv, mt, p, grid, after_wy, stream);
   }
+  if (p.qk_l2norm) return launch_spine_as<false, true>(mq, mk, mv, mt, p, grid, after_wy, stream);
+  return launch_spine_as<false, false>(mq, mk, mv, mt, p, grid, after_wy, stream);
 }
 
 int launch(const void* q, const void* k, const void* v, const float* g, const float* beta, void* state, void* out,
@@ -496,7 +516,8 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
     ps.seg = a.tab1;
     ps.state = a.ptr1;
     ps.B = sl.n1;
-    launch_spine(false, mq, mk, mv, mt, ps, static_cast<int64_t>(sl.n1) * nv, stream);
+    if (cudaError_t e = launch_spine(false, mq, mk, mv, mt, ps, static_cast<int64_t>(sl.n1) * nv, stream))
+      return fail(GDN_ERR_CUDA, "spine launch: %s", cudaGetErrorString(e));
     ++launches;
     for (int gs = 0; gs <= sp.G - 2; ++gs) {
       gdn_segment_combine_kernel<<<static_cast<unsigned>(B * nv * 4), kCombineThreads, 0, stream>>>(a, gs);
@@ -505,12 +526,21 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
     ps.seg = a.tab2;
     ps.state = a.ptr2;
     ps.B = sl.n2;
-    launch_spine(true, mq, mk, mv, mt, ps, static_cast<int64_t>(sl.n2) * nv, stream);
+    if (cudaError_t e = launch_spine(true, mq, mk, mv, mt, ps, static_cast<int64_t>(sl.n2) * nv, stream))
+      return fail(GDN_ERR_CUDA, "spine launch: %s", cudaGetErrorString(e));
     ++launches;
   } else {
     const int64_t grid = static_cast<int64_t>(B) * nv;
     if (grid > INT32_MAX) return fail(GDN_ERR_UNSUPPORTED, "grid of %lld CTAs too large", (long long)grid);
-    launch_spine(true, mq, mk, mv, mt, p, grid, stream);
+    // Overlapped with the WY kernel's tail unless an event must separate the two, and only
+    // where placement cannot matter. A dependent launch puts the spine's CTAs on the first
+    // SMs the WY kernel frees, and those come in groups: a grid that covers part of the
+    // GPU then lands on fewer, fuller GPCs, whose SMs share the instruction cache behind
+    // their own, and its chain runs slower (measured at T = 8192: 64, 96 and 128 CTAs
+    // lost 22-79 us against a serialised launch; 8, 32, 152 and 160 CTAs gained 3-9 us).
+    const bool dependent = g_timing[1] == nullptr && (grid >= d->sms || grid * 4 <= d->sms);
+    if (cudaError_t e = launch_spine(true, mq, mk, mv, mt, p, grid, stream, dependent))
+      return fail(GDN_ERR_CUDA, "spine launch: %s", cudaGetErrorString(e));
     ++launches;
   }
   if (g_timing[2]) cudaEventRecord(g_timing[2], stream);

@@ -619,6 +619,9 @@ __device__ __forceinline__ void consumer_role(const Ctx& x, const ChunkParams& p
     tc::tmem_st_wait();
   }
   signal(x.mb_strdy);  // S^T of the first chunk is ready
+  // output rows overwrite the WY kernel's T diag(beta) rows: no store before that
+  // kernel has completed (see the issuer)
+  tc::grid_dependency_wait();
 
   // S^T <- e^{gc_last} S^T, the decay half of the state update of chunk `cn` (its fp16
   // copy, which the MMAs read, is separate): two 64-column halves, both loads in flight
@@ -887,7 +890,6 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
   }
   issue_kq(0);
   issue_v(0);
-  issue_t(0);
   if (n > 1) {
     issue_kq(1);
     issue_v(1);
@@ -899,6 +901,13 @@ __device__ __forceinline__ void issuer_role(const Ctx& x, const ChunkParams& p, 
     if constexpr (kOut) {
       if ((c > 0 && !wait(x.mb_wrd, (c - 1) & 1)) || !wait(b ? x.mb_kq1 : x.mb_kq0, (c >> 1) & 1)) break;
       gram(c);
+    }
+    // the T diag(beta) rows are the WY kernel's output: under a dependent launch this
+    // CTA may have started while that kernel still runs, so the first copy of them
+    // waits for its completion (the loads and the Gram above need only the inputs)
+    if (c == 0) {
+      tc::grid_dependency_wait();
+      issue_t(0);
     }
     // U of c: V is fp16, T diag(beta) has landed, and u of c-2 has been read
     if (!wait(x.mb_vrdy, c & 1) || !wait(x.mb_t, c & 1) ||
@@ -962,11 +971,13 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     x.zero_v = (p.seg[4 * s + 2] & kSegZeroValues) != 0;
   } else if (p.cu_seqlens) {
     if (s < 0 || s >= p.B) {
+      tc::grid_dependency_wait();
       if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
       return;
     }
     const int a = p.cu_seqlens[s], e = p.cu_seqlens[s + 1];
     if (a < 0 || e < a || e > p.T) {
+      tc::grid_dependency_wait();
       if (tid == 0) atomicOr(p.status, kStatusBadSeqlens);
       return;
     }
@@ -977,7 +988,10 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     x.len = p.T;
   }
   x.nchunks = static_cast<int>((x.len + kChunk - 1) / kChunk);
-  if (x.nchunks == 0) return;  // empty sequence: the state passes through unchanged
+  if (x.nchunks == 0) {  // empty sequence: the state passes through unchanged
+    tc::grid_dependency_wait();
+    return;
+  }
   float* state = p.state_is_table ? reinterpret_cast<float* const*>(p.state)[s]
                                   : reinterpret_cast<float*>(p.state) + static_cast<int64_t>(s) * p.nv * kDim * kDim;
   x.state = state + static_cast<int64_t>(x.h) * kDim * kDim;

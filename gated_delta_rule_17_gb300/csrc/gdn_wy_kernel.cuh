@@ -127,6 +127,9 @@ gdn_wy_kernel(const __grid_constant__ CUtensorMap tmap_k, const WyParams p) {
   __shared__ __align__(8) uint64_t s_mb[3];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the spine may be placed on SMs as they fall idle: it waits for this grid's
+  // completion before it touches the T diag(beta) rows
+  tc::allow_dependent_launch();
 
   int items = p.items;
   if (p.cu_seqlens) {

@@ -220,6 +220,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch. A grid launched with programmatic stream
+// serialisation may start while the kernel before it in the stream still runs;
+// grid_dependency_wait() returns once that kernel has completed and its memory
+// writes are visible (at once for a grid launched without the attribute).
+// allow_dependent_launch() lets the next such grid start before this one ends.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Wait for the phase with the given parity to complete, giving up after
 // `limit_ns` nanoseconds of wall time so that a lost arrival can never hang
 // the GPU. Returns false on expiry.

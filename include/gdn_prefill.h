@@ -188,7 +188,13 @@ int gdn_decode(const void* q, const void* k, const void* v, const float* g, cons
  * its stream before the WY-solve kernel, between the two kernels and after
  * the spine kernel, so each kernel's device time can be read with
  * cudaEventElapsedTime. Any NULL leaves that point unrecorded; all NULL
- * switches the hook off. The events must outlive the calls that record them. */
+ * switches the hook off. The events must outlive the calls that record them.
+ * Without the between-kernels event, the spine kernel of a call that has no
+ * segment schedule, and whose grid covers every SM or at most a quarter of
+ * them, is launched with programmatic stream serialisation: it may start on
+ * SMs the WY kernel has left and overlap that kernel's tail (its reads of the
+ * WY output wait for the WY grid to complete). With that event set, the two
+ * kernels run one after the other. */
 void gdn_set_timing_events(void* before_wy, void* before_spine, void* after_spine);
 
 /* Backward of the prefill (the training pass): gradients of a loss L with

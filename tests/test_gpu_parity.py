@@ -68,6 +68,39 @@ def test_config4_long_context_all_heads():
     assert_parity(dp.out_np(), dp.state_np(), o_ref, s_ref, label="config 4 serial")
 
 
+@pytest.mark.parametrize("B,T,nk,nv", [
+    (2, 1000, 2, 4),  # 8 chains: at most a quarter of the SMs
+    (38, 300, 2, 4),  # 152 chains: every SM of a GB300
+])
+def test_dependent_spine_launch_bitwise(B, T, nk, nv):
+    # grids that cover every SM or at most a quarter of them start the spine under a
+    # dependent launch, overlapping the WY kernel's tail; an event between the kernels
+    # serialises them. Both give the same bits, and the oracle's result.
+    import gated_delta_rule_17_gb300 as gdn
+
+    p = gdn_synth.make_problem(seed=3800 + B, B=B, T=T, nk=nk, nv=nv, h0_std=0.02)
+    empty = torch.empty(0, dtype=torch.uint8, device="cuda")  # the direct schedule, no segments
+    dp = DeviceProblem(p)
+    dp.run(workspace=empty)
+    torch.cuda.synchronize()
+    gdn.check()
+    assert gdn.last_launch_count() == 2
+    ser = DeviceProblem(p)
+    mid = torch.cuda.Event(enable_timing=True)
+    mid.record()
+    gdn.set_timing_events(None, mid, None)
+    try:
+        ser.run(workspace=empty)
+        torch.cuda.synchronize()
+    finally:
+        gdn.set_timing_events()
+    gdn.check()
+    np.testing.assert_array_equal(dp.out_np(), ser.out_np())
+    np.testing.assert_array_equal(dp.state_np(), ser.state_np())
+    o_ref, s_ref = oracle.token_loop(p)
+    assert_parity(dp.out_np(), dp.state_np(), o_ref, s_ref, label=f"dependent launch, {B * nv} chains")
+
+
 def test_hand_off_repeated_calls_bitwise():
     # Ten calls of the benchmarked launch back to back, each from the same carried-in
     # state: every call ends clean and writes the same bits (the spine's hand-off and
