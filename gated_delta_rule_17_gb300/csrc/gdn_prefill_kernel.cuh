@@ -309,6 +309,7 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
     // ---- the Gram MMA of this chunk is issued by the issuer once its tile lands ------
     // this chunk's Kd and A buffers were last read by the spine of chunk c-2
     ok = true;
+    float rk_own = 1.f;  // fused prologue with outputs: 1 / |k_t| of row t = ptid % 64
     if (c >= 2) ok = (*x.s_abort == 0) && tc::mbar_wait_timed(b ? x.mb_c21 : x.mb_c20, ((c - 2) >> 1) & 1, lim);
 
     if (quad < 2) {
@@ -336,26 +337,29 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
       signal(x.mb_vrdy);  // V is fp16: the U MMAs may go
       if constexpr (kNorm && kOut) {
         // fused prologue: |k_t|^2 is the diagonal of the Gram's K K^T half (tensor-memory
-        // lanes 0-63), read by the first warp of lane quarters 0 and 1. Only e^gc K (the
-        // W operand) takes 1 / |k_t| here; A and Kd are formed from the raw keys, and the
-        // consumer scales column t of u by 1 / |k_t| instead (S^T += u^T Kd and
+        // lanes 0-63). Every warp of lane quarters 0 and 1 reads the 32 rows t = quad * 32 +
+        // lane, which are the rows its threads convert below (t = ptid % 64), and keeps
+        // 1 / |k_t| in a register; the first warp of each quarter also publishes it for
+        // lane quarters 2-3 and the consumer, then all arrive without waiting. Only e^gc K
+        // (the W operand) takes 1 / |k_t| here; A and Kd are formed from the raw keys, and
+        // the consumer scales column t of u by 1 / |k_t| instead (S^T += u^T Kd and
         // O^T += u^T A^T each have exactly one factor indexed by t)
         ok = ok && (*x.s_abort == 0) && tc::mbar_wait_timed(x.mb_g, b, lim);
         tc::fence_after_sync();
-        if (half == 0 && ok) {
+        if (ok) {
           uint32_t d[32];
           tc::tmem_ld32(x.tmem + ((quad * 32u) << 16) + P::COL_GW + quad * 32, d);
           tc::tmem_ld_wait();
           float ss = 0.f;
 #pragma unroll
           for (int e = 0; e < 32; ++e) ss = (e == lane) ? __uint_as_float(d[e]) : ss;
-          const int t = quad * 32 + lane;
-          const float r = 1.f / sqrtf(ss + kL2Eps);
-          x.s_rk3[(c % 3) * kChunk + t] = r;
-          x.s_eg[gs + t] *= r;
+          rk_own = 1.f / sqrtf(ss + kL2Eps);
+          if (half == 0) x.s_rk3[(c % 3) * kChunk + quad * 32 + lane] = rk_own;
         }
+        tc::named_barrier_arrive(kBarNorm, kProducerThreads);
+      } else if constexpr (kNorm) {
+        tc::named_barrier(kBarNorm, kProducerThreads);
       }
-      if constexpr (kNorm) tc::named_barrier(kBarNorm, kProducerThreads);
     } else {
       if constexpr (kBwd) {
         // lane quarters 2-3 (no A epilogue without outputs): T -> T diag(beta) in place
@@ -450,7 +454,10 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
           *reinterpret_cast<uint4*>(sm + a_off + 8192 + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
-      if constexpr (kNorm && kOut) tc::named_barrier(kBarNorm, kProducerThreads);
+      if constexpr (kNorm && kOut) {
+        tc::named_barrier(kBarNorm, kProducerThreads);  // lane quarters 0-1 have published 1 / |k_t|
+        rk_own = x.s_rk3[(c % 3) * kChunk + (ptid & 63)];
+      }
     }
 
     // ---- once the Gram MMA has read K: K -> e^gc K (fp16, in place, rows t) and --------
@@ -476,8 +483,9 @@ __device__ __forceinline__ void producer_role(const Ctx& x, const ChunkParams& p
         const bool live = t < clen;
         float f[8];
         unpack_bf16x8(rk[r], f);
+        // (with the fused prologue t = ptid % 64, the row whose 1 / |k_t| this thread holds)
         *reinterpret_cast<uint4*>(sm + kq_off + (cc >> 3) * 16384 + tc::sw128(t, (cc & 7) * 16)) =
-            live ? pack_half8(f, x.s_eg[gs + t]) : make_uint4(0, 0, 0, 0);
+            live ? pack_half8(f, kNorm && kOut ? x.s_eg[gs + t] * rk_own : x.s_eg[gs + t]) : make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4*>(sm + kd_off + (cc >> 3) * 8192 + tc::sw128(t, (cc & 7) * 16)) =
             live ? pack_half8(f, x.s_edec[gs + t]) : make_uint4(0, 0, 0, 0);
       }

@@ -266,6 +266,13 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive on hardware barrier `id` without waiting: the threads that bar.sync on it
+// (nthreads counts both sides) are released once all have arrived, and see this
+// thread's earlier shared-memory writes.
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Barrier among `nthreads` threads on hardware barrier `id` that also returns
 // the AND of every participant's `ok`, so a group takes one uniform decision.
 __device__ __forceinline__ bool barrier_all(uint32_t id, uint32_t nthreads, bool ok) {
