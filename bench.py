@@ -310,29 +310,29 @@ def run_gpu(args, world, rank, local):
     op_gbs = abytes / (op_ms / 1e3) / 1e9
     roofline_ms = max(aflops / (tf_peak * 1e12), abytes / (hbm_peak * 1e9)) * 1e3
 
-    # ---- end to end through the public API with host buffers ----------------------
+    # ---- end to end through the C ABI's host-buffer entry point (gdn_prefill_host):
+    # page-locked host inputs and state, copied in, the op, the output rows and the
+    # state copied back, every step; the state is carried on the host in place ------------
     host = {}
     for name in ("q", "k", "v", "g", "beta"):
         t = getattr(dp, name)
         host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
-    h_state = torch.empty(dp.state.shape, dtype=dp.state.dtype, pin_memory=True).copy_(dp.state)
+    h_state = torch.from_numpy(p.h0.copy()).pin_memory()  # contiguous [B, nv, dk, dv]
     h_out = torch.empty(dp.out.shape, dtype=dp.out.dtype, pin_memory=True)
-    h_state_out = torch.empty_like(h_state)
+    h_cu = None if dp.cu is None else dp.cu.cpu().pin_memory()
     h2d = sum(host[n].numel() * host[n].element_size() for n in host) + h_state.numel() * 4
-    d2h = h_out.numel() * h_out.element_size() + h_state_out.numel() * 4
+    d2h = h_out.numel() * h_out.element_size() + h_state.numel() * 4
     e2e_steps = max(3, min(args.steps, 10))
+    h_scratch = torch.empty(gdn.host_scratch_bytes(p.B, p.T, p.nk, p.nv, p.varlen), dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        for n in host:
-            getattr(dp, n).copy_(host[n], non_blocking=True)
-        dp.state.copy_(h_state, non_blocking=True)
-        gdn.prefill(dp.q, dp.k, dp.v, dp.g, dp.beta, dp.state, dp.out, nk=p.nk, nv=p.nv, B=p.B, T=p.T,
-                    cu_seqlens=dp.cu, state_is_table=dp.table, workspace=ws, qk_l2norm=dp.qk_l2norm)
-        h_out.copy_(dp.out, non_blocking=True)
-        h_state_out.copy_(dp.state, non_blocking=True)
+        gdn.prefill_host(host["q"], host["k"], host["v"], host["g"], host["beta"], h_state, h_out, nk=p.nk,
+                         nv=p.nv, B=p.B, T=p.T, cu_seqlens=h_cu, scratch=h_scratch, qk_l2norm=dp.qk_l2norm)
 
     e2e_step()
+    e2e_launches = gdn.last_launch_count()
     torch.cuda.synchronize()
+    gdn.check()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -369,7 +369,8 @@ def run_gpu(args, world, rank, local):
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)"},
         "cpu_baseline": cpu,
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "entry_point": "gdn_prefill_host",
+                "kernels_per_step": e2e_launches},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }

@@ -11,7 +11,7 @@ import ctypes
 import os
 import threading
 
-__all__ = ["prefill", "prefill_noalloc", "NOALLOC_MAX_SEQS", "workspace_bytes", "check", "last_launch_count",
+__all__ = ["prefill", "prefill_noalloc", "prefill_host", "host_scratch_bytes", "NOALLOC_MAX_SEQS", "workspace_bytes", "check", "last_launch_count",
            "backward", "backward_workspace_bytes",
            "set_timing_events", "set_test_hooks", "decode", "lib_path", "load", "GdnError",
            "Strides", "GDN_OK", "GDN_ERR_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_CUDA",
@@ -68,6 +68,10 @@ def load():
             lib.gdn_last_launch_count.restype = i
             lib.gdn_prefill_noalloc.argtypes = common + [vp]
             lib.gdn_prefill_noalloc.restype = i
+            lib.gdn_prefill_host.argtypes = common + [vp, sz, vp]
+            lib.gdn_prefill_host.restype = i
+            lib.gdn_prefill_host_scratch_bytes.argtypes = [i, i, i, i, i, i, i]
+            lib.gdn_prefill_host_scratch_bytes.restype = sz
             lib.gdn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(Strides), vp]
             lib.gdn_decode.restype = i
             lib.gdn_prefill_backward_workspace_bytes.argtypes = [i, i, i, i, i, i]
@@ -213,6 +217,54 @@ def prefill_noalloc(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | 
     rc = lib.gdn_prefill_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(),
                                  state.data_ptr(), out.data_ptr(), B, T, nk, nv, dk, dv, ctypes.byref(st),
                                  None if cu_seqlens is None else cu_seqlens.data_ptr(), stream)
+    if rc != GDN_OK:
+        _raise(rc)
+
+
+def host_scratch_bytes(B, T, nk, nv, varlen, dk=128, dv=128) -> int:
+    """Device scratch of ``prefill_host`` (``gdn_prefill_host_scratch_bytes``)."""
+    return int(load().gdn_prefill_host_scratch_bytes(B, T, nk, nv, dk, dv, 1 if varlen else 0))
+
+
+def prefill_host(q, k, v, g, beta, state, out, *, nk: int, nv: int, B: int | None = None, T: int | None = None,
+                 cu_seqlens=None, scratch=None, stream=None, dk: int = 128, dv: int = 128,
+                 qk_l2norm: bool = False) -> None:
+    """``gdn_prefill_host``: the prefill over page-locked host tensors (``pin_memory()``),
+    packed as for ``prefill`` (q, k [rows, nk*dk] bf16; v, out [rows, nv*dv] bf16; g, beta
+    [rows, nv] fp32; state [B, nv, dk, dv] fp32, updated in place; cu_seqlens int32 [B+1]).
+    Enqueued on ``stream`` (default: torch's current CUDA stream); the host tensors must
+    stay untouched until that stream passes the call. ``scratch``: optional uint8 CUDA
+    tensor of ``host_scratch_bytes(...)`` bytes (else allocated stream-ordered)."""
+    import torch
+
+    lib = load()
+    named = [("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16), ("g", g, torch.float32),
+             ("beta", beta, torch.float32), ("state", state, torch.float32), ("out", out, torch.bfloat16)]
+    if cu_seqlens is not None:
+        named.append(("cu_seqlens", cu_seqlens, torch.int32))
+    for name, t, dt in named:
+        if t.device.type != "cpu" or not t.is_pinned():
+            raise GdnError(GDN_ERR_ARG, f"{name} must be a page-locked CPU tensor (pin_memory())")
+        if t.dtype != dt or not t.is_contiguous():
+            raise GdnError(GDN_ERR_ARG, f"{name} must be a contiguous {dt} tensor")
+    if scratch is not None and (not scratch.is_cuda or scratch.dtype != torch.uint8):
+        raise GdnError(GDN_ERR_ARG, "scratch must be a uint8 CUDA tensor")
+    rows = q.shape[0]
+    if cu_seqlens is not None:
+        B = cu_seqlens.numel() - 1
+        T = rows
+    elif B is None or T is None:
+        raise GdnError(GDN_ERR_ARG, "dense batches need B and T")
+    st = Strides(nk * dk, nk * dk, nv * dv, nv, nv, nv * dv, 0, 1 if qk_l2norm else 0)
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = lib.gdn_prefill_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(),
+                              state.data_ptr(), out.data_ptr(), B, T, nk, nv, dk, dv, ctypes.byref(st),
+                              None if cu_seqlens is None else cu_seqlens.data_ptr(),
+                              None if scratch is None or not scratch.numel() else scratch.data_ptr(),
+                              0 if scratch is None else scratch.numel(), stream)
     if rc != GDN_OK:
         _raise(rc)
 

@@ -68,6 +68,7 @@ struct DeviceInfo {
   bool ok = false;
   bool attrs = false;
   unsigned* status = nullptr;
+  cudaStream_t copy_in = nullptr, copy_out = nullptr;  // gdn_prefill_host's copy streams
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -421,7 +422,7 @@ cudaError_t launch_spine(bool out_rows, const CUtensorMap& mq, const CUtensorMap
 
 int launch(const void* q, const void* k, const void* v, const float* g, const float* beta, void* state, void* out,
            int B, int T, int nk, int nv, const Resolved& r, const int32_t* cu, int32_t* sched, cudaStream_t stream,
-           void* seg_ws = nullptr, size_t seg_ws_bytes = 0) {
+           void* seg_ws = nullptr, size_t seg_ws_bytes = 0, int c_begin = 0, int c_count = 0) {
   DeviceInfo* d = nullptr;
   if (int rc = device_info(&d)) return rc;
   const int64_t rows = cu ? static_cast<int64_t>(T) : static_cast<int64_t>(B) * T;
@@ -450,10 +451,18 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   w.nk = nk;
   w.nv = nv;
   w.chunks_per_seq = (T + gdn::kChunk - 1) / gdn::kChunk;
+  w.chunk_begin = 0;
   w.qk_l2norm = r.l2norm;
   w.t_only = 0;
   int64_t wy_grid = 0;
   if (int rc = wy_geometry(*d, B, T, nv, cu != nullptr, &w.items, &wy_grid)) return rc;
+  if (c_count > 0 && !cu) {  // dense: only the chunk range [c_begin, c_begin + c_count) of every sequence
+    w.chunk_begin = c_begin;
+    w.chunks_per_seq = c_count;
+    w.items = static_cast<int>(static_cast<int64_t>(B) * c_count * nv);
+    const int64_t slots = static_cast<int64_t>(d->sms) * gdn::kWyCtasPerSm;
+    wy_grid = w.items < slots ? w.items : slots;
+  }
 
   gdn::ChunkParams p;
   p.g = g;
@@ -471,6 +480,8 @@ int launch(const void* q, const void* k, const void* v, const float* g, const fl
   p.state_is_table = r.table;
   p.qk_l2norm = r.l2norm;
   p.seg = nullptr;
+  p.chunk_begin = c_count > 0 && !cu ? c_begin : 0;
+  p.chunk_count = c_count > 0 && !cu ? c_count : 0;
   p.test_wait_ns = g_hooks.wait_ns > 0 ? g_hooks.wait_ns : static_cast<int64_t>(gdn::kWaitLimitNs);
   p.test_delay_ns = g_hooks.delay_ns;
   p.test_skip_chunk = g_hooks.skip_chunk;
@@ -611,6 +622,79 @@ BwdLayout bwd_layout(int B, int T, int nv, int varlen) {
   return l;
 }
 
+// ---- end-to-end entry point from page-locked host memory (gdn_prefill_host) ---------
+
+// Device staging: packed copies of q, k, v, g, beta, the state and the output rows,
+// cu_seqlens, then the op's own workspace; 256-byte aligned parts.
+struct HostLayout {
+  size_t q = 0, k = 0, v = 0, g = 0, beta = 0, state = 0, out = 0, cu = 0, ws = 0, ws_bytes = 0, total = 0;
+};
+
+HostLayout host_layout(int B, int T, int nk, int nv, bool varlen) {
+  HostLayout l;
+  const size_t rows = varlen ? static_cast<size_t>(T) : static_cast<size_t>(B) * T;
+  const size_t qk = rows * nk * gdn::kDim * 2, vo = rows * nv * gdn::kDim * 2, gb = rows * nv * sizeof(float);
+  l.k = align256(l.q + qk);
+  l.v = align256(l.k + qk);
+  l.g = align256(l.v + vo);
+  l.beta = align256(l.g + gb);
+  l.state = align256(l.beta + gb);
+  l.out = align256(l.state + static_cast<size_t>(B) * nv * kStateFloats * sizeof(float));
+  l.cu = align256(l.out + vo);
+  l.ws = align256(l.cu + (varlen ? (static_cast<size_t>(B) + 1) * sizeof(int32_t) : 0));
+  l.ws_bytes = workspace_bytes(B, T, nv, varlen);
+  l.total = align256(l.ws + l.ws_bytes);
+  return l;
+}
+
+int check_pinned(const void* p, const char* name) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(GDN_ERR_ARG, "%s: cudaPointerGetAttributes: %s", name, cudaGetErrorString(e));
+  }
+  if (a.type != cudaMemoryTypeHost)
+    return fail(GDN_ERR_ARG, "%s must be page-locked host memory (cudaHostAlloc or cudaHostRegister)", name);
+  return GDN_OK;
+}
+
+int copy_streams(DeviceInfo* d) {
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  for (cudaStream_t* s : {&d->copy_in, &d->copy_out}) {
+    if (*s) continue;
+    cudaError_t e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaStreamCreateWithFlags: %s", cudaGetErrorString(e));
+  }
+  return GDN_OK;
+}
+
+// Rows [r0, r1) of every sequence of a dense [B][T][row_bytes] tensor, in one strided
+// copy (one block of rows per sequence; per sequence when the pitch is too wide).
+cudaError_t copy_rows(void* dst, const void* src, size_t row_bytes, int B, int T, int r0, int r1, cudaMemcpyKind kind,
+                      cudaStream_t s) {
+  const size_t pitch = static_cast<size_t>(T) * row_bytes, off = static_cast<size_t>(r0) * row_bytes;
+  const size_t width = static_cast<size_t>(r1 - r0) * row_bytes;
+  if (pitch < (static_cast<size_t>(1) << 31))
+    return cudaMemcpy2DAsync(static_cast<char*>(dst) + off, pitch, static_cast<const char*>(src) + off, pitch, width,
+                             static_cast<size_t>(B), kind, s);
+  for (int b = 0; b < B; ++b)
+    if (cudaError_t e = cudaMemcpyAsync(static_cast<char*>(dst) + b * pitch + off,
+                                        static_cast<const char*>(src) + b * pitch + off, width, kind, s))
+      return e;
+  return cudaSuccess;
+}
+
+// Chunk ranges of the pipelined path: a dense batch of at least 32 chunks per sequence
+// that does not take the segment schedule is cut into 2-16 ranges of >= 8 chunks, so
+// each range's copies in overlap the op and the copies out of the ranges before it.
+int host_ranges(int B, int T, int nv, int sms) {
+  const int nchunks = static_cast<int>((static_cast<int64_t>(T) + gdn::kChunk - 1) / gdn::kChunk);
+  if (nchunks < 32 || seg_plan(B, T, nv, sms).G >= 2) return 1;
+  const int n = nchunks / 8;
+  return n < 2 ? 2 : (n > 16 ? 16 : n);
+}
+
 }  // namespace
 
 extern "C" {
@@ -686,6 +770,135 @@ int gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float
   }
   return launch(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, r, cu_seqlens, order,
                 static_cast<cudaStream_t>(stream));
+}
+
+size_t gdn_prefill_host_scratch_bytes(int B, int T, int nk, int nv, int dk, int dv, int varlen) {
+  if (B < 0 || T < 0 || nk <= 0 || nv <= 0 || dk != gdn::kDim || dv != gdn::kDim) return 0;
+  return host_layout(B, T, nk, nv, varlen != 0).total;
+}
+
+int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                     void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
+                     const gdn_strides_t* strides, const int32_t* cu_seqlens, void* scratch, size_t scratch_bytes,
+                     void* stream) {
+  g_err[0] = 0;
+  g_launches = 0;
+  Resolved r;
+  if (int rc = validate(q, k, v, g, beta, h_state_inout, out, B, T, nk, nv, dk, dv, strides, &r)) return rc;
+  if (r.table) return fail(GDN_ERR_UNSUPPORTED, "gdn_prefill_host takes a contiguous state (state_is_table = 0)");
+  if (r.q != static_cast<int64_t>(nk) * dk || r.k != static_cast<int64_t>(nk) * dk || r.v != static_cast<int64_t>(nv) * dv ||
+      r.out != static_cast<int64_t>(nv) * dv || r.g != nv || r.beta != nv)
+    return fail(GDN_ERR_UNSUPPORTED, "gdn_prefill_host takes packed rows (q, k: nk*dk; v, out: nv*dv; g, beta: nv)");
+  if (B == 0 || T == 0) return GDN_OK;
+  if (scratch && (reinterpret_cast<uintptr_t>(scratch) & 255u)) return fail(GDN_ERR_ARG, "scratch must be 256-byte aligned");
+  const bool varlen = cu_seqlens != nullptr;
+  const HostLayout l = host_layout(B, T, nk, nv, varlen);
+  if (scratch && scratch_bytes < l.total)
+    return fail(GDN_ERR_ARG, "scratch of %zu bytes is smaller than the %zu required", scratch_bytes, l.total);
+  const std::pair<const void*, const char*> host[] = {{q, "q"}, {k, "k"}, {v, "v"}, {g, "g"}, {beta, "beta"},
+                                                      {h_state_inout, "h_state_inout"}, {out, "out"},
+                                                      {cu_seqlens ? cu_seqlens : q, "cu_seqlens"}};
+  for (const auto& h : host)
+    if (int rc = check_pinned(h.first, h.second)) return rc;
+  DeviceInfo* d = nullptr;
+  if (int rc = device_info(&d)) return rc;
+  if (int rc = copy_streams(d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(scratch);
+  if (!base) {
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&base), l.total, s);
+    if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "cudaMallocAsync(%zu): %s", l.total, cudaGetErrorString(e));
+  }
+  void *dq = base + l.q, *dkk = base + l.k, *dvv = base + l.v, *dstate = base + l.state, *dout = base + l.out;
+  float *dg = reinterpret_cast<float*>(base + l.g), *dbeta = reinterpret_cast<float*>(base + l.beta);
+  int32_t* dcu = varlen ? reinterpret_cast<int32_t*>(base + l.cu) : nullptr;
+  void* dws = l.ws_bytes ? base + l.ws : nullptr;
+  Resolved packed = r;  // the staging rows are packed like the host rows
+  const size_t rows = varlen ? static_cast<size_t>(T) : static_cast<size_t>(B) * T;
+  const size_t bq = rows * nk * dk * 2, bv = rows * nv * dv * 2, bg = rows * nv * sizeof(float);
+  const size_t bs = static_cast<size_t>(B) * nv * kStateFloats * sizeof(float);
+  const int nr = varlen ? 1 : host_ranges(B, T, nv, d->sms);
+  int rc = GDN_OK, launches = 0;
+  cudaError_t e = cudaSuccess;
+  auto h2d = [&](void* dst, const void* src, size_t n, cudaStream_t st) {
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, n, cudaMemcpyHostToDevice, st);
+  };
+  if (nr == 1) {
+    // one pass: everything in, the op, everything out, in stream order
+    h2d(dq, q, bq, s);
+    h2d(dkk, k, bq, s);
+    h2d(dvv, v, bv, s);
+    h2d(dg, g, bg, s);
+    h2d(dbeta, beta, bg, s);
+    h2d(dstate, h_state_inout, bs, s);
+    if (varlen) h2d(dcu, cu_seqlens, (static_cast<size_t>(B) + 1) * sizeof(int32_t), s);
+    if (e != cudaSuccess) rc = fail(GDN_ERR_CUDA, "host to device copy: %s", cudaGetErrorString(e));
+    if (rc == GDN_OK) {
+      rc = varlen ? launch(dq, dkk, dvv, dg, dbeta, dstate, dout, B, T, nk, nv, packed, dcu, static_cast<int32_t*>(dws), s)
+                  : launch(dq, dkk, dvv, dg, dbeta, dstate, dout, B, T, nk, nv, packed, nullptr, nullptr, s, dws, l.ws_bytes);
+      launches = g_launches;
+    }
+    if (rc == GDN_OK) {
+      e = cudaMemcpyAsync(out, dout, bv, cudaMemcpyDeviceToHost, s);
+      if (e == cudaSuccess) e = cudaMemcpyAsync(h_state_inout, dstate, bs, cudaMemcpyDeviceToHost, s);
+      if (e != cudaSuccess) rc = fail(GDN_ERR_CUDA, "device to host copy: %s", cudaGetErrorString(e));
+    }
+  } else {
+    // pipelined: range i's rows are copied in on copy_in, its WY solve and spine run on
+    // `stream` once they have landed, and its output rows go back on copy_out once the
+    // spine is done, while the next range's rows are already coming in. Events order
+    // the three streams; no kernel waits for another.
+    const int nchunks = static_cast<int>((static_cast<int64_t>(T) + gdn::kChunk - 1) / gdn::kChunk);
+    cudaEvent_t ev[2 * 16 + 3] = {};
+    const int nev = 2 * nr + 3;  // start, (in, op) per range, end of copy_in, end of copy_out
+    for (int i = 0; i < nev && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[0], s);  // the staging is ours from here
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->copy_in, ev[0], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(d->copy_out, ev[0], 0);
+    h2d(dstate, h_state_inout, bs, d->copy_in);
+    for (int i = 0; i < nr && e == cudaSuccess && rc == GDN_OK; ++i) {
+      const int c0 = static_cast<int>(static_cast<int64_t>(nchunks) * i / nr);
+      const int c1 = static_cast<int>(static_cast<int64_t>(nchunks) * (i + 1) / nr);
+      const int r0 = c0 * gdn::kChunk, r1 = c1 * gdn::kChunk < T ? c1 * gdn::kChunk : T;
+      const std::pair<std::pair<void*, const void*>, size_t> parts[] = {
+          {{dq, q}, static_cast<size_t>(nk) * dk * 2}, {{dkk, k}, static_cast<size_t>(nk) * dk * 2},
+          {{dvv, v}, static_cast<size_t>(nv) * dv * 2}, {{dg, g}, nv * sizeof(float)},
+          {{dbeta, beta}, nv * sizeof(float)}};
+      for (const auto& pt : parts)
+        if (e == cudaSuccess)
+          e = copy_rows(pt.first.first, pt.first.second, pt.second, B, T, r0, r1, cudaMemcpyHostToDevice, d->copy_in);
+      if (e == cudaSuccess) e = cudaEventRecord(ev[1 + 2 * i], d->copy_in);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev[1 + 2 * i], 0);
+      if (e != cudaSuccess) break;
+      rc = launch(dq, dkk, dvv, dg, dbeta, dstate, dout, B, T, nk, nv, packed, nullptr, nullptr, s, nullptr, 0, c0,
+                  c1 - c0);
+      launches += g_launches;
+      if (rc != GDN_OK) break;
+      e = cudaEventRecord(ev[2 + 2 * i], s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(d->copy_out, ev[2 + 2 * i], 0);
+      if (e == cudaSuccess)
+        e = copy_rows(out, dout, static_cast<size_t>(nv) * dv * 2, B, T, r0, r1, cudaMemcpyDeviceToHost, d->copy_out);
+    }
+    if (e == cudaSuccess && rc == GDN_OK) e = cudaMemcpyAsync(h_state_inout, dstate, bs, cudaMemcpyDeviceToHost, d->copy_out);
+    // the call ends on `stream` once both copy streams have (also after an error, so that
+    // nothing uses the staging once `stream` passes the call)
+    for (int j = 0; j < 2; ++j) {
+      cudaEvent_t end = ev[nev - 2 + j];
+      if (!end) continue;
+      cudaError_t je = cudaEventRecord(end, j == 0 ? d->copy_in : d->copy_out);
+      if (je == cudaSuccess) je = cudaStreamWaitEvent(s, end, 0);
+      if (je != cudaSuccess && e == cudaSuccess) e = je;
+    }
+    for (int i = 0; i < nev; ++i)
+      if (ev[i]) cudaEventDestroy(ev[i]);  // released once the work that records it completes
+    if (e != cudaSuccess && rc == GDN_OK) rc = fail(GDN_ERR_CUDA, "pipelined copies: %s", cudaGetErrorString(e));
+  }
+  if (!scratch) {
+    cudaError_t fe = cudaFreeAsync(base, s);
+    if (fe != cudaSuccess && rc == GDN_OK) rc = fail(GDN_ERR_CUDA, "cudaFreeAsync: %s", cudaGetErrorString(fe));
+  }
+  if (rc == GDN_OK) g_launches = launches;
+  return rc;
 }
 
 int gdn_prefill_check(void* stream) {
@@ -834,6 +1047,7 @@ int gdn_prefill_backward(const void* q, const void* k, const void* v, const floa
   w.nk = nk;
   w.nv = nv;
   w.chunks_per_seq = (T + gdn::kChunk - 1) / gdn::kChunk;
+  w.chunk_begin = 0;
   w.qk_l2norm = 0;
   w.t_only = 1;
 

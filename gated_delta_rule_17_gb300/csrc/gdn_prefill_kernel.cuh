@@ -78,6 +78,11 @@ struct ChunkParams {
   // skips the output rows (the range's T diag(beta) rows stay in place for a later run),
   // bit 1 runs it with v = 0 (the state map's linear part).
   const int32_t* seg;
+  // Dense batches without a segment table: the chunk range [chunk_begin, chunk_begin +
+  // chunk_count) of every sequence (chunk_count 0: to the sequence's end). The state is
+  // read at the range's start and written at its end, so consecutive ranges run one
+  // after the other carry it in place.
+  int chunk_begin, chunk_count;
   // Test hooks, read only by the test instantiation (kTest = true): a wait limit in
   // nanoseconds in place of kWaitLimitNs, a consumer delay in nanoseconds before the
   // hand-off wait of every odd chunk (so the producer runs ahead), and a chunk whose
@@ -992,8 +997,11 @@ gdn_prefill_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     x.row0 = a;
     x.len = e - a;
   } else {
-    x.row0 = static_cast<int64_t>(s) * p.T;
-    x.len = p.T;
+    const int64_t skip = static_cast<int64_t>(p.chunk_begin) * kChunk < p.T ? static_cast<int64_t>(p.chunk_begin) * kChunk : p.T;
+    x.row0 = static_cast<int64_t>(s) * p.T + skip;
+    x.len = p.T - skip;
+    if (p.chunk_count > 0 && x.len > static_cast<int64_t>(p.chunk_count) * kChunk)
+      x.len = static_cast<int64_t>(p.chunk_count) * kChunk;
   }
   x.nchunks = static_cast<int>((x.len + kChunk - 1) / kChunk);
   if (x.nchunks == 0) {  // empty sequence: the state passes through unchanged

@@ -51,7 +51,8 @@ struct WyParams {
   int64_t g_stride, beta_stride, out_stride;
   int items;                  // dense: chunks * nv; varlen: an upper bound on it (< 2^31)
   int B, T, nk, nv;
-  int chunks_per_seq;         // dense batches: ceil(T / 64)
+  int chunks_per_seq;         // dense batches: chunks of every sequence that the items cover
+  int chunk_begin;            // dense batches: the first of them
   int qk_l2norm;              // fused prologue: normalise every key row first
   int t_only;                 // write T itself instead of T diag(beta) (the backward's operand)
 };
@@ -109,7 +110,7 @@ __device__ __forceinline__ WyItem wy_locate(const WyParams& p, int item) {
     w.clen = rem < kChunk ? static_cast<int>(rem) : kChunk;
   } else {
     const unsigned s = xc / static_cast<unsigned>(p.chunks_per_seq);
-    const int c = static_cast<int>(xc - s * static_cast<unsigned>(p.chunks_per_seq));
+    const int c = p.chunk_begin + static_cast<int>(xc - s * static_cast<unsigned>(p.chunks_per_seq));
     const int rem = p.T - c * kChunk;
     w.row0 = static_cast<int64_t>(s) * p.T + c * kChunk;
     w.clen = rem < kChunk ? static_cast<int>(rem) : kChunk;

@@ -172,6 +172,38 @@ int gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float
                         void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
                         const gdn_strides_t* strides, const int32_t* cu_seqlens, void* stream);
 
+/* End-to-end prefill from page-locked host memory: gdn_prefill over inputs
+ * and outputs that live on the host. It has no counterpart in the GDN prefill
+ * op, which runs on device buffers; it exists for callers whose tensors are on
+ * the host, and is how the library measures its end-to-end throughput.
+ *   q, k, v, g, beta, h_state_inout, out, cu_seqlens : host buffers allocated
+ *             with cudaHostAlloc / cudaMallocHost or registered with
+ *             cudaHostRegister (else GDN_ERR_ARG), laid out as for gdn_prefill
+ *             with packed rows (strides NULL or equal to the packed widths) and
+ *             a contiguous state (state_is_table 0; else GDN_ERR_UNSUPPORTED).
+ *             qk_l2norm is honoured. cu_seqlens may be NULL (dense).
+ *   scratch : device buffer of gdn_prefill_host_scratch_bytes() bytes,
+ *             256-byte aligned, or NULL (the call then allocates and frees it
+ *             stream-ordered on `stream`).
+ * Enqueues on `stream` and returns: the copies in, the op and the copies out.
+ * A dense batch of at least 32 chunks per sequence that does not take the
+ * segment schedule is cut into 2-16 ranges of whole chunks, and the library
+ * pipelines them over two internal streams of its own: range i's rows are
+ * copied in, its WY solve and spine run on `stream` (the state carried from
+ * range to range on the device), and its output rows are copied out while
+ * range i + 1's rows come in. The results equal gdn_prefill's bit for bit.
+ * Every copy is ordered after the work already on `stream` when the call is
+ * made, and `stream` passes the call only after the last copy out, so the
+ * usual stream semantics hold: the host buffers must stay valid and unchanged
+ * (out and the state unread) until then. Numerics, errors and the device
+ * status word are as for gdn_prefill; gdn_last_launch_count counts the
+ * kernels (two per range). */
+size_t gdn_prefill_host_scratch_bytes(int B, int T, int nk, int nv, int dk, int dv, int varlen);
+int gdn_prefill_host(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                     void* h_state_inout, void* out, int B, int T, int nk, int nv, int dk, int dv,
+                     const gdn_strides_t* strides, const int32_t* cu_seqlens, void* scratch, size_t scratch_bytes,
+                     void* stream);
+
 /* Single-token decode step, the recurrent update that follows a prefill in
  * serving (same recurrence and state as gdn_prefill, one token per sequence):
  * for every sequence b and value head h, with kh = h / (nv / nk),

@@ -247,3 +247,46 @@ def test_binding_rejects_host_tensors_and_wrong_types(lib):
         gdn.prefill(q.float(), k, v, g, beta, state, out, nk=nk, nv=nv, B=1, T=rows)
     with pytest.raises(gdn.GdnError, match="got torch.float16"):
         gdn.prefill_noalloc(q.half(), k, v, g, beta, state, out, nk=nk, nv=nv, B=1, T=rows)
+
+
+def _call_host(lib, B=1, T=64, nk=1, nv=1, dk=128, dv=128, strides=None, ptr=16):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    st = ctypes.byref(strides) if strides is not None else None
+    rc = lib.gdn_prefill_host(p, p, p, p, p, p, p, B, T, nk, nv, dk, dv, st, None, None, 0, None)
+    return rc, lib.gdn_last_error().decode()
+
+
+def test_host_entry_point_rejects_before_any_device_call(lib):
+    # argument checks of gdn_prefill_host that run before it touches CUDA
+    import gated_delta_rule_17_gb300 as gdn
+
+    rc, msg = _call_host(lib, dk=64)
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "128" in msg
+    st = gdn.Strides(128, 128, 128, 1, 1, 128, 1, 0)  # a state table
+    rc, msg = _call_host(lib, strides=st)
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "contiguous state" in msg
+    st = gdn.Strides(256, 128, 128, 1, 1, 128, 0, 0)  # padded q rows
+    rc, msg = _call_host(lib, strides=st)
+    assert rc == gdn.GDN_ERR_UNSUPPORTED and "packed rows" in msg
+    assert _call_host(lib, ptr=0)[0] == gdn.GDN_ERR_ARG
+    assert _call_host(lib, B=0, ptr=0)[0] == gdn.GDN_OK
+    assert lib.gdn_last_launch_count() == 0
+
+
+def test_host_scratch_sizes(lib):
+    # packed staging of q, k, v, g, beta, the state and out (each 256-byte aligned),
+    # cu_seqlens for varlen batches, then the op's own workspace
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    B, T, nk, nv = 4, 8192, 16, 32
+    rows = B * T
+    qk, vo, gb, st = rows * nk * 256, rows * nv * 256, rows * nv * 4, B * nv * 128 * 128 * 4
+    dense = up(qk) * 2 + up(vo) + up(gb) * 2 + up(st) + up(vo)
+    assert lib.gdn_prefill_host_scratch_bytes(B, T, nk, nv, 128, 128, 0) == dense
+    B, T, nk, nv = 3, 405, 2, 4
+    parts = [T * nk * 256] * 2 + [T * nv * 256, T * nv * 4, T * nv * 4, B * nv * 128 * 128 * 4, T * nv * 256,
+                                  (B + 1) * 4]
+    want = sum(up(x) for x in parts) + lib.gdn_prefill_workspace_bytes(B, T, nv, 128, 128, 1)
+    assert lib.gdn_prefill_host_scratch_bytes(B, T, nk, nv, 128, 128, 1) == want
+    assert lib.gdn_prefill_host_scratch_bytes(B, T, nk, nv, 64, 128, 1) == 0
