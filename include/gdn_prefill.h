@@ -187,7 +187,7 @@ int gdn_prefill_noalloc(const void* q, const void* k, const void* v, const float
  *             stream-ordered on `stream`).
  * Enqueues on `stream` and returns: the copies in, the op and the copies out.
  * A dense batch of at least 32 chunks per sequence that does not take the
- * segment schedule is cut into 2-16 ranges of whole chunks, and the library
+ * segment schedule is cut into 2-8 ranges of whole chunks, and the library
  * pipelines them over two internal streams of its own: range i's rows are
  * copied in, its WY solve and spine run on `stream` (the state carried from
  * range to range on the device), and its output rows are copied out while
